@@ -1,0 +1,335 @@
+"""Pins of the fp64 oracle to facts other than itself (CPU only).
+
+Each test checks the oracle against a closed form, an exhaustive decode, a
+library routine computing the same mathematical object in another way, brute
+force on tiny inputs, or a hand-worked case from ``tests/golden``.  Together
+they catch a dropped term (eps, gamma, rstd), a wrong sign or index, a
+transposed operand, and the strict/non-strict comparisons of the sampler.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ------------------------------------------------------------------ widening (exhaustive)
+
+def _bf16_decode_ldexp(bits: int) -> float:
+    s = -1.0 if bits >> 15 else 1.0
+    e = (bits >> 7) & 0xFF
+    f = bits & 0x7F
+    if e == 0:
+        return s * math.ldexp(f, -133)           # subnormal: f * 2^-7 * 2^-126
+    if e == 255:
+        return s * math.inf if f == 0 else math.nan
+    return s * math.ldexp(128 + f, e - 134)       # (1 + f/128) * 2^(e-127)
+
+
+def test_widen_bf16_exhaustive():
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle.widen(bits, "bf16")
+    want = np.array([_bf16_decode_ldexp(int(b)) for b in bits])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    # sign of zero survives
+    assert math.copysign(1.0, got[0x8000]) == -1.0
+
+
+def test_widen_f16_exhaustive_against_numpy():
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle.widen(bits, "f16")
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert got[1] == 2.0 ** -24          # smallest subnormal
+    assert got[0x7BFF] == 65504.0        # largest finite
+
+
+def test_widen_f32_identity():
+    x = np.array([1.5, -0.0, 3.4028235e38, 1e-45], dtype=np.float32)
+    assert np.array_equal(oracle.widen(x, "f32"), x.astype(np.float64))
+
+
+# ------------------------------------------------------------------ RMSNorm scale
+
+@pytest.mark.parametrize("c", [1.0, 0.37, 25.0])
+def test_rstd_constant_row_closed_form(c):
+    H = 48
+    x = np.full((1, H), c, dtype=np.float32)
+    got = oracle.rstd(x, "f32", H, H, 1e-5, 1)[0]
+    c = float(np.float32(c))
+    assert got == pytest.approx(1.0 / math.sqrt(c * c + float(np.float32(1e-5))), rel=1e-14)
+
+
+def test_rstd_divides_by_hidden_actual_not_H():
+    # 24 active lanes of value 2, 8 zero pads (j % 16 == 15 style positions): mean is 4, not 3.
+    H, Hu = 32, 30
+    pads = gen.pad_lanes(H, Hu)
+    x = np.where(pads, 0.0, 2.0).astype(np.float32)[None, :]
+    got = oracle.rstd(x, "f32", H, Hu, 1e-5, 1)[0]
+    assert got == pytest.approx(1.0 / math.sqrt(4.0 + float(np.float32(1e-5))), rel=1e-14)
+
+
+def test_rstd_ignores_lanes_beyond_hidden_actual_when_not_zero_padded():
+    H, Hu = 32, 20
+    x = np.full((1, H), 3.0, dtype=np.float32)
+    x[0, Hu:] = 1000.0  # garbage lanes beyond H_u
+    got = oracle.rstd(x, "f32", H, Hu, 1e-5, 0)[0]
+    assert got == pytest.approx(1.0 / math.sqrt(9.0 + float(np.float32(1e-5))), rel=1e-14)
+
+
+def test_rstd_eps_dominates_tiny_rows():
+    x = np.full((1, 64), 1e-3, dtype=np.float64).astype(np.float32)
+    got = oracle.rstd(x, "f32", 64, 64, 1e-5, 1)[0]
+    ms = float(np.float32(1e-3)) ** 2
+    assert got == pytest.approx(1.0 / math.sqrt(ms + float(np.float32(1e-5))), rel=1e-13)
+    assert got < 1.0 / math.sqrt(float(np.float32(1e-5))) and got > 250.0
+
+
+# ------------------------------------------------------------------ lm_head logits
+
+def _tiny(B=3, H=32, V=40, dtype="f32", seed=5, **kw):
+    return gen.custom(B, H, V, 4, hidden_dtype=dtype, seed=seed, **kw)
+
+
+def test_logits_one_hot_columns_exact():
+    """W[h, v] = 1 when h == perm[v]: logit = rstd * x[perm[v]] * gamma[perm[v]] exactly."""
+    w = _tiny(B=2, H=16, V=48)
+    rng = np.random.default_rng(0)
+    perm = rng.integers(0, w.H, size=w.V)
+    W = np.zeros((w.H, w.V), dtype=np.uint16)
+    W[perm, np.arange(w.V)] = 0x3F80  # bf16 1.0
+    L = oracle.logits(w.hidden, "f32", w.gamma, W, w.H, 1e-5, 1)
+    r = oracle.rstd(w.hidden, "f32", w.H, w.H, 1e-5, 1)
+    x = w.hidden.astype(np.float64)
+    g = w.gamma.astype(np.float64)
+    want = r[:, None] * (x[:, perm] * g[perm][None, :])
+    assert np.array_equal(L, want)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_logits_match_numpy_matmul(dtype):
+    w = _tiny(B=4, H=64, V=96, dtype=dtype)
+    L = oracle.logits(w.hidden, dtype, w.gamma, w.w_t, w.H, w.eps, 1)
+    if dtype == "f32":
+        x = w.hidden.astype(np.float64)
+    elif dtype == "bf16":
+        x = gen.bf16_bits_to_f32(w.hidden).astype(np.float64)
+    else:
+        x = w.hidden.view(np.float16).astype(np.float64)
+    Wd = gen.bf16_bits_to_f32(w.w_t).astype(np.float64)
+    ms = (x * x).mean(axis=1)
+    rstd = 1.0 / np.sqrt(ms + float(np.float32(w.eps)))
+    want = ((x * w.gamma.astype(np.float64)[None, :]) @ Wd) * rstd[:, None]
+    np.testing.assert_allclose(L, want, rtol=1e-12, atol=1e-13)
+
+
+def test_logits_pad_invariance():
+    """Zero pad lanes in x, gamma and W change nothing: equal to the squeezed problem."""
+    H, Hu, V = 64, 60, 80
+    w = gen.custom(3, H, V, 4, hidden_dtype="f16", Hu=Hu, zero_pad=1, seed=9)
+    pads = gen.pad_lanes(H, Hu)
+    L = oracle.logits(w.hidden, "f16", w.gamma, w.w_t, Hu, w.eps, 1)
+    keep = ~pads
+    Ls = oracle.logits(np.ascontiguousarray(w.hidden[:, keep]), "f16",
+                       np.ascontiguousarray(w.gamma[keep]), np.ascontiguousarray(w.w_t[keep]),
+                       Hu, w.eps, 1)
+    np.testing.assert_allclose(L, Ls, rtol=1e-13, atol=1e-14)
+
+
+def test_logits_scale_relation_exact():
+    """Power-of-two row scales c are exact in fp32, so for every column
+    logit(c x) / logit(x) = c sqrt(ms + eps) / sqrt(c^2 ms + eps): eps must sit inside the
+    square root next to the mean of squares, and the mean must use H_u."""
+    w = _tiny(B=1, H=32, V=24, dtype="f32", seed=11)
+    x = w.hidden.astype(np.float64)
+    ms = float((x * x).mean())
+    e = float(np.float32(w.eps))
+    L1 = oracle.logits(w.hidden, "f32", w.gamma, w.w_t, w.H, w.eps, 1)
+    for c in (1024.0, 1.0 / 1024.0, 4.0):
+        xc = (w.hidden * np.float32(c)).astype(np.float32)
+        L2 = oracle.logits(xc, "f32", w.gamma, w.w_t, w.H, w.eps, 1)
+        want = c * math.sqrt(ms + e) / math.sqrt(c * c * ms + e)
+        np.testing.assert_allclose(L2 / L1, want, rtol=1e-12)
+
+
+def test_logits_sign_and_gamma_enter_linearly():
+    w = _tiny(B=2, H=32, V=16, seed=12)
+    L = oracle.logits(w.hidden, "f32", w.gamma, w.w_t, w.H, w.eps, 1)
+    Ln = oracle.logits((-w.hidden).astype(np.float32), "f32", w.gamma, w.w_t, w.H, w.eps, 1)
+    Lg = oracle.logits(w.hidden, "f32", (2 * w.gamma).astype(np.float32), w.w_t, w.H, w.eps, 1)
+    assert np.array_equal(Ln, -L)
+    np.testing.assert_allclose(Lg, 2 * L, rtol=1e-14, atol=0)
+
+
+def test_logits_zero_pad_off_ignores_weights_beyond_hidden_actual():
+    H, Hu, V = 32, 24, 16
+    w = _tiny(B=2, H=H, V=V, seed=13)
+    x = w.hidden.copy()
+    x[:, Hu:] = 7.0  # not part of the state
+    L = oracle.logits(x, "f32", w.gamma, w.w_t, Hu, w.eps, 0)
+    Ls = oracle.logits(np.ascontiguousarray(x[:, :Hu]), "f32", np.ascontiguousarray(w.gamma[:Hu]),
+                       np.ascontiguousarray(w.w_t[:Hu]), Hu, w.eps, 1)
+    np.testing.assert_allclose(L, Ls, rtol=1e-13, atol=1e-14)
+
+
+# ------------------------------------------------------------------ top-k
+
+def test_topk_matches_lexsort_brute_force():
+    rng = np.random.default_rng(1)
+    L = rng.standard_normal((5, 300))
+    L[1, 10:20] = L[1, 50]              # exact ties
+    L[2, :] = np.round(L[2, :], 1)      # many ties
+    vals, idx = oracle.topk(L, 37)
+    for b in range(L.shape[0]):
+        order = np.lexsort((np.arange(L.shape[1]), -L[b]))[:37]
+        assert np.array_equal(idx[b], order)
+        assert np.array_equal(vals[b], L[b, order])
+
+
+def test_topk_is_prefix_of_a_permutation_of_the_full_sort():
+    rng = np.random.default_rng(2)
+    L = rng.standard_normal((3, 257))
+    vals, idx = oracle.topk(L, 257)
+    for b in range(3):
+        assert sorted(idx[b].tolist()) == list(range(257))
+        assert np.all(np.diff(vals[b]) <= 0)
+    v16, i16 = oracle.topk(L, 16)
+    assert np.array_equal(i16, idx[:, :16])
+
+
+def test_topk_signed_zero_ties_by_index_and_infinities():
+    L = np.array([[0.0, -0.0, 1.0, -np.inf, np.inf, -0.0, 0.5]])
+    vals, idx = oracle.topk(L, 7)
+    assert idx[0].tolist() == [4, 2, 6, 0, 1, 5, 3]
+
+
+def test_topk_duplicated_columns_tie_exactly():
+    w = gen.custom(2, 64, 64, 8, hidden_dtype="bf16", seed=21, dup_cols=4)
+    L = oracle.logits(w.hidden, "bf16", w.gamma, w.w_t, w.H, w.eps, 1)
+    groups = L.reshape(2, 16, 4)
+    assert np.all(groups == groups[:, :, :1])
+    vals, idx = oracle.topk(L, 10)
+    # within each tie group the lower index comes first
+    for b in range(2):
+        for t in range(9):
+            if vals[b, t] == vals[b, t + 1]:
+                assert idx[b, t] < idx[b, t + 1]
+
+
+# ------------------------------------------------------------------ sampler
+
+def _parse_vals(s):
+    out = []
+    for tok in s.split(","):
+        tok = tok.strip()
+        if tok == "ln3":
+            out.append(math.log(3.0))
+        elif tok == "2ln3":
+            out.append(2 * math.log(3.0))
+        else:
+            out.append(float(tok))
+    return np.array(out)
+
+
+def _golden_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "sampler_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, vals, idx, params, want = [c.strip() for c in line.split("|")]
+            cases.append((name, _parse_vals(vals), np.array([int(i) for i in idx.split(",")]),
+                          np.array([float(p) for p in params.split()], dtype=np.float32),
+                          int(want)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c[0])
+def test_sampler_hand_worked(case):
+    name, vals, idx, p, want = case
+    assert oracle.sample_row(vals, idx, p).token == want
+
+
+def test_sampler_probabilities_are_scipy_softmax():
+    sp = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(3)
+    vals = np.sort(rng.standard_normal(64))[::-1].copy()
+    idx = np.arange(64)
+    for T, top_k, top_p in [(0.7, 0, 1.0), (1.3, 20, 1.0), (0.5, 0, 0.8), (2.0, 33, 0.6)]:
+        r = oracle.sample_row(vals, idx, np.array([top_k, top_p, T, 0.3], np.float32))
+        kk = r.kk
+        assert kk == (top_k if top_k >= 1 else 64)
+        p_kk = sp.softmax(vals[:kk] / np.float64(np.float32(T)))
+        np.testing.assert_allclose(r.pcum, np.cumsum(p_kk), rtol=1e-12, atol=1e-14)
+        assert abs(r.pcum[-1] - 1.0) < 1e-12
+        m = r.m
+        p_m = sp.softmax(vals[:m] / np.float64(np.float32(T)))
+        np.testing.assert_allclose(np.diff(np.concatenate([[0.0], r.cdf])), p_m, rtol=1e-12,
+                                   atol=1e-14)
+        assert abs(r.cdf[-1] - 1.0) < 1e-12
+        # m is the shortest prefix reaching top_p
+        if top_p < 1.0:
+            assert r.pcum[m - 1] >= np.float32(top_p)
+            assert m == 1 or r.pcum[m - 2] < np.float32(top_p)
+
+
+def test_sampler_u_sweep_hits_every_bucket():
+    rng = np.random.default_rng(4)
+    vals = np.sort(rng.standard_normal(16) * 0.5)[::-1].copy()
+    idx = np.arange(100, 116)
+    p = np.array([0, 1.0, 1.0, 0.0], np.float32)
+    r = oracle.sample_row(vals, idx, p)
+    edges = np.concatenate([[0.0], r.cdf])
+    seen = []
+    for j in range(r.m):
+        p[3] = np.float32(0.5 * (edges[j] + edges[j + 1]))
+        seen.append(oracle.sample_row(vals, idx, p).token)
+    assert seen == list(idx[: r.m])
+
+
+def test_sampler_u_zero_is_first_candidate():
+    rng = np.random.default_rng(5)
+    vals = np.sort(rng.standard_normal(32))[::-1].copy()
+    for T in (0.3, 1.0, 5.0):
+        r = oracle.sample_row(vals, np.arange(32), np.array([0, 1.0, T, 0.0], np.float32))
+        assert r.token == 0
+
+
+# ------------------------------------------------------------------ whole tail on tiny shapes
+
+def test_tail_composition_brute_force():
+    w = gen.custom(3, 48, 200, 12, hidden_dtype="bf16", seed=31)
+    L, tv, ti, toks = oracle.tail(w.hidden, "bf16", w.gamma, w.w_t, w.H, w.k, w.eps, 1, w.params)
+    x = gen.bf16_bits_to_f32(w.hidden).astype(np.float64)
+    Wd = gen.bf16_bits_to_f32(w.w_t).astype(np.float64)
+    rstd = 1.0 / np.sqrt((x * x).mean(1) + float(np.float32(w.eps)))
+    Lb = ((x * w.gamma.astype(np.float64)) @ Wd) * rstd[:, None]
+    np.testing.assert_allclose(L, Lb, rtol=1e-12, atol=1e-13)
+    for b in range(3):
+        order = np.lexsort((np.arange(w.V), -L[b]))[: w.k]
+        assert np.array_equal(ti[b], order)
+        assert toks[b] == oracle.sample_row(L[b, order], order, w.params[b]).token
+
+
+def test_tail_without_params_leaves_no_tokens():
+    w = gen.custom(2, 32, 64, 8, hidden_dtype="f32", seed=32)
+    out = oracle.tail(w.hidden, "f32", w.gamma, w.w_t, w.H, w.k, w.eps, 1, None)
+    assert out[3] is None
+
+
+def test_tiny_workload_shape_and_determinism():
+    a = gen.make("tiny")
+    b = gen.make("tiny")
+    assert a.hidden.shape == (1, 256) and a.w_t.shape == (256, 4096)
+    assert np.array_equal(a.w_t, b.w_t) and np.array_equal(a.hidden, b.hidden)
+    assert a.params.tolist() == [[16.0, pytest.approx(0.9), pytest.approx(0.7), 0.5]]
