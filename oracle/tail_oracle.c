@@ -299,8 +299,9 @@ int oracle_topk(const double *logits, int B, int V, int k, int nthreads, double 
  *
  * The page names the columns only.  The order of operations used here is the
  * standard nucleus-sampling one:
- *   1. kk = trunc(top_k); if kk < 1 or kk > n (the candidates kept), kk = n.
- *   2. temperature <= 0 or kk == 1: greedy, token = idx_0.
+ *   1. kk = trunc(top_k) when 1 <= top_k < n + 1 (n: the candidates kept),
+ *      else kk = n (the cut is disabled).
+ *   2. temperature <= 0 (or NaN) or kk == 1: greedy, token = idx_0.
  *   3. s_i = (l_i - l_0) / T, e_i = exp(s_i), Z = sum_{i<kk} e_i, p_i = e_i/Z.
  *   4. top_p >= 1: m = kk; otherwise m = the smallest j+1 with
  *      sum_{i<=j} p_i >= top_p (so top_p <= 0 keeps one candidate).
@@ -319,15 +320,17 @@ int oracle_sample_row(const double *vals, const int32_t *idx, int n, const float
     const double temp = (double)p4[2];
     const double u = ncols == 4 ? (double)p4[3] : 0.5;
 
-    long kk = (long)trunc(top_k);
-    if (!(top_k == top_k) || kk < 1 || kk > n) kk = n;
+    /* top_k outside [1, n] (and NaN) disables the cut; compared as a double so
+       that no out-of-range value is converted to an integer */
+    long kk = (top_k >= 1.0 && top_k < (double)n + 1.0) ? (long)trunc(top_k) : (long)n;
     if (cdf_out)
         for (int i = 0; i < n; ++i) cdf_out[i] = 0.0;
     if (pcum_out)
         for (int i = 0; i < n; ++i) pcum_out[i] = 0.0;
     if (kk_out) *kk_out = (int32_t)kk;
 
-    if (temp <= 0.0 || kk == 1) {
+    /* a temperature that is not positive (including NaN) means greedy */
+    if (!(temp > 0.0) || kk == 1) {
         *token = idx[0];
         if (m_out) *m_out = 1;
         if (cdf_out) cdf_out[0] = 1.0;

@@ -43,7 +43,7 @@ MUTANTS = [
      [lambda: _golden("temp2_u076")]),
     ("three_col_default_draw", "ncols == 4 ? (double)p4[3] : 0.5", "ncols == 4 ? (double)p4[3] : 0.0",
      [lambda: _golden("equal_3col")]),
-    ("top_k_off_by_one", "kk > n) kk = n;", "kk > n) kk = n;\n    else kk += 1;",
+    ("top_k_off_by_one", "? (long)trunc(top_k) : (long)n;", "? (long)trunc(top_k) + 1 : (long)n;",
      [lambda: _golden("unif8_k4_u09")]),
     ("bf16_widen_wrong_shift", "((uint32_t)bits) << 16", "((uint32_t)bits) << 15",
      [pins.test_widen_bf16_exhaustive]),
