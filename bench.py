@@ -1,0 +1,347 @@
+"""Benchmark of the decode sampling tail on GB300.
+
+One step = one whole tail (RMSNorm -> lm_head -> global top-k -> sampler) over
+one batch of the synthetic workload, inputs resident in HBM.  Default
+workload: the GPT-OSS-shaped decode tail (gbs=8, H=2880, V=201088, k=256,
+emit_logits off).  The bf16 weight (1.16 GB) is far larger than the 129 MB L2,
+so every step streams it from HBM; no L2 flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--emit]
+    python bench.py --impl reference ...   # the fp64 CPU oracle as the reference arm
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
+independent replica on its own GPU: the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tail µs/step & rows/s at H=2880,V=201088; achieved HBM GB/s vs peak"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gptoss_g8")
+    ap.add_argument("--emit", action="store_true", help="also write the fp32 logits (emit_logits on)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_bytes(w, emit: bool) -> dict:
+    """Bytes one step must move at minimum: W once, hidden, gamma, params, tokens, logits if emitted."""
+    s_in = 4 if w.hidden_dtype == "f32" else 2
+    lm_head = 2 * w.H * w.V + (4 * w.B * w.V if emit else 0)
+    step = lm_head + w.B * w.H * s_in + 4 * w.H + 16 * w.B + 4 * w.B
+    return {"lm_head": lm_head, "step": step}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_sampling_tail_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, emit: bool):
+    """DRAM bytes per lm_head launch from the committed ncu summary, when it matches these sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(f"{workload}{'_emit' if emit else ''}")
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_step(w, nthreads):
+    import oracle
+    oracle.tail(w.hidden, w.hidden_dtype, w.gamma, w.w_t, w.Hu, w.k, w.eps, w.zero_pad, w.params,
+                nthreads=nthreads)
+
+
+def cpu_baseline(w, budget_s=12.0, max_steps=20):
+    """The fp64 oracle as it stands on the host cores: whole steps until ~budget_s of CPU time."""
+    import oracle
+    nthreads = oracle.default_threads()
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_steps and time.perf_counter() - t_all < budget_s:
+        t0 = time.perf_counter()
+        cpu_oracle_step(w, nthreads)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.median(times)
+    return {"value": w.B / sec, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
+            "us_per_step": sec * 1e6,
+            "sample": f"{len(times)} whole steps of the {w.name} workload ({w.B} rows x V={w.V}), median"}
+
+
+def run_reference(args, w):
+    """Reference arm: the fp64 CPU oracle timed on the host cores (rank 0 only)."""
+    import oracle
+    nthreads = oracle.default_threads()
+    for _ in range(max(0, args.warmup if args.warmup < 2 else 1)):
+        cpu_oracle_step(w, nthreads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        cpu_oracle_step(w, nthreads)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = w.B * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "gbs": w.B, "H": w.H, "V": w.V, "k": w.k, "emit_logits": False,
+                   "hidden_dtype": w.hidden_dtype},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"{args.steps} whole steps of {w.name}"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import gen
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, gen.make(args.workload))
+        return
+
+    import numpy as np
+    import torch
+    import decode_sampling_tail_gb300 as dst
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    w = gen.make(args.workload)
+    emit = bool(args.emit)
+    from gen.torch_io import to_device
+    hidden, gamma, w_t, params = to_device(w, torch, str(dev))
+    tokens = torch.empty(w.B, dtype=torch.int32, device=dev)
+    logits = torch.empty((w.B, w.V), dtype=torch.float32, device=dev) if emit else None
+    t = dst.Tail(w.H, w.V, w.k, w.B, hidden_actual=w.Hu, eps=w.eps, hidden_dtype=w.hidden_dtype,
+                 zero_interleaved_pad=bool(w.zero_pad), device=local_rank)
+    stream = torch.cuda.Stream(dev)
+    passes = (w.B + t.info.rows_per_pass - 1) // t.info.rows_per_pass
+    launches_per_step = t.info.kernels_per_run * passes
+
+    def step():
+        t.run(hidden, gamma, w_t, params, out_tokens=tokens, out_logits=logits, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize(dev)
+    t.check()
+
+    # ---------------- timed region: K whole steps, events on the launching stream
+    clocks = ClockSampler(local_rank)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler come up before the timed region
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(args.steps):
+            step()
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    clock_rec = clocks.stop()
+    if dist:
+        dist.barrier()
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    t.check()
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    rows_s = w.B * args.steps * world / (total_ms / 1e3)
+
+    # ---------------- per-kernel device times (own loop: events between the kernels)
+    dst.tail_profile_enable(t.h, True)
+    with torch.cuda.stream(stream):
+        for _ in range(min(args.steps, 200 // max(1, passes))):
+            step()
+    kms, npass = dst.tail_profile_read(t.h)
+    dst.tail_profile_enable(t.h, False)
+    lm_ms = kms["lm_head"] / max(1, npass)
+    kshare = {k: v / max(1e-9, sum(kms.values())) for k, v in kms.items()}
+
+    # ---------------- end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        hid_h = torch.from_numpy(np.ascontiguousarray(w.hidden.view(np.int16) if w.hidden_dtype != "f32"
+                                                      else w.hidden)).pin_memory()
+        par_h = torch.from_numpy(np.ascontiguousarray(w.params)).pin_memory()
+        tok_h = torch.empty(w.B, dtype=torch.int32).pin_memory()
+        for _ in range(3):
+            t.run_host(hid_h, gamma, w_t, par_h, tok_h, stream=stream)
+        if dist:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            t.run_host(hid_h, gamma, w_t, par_h, tok_h, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        e2e_ms = max(e0.elapsed_time(e1), wall * 1e3)
+        if dist:
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        s_in = 4 if w.hidden_dtype == "f32" else 2
+        e2e = {"value": w.B * args.steps * world / (e2e_ms / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": w.B * w.H * s_in + w.B * 4 * 4, "d2h_bytes_per_step": w.B * 4,
+               "us_per_step": 1e3 * e2e_ms / args.steps, "api": "tail_run_host"}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        t.close()
+        return
+
+    pk, pk_kind = peaks()
+    ab = algorithmic_bytes(w, emit)
+    achieved = ab["lm_head"] / (lm_ms / 1e3) / 1e9
+    step_gbs = ab["step"] / (ms_step / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": rows_s, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
+        "us_per_step_p10": 1e3 * float(np.percentile(per_step, 10)),
+        "us_per_step_p90": 1e3 * float(np.percentile(per_step, 90)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generators, distributions of the named workload)",
+        "config": {"workload": w.name, "gbs": w.B, "H": w.H, "hidden_actual": w.Hu, "V": w.V, "k": w.k,
+                   "hidden_dtype": w.hidden_dtype, "emit_logits": emit,
+                   "arithmetic": "bf16 W x bf16 hi+lo activations, fp32 accumulate",
+                   "l2": "no flush: the 1.16 GB weight is larger than L2 and streams from HBM every step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "step_hbm_gbs": step_gbs,
+        "step_frac_of_spec_8tbs": step_gbs / SPEC_HBM_GBS,
+        "roofline": {"bound": "hbm", "kernel": "lmhead_gemv_kernel", "achieved": achieved,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "peak_kind": f"{pk_kind} copy bandwidth", "frac_of_spec_8tbs": achieved / SPEC_HBM_GBS,
+                     "algorithmic_bytes_per_launch": ab["lm_head"], "launch_us": lm_ms * 1e3,
+                     "traffic": ncu_traffic(w.name, emit)},
+        "kernel_us": {k: 1e3 * v / max(1, npass) for k, v in kms.items()},
+        "kernel_share": kshare,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clock_rec,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    t.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+"""GB300-native decode sampling tail: final RMSNorm -> bf16 lm_head -> global top-k -> sampler.
+
+Thin ctypes binding of ``libtail.so`` (C ABI declared in ``include/tail.h``).
+The functions below only marshal arguments: every step of the tail runs in
+the library's CUDA kernels.  There is no CPU fallback: importing works without
+the library, but creating a handle raises ``TailLibraryMissing`` when
+``libtail.so`` has not been built (``python -m decode_sampling_tail_gb300.build``
+or ``__graft_entry__.build()``).
+
+The operation follows "GPT-OSS Tail Chunked Megakernel Kernel API Reference"
+(function gpt_oss_tail_chunked_megakernel) on one GPU holding the whole
+vocabulary.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtail.so")
+
+TAIL_F32, TAIL_F16, TAIL_BF16 = 0, 1, 2
+TAIL_OK = 0
+TAIL_ERR_INVALID_ARG = -1
+TAIL_ERR_UNSUPPORTED = -2
+TAIL_ERR_CUDA = -3
+TAIL_ERR_OOM = -4
+TAIL_ERR_DEVICE = -5
+
+EXPORTS = ("tail_create", "tail_run", "tail_run_ex", "tail_run_host", "tail_check", "tail_get_info",
+           "tail_destroy", "tail_status_string", "tail_profile_enable", "tail_profile_read",
+           "tail_set_wait_limit")
+KERNELS = ("rms_rows", "lm_head", "merge1", "merge2_sample")
+
+
+class TailLibraryMissing(RuntimeError):
+    pass
+
+
+class TailError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class tail_config(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("hidden_actual", ctypes.c_int32), ("V", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("gbs_max", ctypes.c_int32), ("eps", ctypes.c_float),
+                ("hidden_dtype", ctypes.c_int32), ("zero_interleaved_pad", ctypes.c_int32),
+                ("deferred_rms", ctypes.c_int32)]
+
+
+class tail_info(ctypes.Structure):
+    _fields_ = [("num_sms", ctypes.c_int32), ("nslab", ctypes.c_int32), ("merge_groups", ctypes.c_int32),
+                ("lmhead_path", ctypes.c_int32), ("rows_per_pass", ctypes.c_int32),
+                ("kernels_per_run", ctypes.c_int32), ("scratch_bytes", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib(path: str | None = None):
+    """Loads libtail.so (raises TailLibraryMissing if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise TailLibraryMissing(f"{p} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(p)
+        P, i32 = ctypes.c_void_p, ctypes.c_int32
+        L.tail_create.argtypes = [ctypes.POINTER(tail_config), ctypes.c_int, ctypes.POINTER(P)]
+        L.tail_create.restype = ctypes.c_int
+        L.tail_run.argtypes = [P, P, P, P, P, i32, i32, P, P, P]
+        L.tail_run.restype = ctypes.c_int
+        L.tail_run_ex.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P, P]
+        L.tail_run_ex.restype = ctypes.c_int
+        L.tail_run_host.argtypes = [P, P, P, P, P, i32, i32, P, P, P]
+        L.tail_run_host.restype = ctypes.c_int
+        L.tail_check.argtypes = [P]
+        L.tail_check.restype = ctypes.c_int
+        L.tail_get_info.argtypes = [P, ctypes.POINTER(tail_info)]
+        L.tail_get_info.restype = ctypes.c_int
+        L.tail_destroy.argtypes = [P]
+        L.tail_destroy.restype = None
+        L.tail_profile_enable.argtypes = [P, ctypes.c_int]
+        L.tail_profile_enable.restype = ctypes.c_int
+        L.tail_profile_read.argtypes = [P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)]
+        L.tail_profile_read.restype = ctypes.c_int
+        L.tail_set_wait_limit.argtypes = [P, ctypes.c_uint64]
+        L.tail_set_wait_limit.restype = ctypes.c_int
+        L.tail_status_string.argtypes = [ctypes.c_int]
+        L.tail_status_string.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().tail_status_string(status).decode()
+    except TailLibraryMissing:
+        return "library missing"
+
+
+# ------------------------------------------------------------------ raw C-ABI mirrors (pointers as ints)
+
+def tail_create(cfg: tail_config, device: int = 0) -> int:
+    h = ctypes.c_void_p()
+    rc = lib().tail_create(ctypes.byref(cfg), device, ctypes.byref(h))
+    if rc != TAIL_OK:
+        raise TailError(rc, "tail_create")
+    return h.value
+
+
+def tail_run(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, stream) -> int:
+    return lib().tail_run(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, stream)
+
+
+def tail_run_ex(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt,
+                out_topk_vals_opt, out_topk_idx_opt, stream) -> int:
+    return lib().tail_run_ex(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt,
+                             out_topk_vals_opt, out_topk_idx_opt, stream)
+
+
+def tail_run_host(h, hidden_host, gamma, w_t, params_host, n_param_cols, gbs, out_tokens_host,
+                  out_logits_host_opt, stream) -> int:
+    return lib().tail_run_host(h, hidden_host, gamma, w_t, params_host, n_param_cols, gbs, out_tokens_host,
+                               out_logits_host_opt, stream)
+
+
+def tail_check(h) -> int:
+    return lib().tail_check(h)
+
+
+def tail_get_info(h) -> tail_info:
+    info = tail_info()
+    rc = lib().tail_get_info(h, ctypes.byref(info))
+    if rc != TAIL_OK:
+        raise TailError(rc, "tail_get_info")
+    return info
+
+
+def tail_profile_enable(h, enable: bool) -> int:
+    return lib().tail_profile_enable(h, int(enable))
+
+
+def tail_profile_read(h):
+    """Returns ({kernel name: summed ms}, passes recorded)."""
+    ms = (ctypes.c_float * 4)()
+    n = ctypes.c_int32()
+    rc = lib().tail_profile_read(h, ms, ctypes.byref(n))
+    if rc != TAIL_OK:
+        raise TailError(rc, "tail_profile_read")
+    return dict(zip(KERNELS, list(ms))), n.value
+
+
+def tail_set_wait_limit(h, ns: int) -> int:
+    return lib().tail_set_wait_limit(h, ctypes.c_uint64(ns))
+
+
+def tail_destroy(h) -> None:
+    if h:
+        lib().tail_destroy(h)
+
+
+# ------------------------------------------------------------------ torch convenience wrapper
+
+_DTYPES = {"f32": TAIL_F32, "f16": TAIL_F16, "bf16": TAIL_BF16}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class Tail:
+    """A tail handle bound to one device; tensors are torch CUDA tensors.
+
+    ``hidden`` is [gbs, H] (float32, float16 or bfloat16 matching ``hidden_dtype``;
+    uint16/int16 bit patterns are accepted for the 16-bit types), ``gamma`` [H]
+    float32, ``w_t`` [H, V] bfloat16 (or its int16 bits), ``params`` [gbs, 3|4]
+    float32 or None.
+    """
+
+    def __init__(self, H: int, V: int, k: int = 256, gbs_max: int = 64, *, hidden_actual: int = 0,
+                 eps: float = 1e-5, hidden_dtype: str = "bf16", zero_interleaved_pad: bool = True,
+                 deferred_rms: bool = True, device: int = 0):
+        self.cfg = tail_config(H, hidden_actual, V, k, gbs_max, eps, _DTYPES[hidden_dtype],
+                               int(zero_interleaved_pad), int(deferred_rms))
+        self.device = device
+        self.h = tail_create(self.cfg, device)
+        self.info = tail_get_info(self.h)
+
+    def close(self):
+        if self.h:
+            tail_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def _stream(self, stream):
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream(self.device)
+        return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+    def run(self, hidden, gamma, w_t, params=None, out_tokens=None, out_logits=None, out_topk_vals=None,
+            out_topk_idx=None, stream=None):
+        gbs = int(hidden.shape[0])
+        ncols = int(params.shape[1]) if params is not None else 4
+        rc = tail_run_ex(self.h, _ptr(hidden), _ptr(gamma), _ptr(w_t), _ptr(params), ncols, gbs,
+                         _ptr(out_tokens), _ptr(out_logits), _ptr(out_topk_vals), _ptr(out_topk_idx),
+                         self._stream(stream))
+        if rc != TAIL_OK:
+            raise TailError(rc, "tail_run_ex")
+        return out_tokens
+
+    def run_host(self, hidden_host, gamma, w_t, params_host=None, out_tokens_host=None,
+                 out_logits_host=None, stream=None):
+        """hidden_host / params_host / outputs are host (ideally pinned) tensors or numpy arrays."""
+        def hp(x):
+            if x is None:
+                return None
+            if hasattr(x, "data_ptr"):
+                return ctypes.c_void_p(x.data_ptr())
+            return x.ctypes.data_as(ctypes.c_void_p)
+        gbs = int(hidden_host.shape[0])
+        ncols = int(params_host.shape[1]) if params_host is not None else 4
+        rc = tail_run_host(self.h, hp(hidden_host), _ptr(gamma), _ptr(w_t), hp(params_host), ncols, gbs,
+                           hp(out_tokens_host), hp(out_logits_host), self._stream(stream))
+        if rc != TAIL_OK:
+            raise TailError(rc, "tail_run_host")
+        return out_tokens_host
+
+    def check(self):
+        rc = tail_check(self.h)
+        if rc != TAIL_OK:
+            raise TailError(rc, "tail_check")

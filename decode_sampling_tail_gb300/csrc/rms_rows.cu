@@ -1,0 +1,136 @@
+// Final RMSNorm of the tail ("GPT-OSS Tail Chunked Megakernel Kernel API
+// Reference", parameters `hidden_states`, `gamma`, `eps`, `hidden_actual`,
+// `zero_interleaved_pad`, `deferred_rms`).
+//
+// One CTA per batch row:
+//   1. widen the row exactly to fp32 (bf16 and fp16 are subsets of fp32);
+//   2. ss = sum of x^2 over the active lanes (all H lanes when the pads are
+//      zero, else lanes [0, H_u)); rstd = 1 / sqrt(ss / H_u + eps);
+//   3. a = x * gamma (deferred: rstd is applied to the GEMM output) or
+//      a = (x * rstd) * gamma (legacy form feeding the GEMM);
+//   4. split a = hi + lo into two bf16 values (hi = bf16(a), lo = bf16(a - hi))
+//      so the bf16 tensor-core GEMM keeps about 16 significant bits of the
+//      activation, and store both in mma.sync m16n8k16 A-fragment order:
+//      m-tile = 8 batch rows, fragment rows 0-7 are their hi parts, rows 8-15
+//      their lo parts.
+// Rows in [B, B_pad) are written as zeros so the last m-tile is complete.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tail {
+
+namespace {
+
+constexpr int RMS_THREADS = 256;
+
+template <int DT>
+__device__ __forceinline__ float load_widen(const void* p, int64_t i) {
+  if constexpr (DT == 0) {
+    return static_cast<const float*>(p)[i];
+  } else if constexpr (DT == 1) {
+    return __half2float(static_cast<const __half*>(p)[i]);
+  } else {
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+  }
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float v) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+}
+
+// Word offset of the (hi or lo) register pair holding k-columns (kk, kk+1) of
+// batch row g of m-tile mt in k-step ks.  kk is even.
+__device__ __forceinline__ int64_t pack_word(int ks, int mt, int n_mt, int g, int kk, int lo) {
+  const int lane = g * 4 + ((kk & 7) >> 1);
+  const int reg = (kk < 8 ? 0 : 2) + lo;
+  return ((static_cast<int64_t>(ks) * n_mt + mt) * 32 + lane) * 4 + reg;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(RMS_THREADS) rms_pack_kernel(RmsArgs a) {
+  pdl_wait();  // scratch is reused across steps: wait for the previous step to finish with it
+  pdl_launch_dependents();
+  __shared__ float red[RMS_THREADS / 32];
+  __shared__ float s_rstd;
+  const int b = blockIdx.x;
+  const int mt = b / MTILE_ROWS, g = b % MTILE_ROWS;
+  const int H = a.H;
+
+  if (b >= a.B) {  // padding rows of the last m-tile
+    for (int h2 = 2 * threadIdx.x; h2 < H; h2 += 2 * RMS_THREADS) {
+      a.apack[pack_word(h2 / KSTEP, mt, a.mt, g, h2 % KSTEP, 0)] = 0u;
+      a.apack[pack_word(h2 / KSTEP, mt, a.mt, g, h2 % KSTEP, 1)] = 0u;
+    }
+    if (threadIdx.x == 0) a.row_scale[b] = 0.f;
+    return;
+  }
+
+  const int64_t row = static_cast<int64_t>(b) * H;
+  const int active_end = a.zero_pad ? H : a.Hu;
+  float ss = 0.f;
+  for (int h = threadIdx.x; h < active_end; h += RMS_THREADS) {
+    const float v = load_widen<DT>(a.hidden, row + h);
+    ss = fmaf(v, v, ss);
+  }
+  // fixed-order reduction: xor butterfly in each warp, then warps in order
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < RMS_THREADS / 32; ++w) t += red[w];
+    s_rstd = 1.0f / sqrtf(t / static_cast<float>(a.Hu) + a.eps);
+  }
+  __syncthreads();
+  const float rstd = s_rstd;
+  const float pre = a.deferred ? 1.0f : rstd;
+
+  for (int h2 = 2 * threadIdx.x; h2 < H; h2 += 2 * RMS_THREADS) {
+    float v[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = h2 + j;
+      if (h < active_end) {
+        const float x = load_widen<DT>(a.hidden, row + h);
+        v[j] = (x * pre) * a.gamma[h];
+      } else {
+        v[j] = 0.f;
+      }
+    }
+    uint32_t hi[2], lo[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      hi[j] = bf16_bits(v[j]);
+      const float hif = __uint_as_float(hi[j] << 16);
+      lo[j] = bf16_bits(v[j] - hif);
+    }
+    const int ks = h2 / KSTEP, kk = h2 % KSTEP;
+    a.apack[pack_word(ks, mt, a.mt, g, kk, 0)] = hi[0] | (hi[1] << 16);
+    a.apack[pack_word(ks, mt, a.mt, g, kk, 1)] = lo[0] | (lo[1] << 16);
+  }
+  if (threadIdx.x == 0) a.row_scale[b] = a.deferred ? rstd : 1.0f;
+}
+
+}  // namespace
+
+cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B_pad);
+  cfg.blockDim = dim3(RMS_THREADS);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  switch (a.dtype) {
+    case 0: return cudaLaunchKernelEx(&cfg, rms_pack_kernel<0>, a);
+    case 1: return cudaLaunchKernelEx(&cfg, rms_pack_kernel<1>, a);
+    case 2: return cudaLaunchKernelEx(&cfg, rms_pack_kernel<2>, a);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace tail

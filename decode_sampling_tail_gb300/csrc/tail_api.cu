@@ -1,0 +1,476 @@
+// C ABI of the decode sampling tail: handle lifetime, argument validation,
+// scratch ownership and the launch sequence of one step
+//   rms_rows -> lm_head (+ stage-1 top-k) -> merge1 -> merge2 + sampler,
+// all on the caller's stream, chained with programmatic dependent launch.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/tail.h"
+#include "internal.h"
+
+using namespace tail;
+
+struct tail_s {
+  tail_config cfg;
+  int device;
+  int num_sms;
+  int max_smem;
+  int nslab;
+  int G;
+  int rows_pass;  // rows per lm_head pass
+  int64_t scratch_bytes;
+  // device scratch
+  uint32_t* apack;
+  float* row_scale;
+  uint32_t* cand_key;
+  int32_t* cand_idx;
+  float* logit_scratch;
+  uint32_t* m1_key;
+  int32_t* m1_idx;
+  int32_t* m1_cnt;
+  float* topk_val;
+  int32_t* topk_idx;
+  int* err;
+  // staging of tail_run_host
+  void* st_hidden;
+  float* st_params;
+  int32_t* st_tokens;
+  float* st_logits;
+  // wait bound of the kernels
+  uint64_t wait_limit_ns;
+  // per-kernel profiling
+  int prof_on;
+  int prof_n;
+  cudaEvent_t* prof_ev;  // [PROF_MAX][5]
+};
+
+static constexpr int PROF_MAX = 256;
+static constexpr int PROF_EV = 5;
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+int elem_bytes(int dtype) { return dtype == TAIL_F32 ? 4 : 2; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t n, int64_t* total) {
+  *p = nullptr;
+  if (n == 0) return cudaSuccess;
+  *total += static_cast<int64_t>(n * sizeof(T));
+  return cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T));
+}
+
+void free_all(tail_t* h) {
+  void* ptrs[] = {h->apack,    h->row_scale, h->cand_key,  h->cand_idx,   h->logit_scratch,
+                  h->m1_key,   h->m1_idx,    h->m1_cnt,    h->topk_val,   h->topk_idx,
+                  h->err,      h->st_hidden, h->st_params, h->st_tokens,  h->st_logits};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+}
+
+int validate_config(const tail_config* c) {
+  if (!c) return TAIL_ERR_INVALID_ARG;
+  const int Hu = c->hidden_actual <= 0 ? c->H : c->hidden_actual;
+  if (c->H <= 0 || c->V <= 0 || Hu < 1 || Hu > c->H) return TAIL_ERR_INVALID_ARG;
+  if (c->k < 1 || c->k > MAX_K || c->k > c->V) return TAIL_ERR_INVALID_ARG;
+  if (c->gbs_max < 1 || c->gbs_max > 4096) return TAIL_ERR_INVALID_ARG;
+  if (c->hidden_dtype < TAIL_F32 || c->hidden_dtype > TAIL_BF16) return TAIL_ERR_INVALID_ARG;
+  if (!(c->eps >= 0.0f)) return TAIL_ERR_INVALID_ARG;
+  if (c->H % KSTEP != 0 || c->V % 16 != 0) return TAIL_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(c->H) * c->V >= (int64_t(1) << 40)) return TAIL_ERR_UNSUPPORTED;
+  return TAIL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tail_status_string(int s) {
+  switch (s) {
+    case TAIL_OK: return "ok";
+    case TAIL_ERR_INVALID_ARG: return "invalid argument";
+    case TAIL_ERR_UNSUPPORTED: return "unsupported shape, dtype or device";
+    case TAIL_ERR_CUDA: return "CUDA runtime error";
+    case TAIL_ERR_OOM: return "out of device memory";
+    case TAIL_ERR_DEVICE: return "device-side error flag raised (bounded wait ran out)";
+    default: return "unknown status";
+  }
+}
+
+int tail_create(const tail_config* cfg, int device, tail_t** out) {
+  if (!out) return TAIL_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return TAIL_ERR_INVALID_ARG;
+  DeviceGuard guard(device);
+  if (!guard.ok) return TAIL_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return TAIL_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return TAIL_ERR_UNSUPPORTED;  // built for sm_103a only
+
+  tail_t* h = new (std::nothrow) tail_t();
+  if (!h) return TAIL_ERR_OOM;
+  memset(h, 0, sizeof(*h));
+  h->cfg = *cfg;
+  if (h->cfg.hidden_actual <= 0) h->cfg.hidden_actual = h->cfg.H;
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  h->max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
+  const int64_t npairs = cfg->V / 16;
+  // one slab per SM, at least 8 pairs (128 columns) per slab
+  int64_t nslab = npairs / 8;
+  if (nslab < 1) nslab = 1;
+  if (nslab > h->num_sms) nslab = h->num_sms;
+  h->nslab = static_cast<int>(nslab);
+  h->G = merge_groups(h->nslab, cfg->k);
+  if (h->G < 1) {
+    delete h;
+    return TAIL_ERR_UNSUPPORTED;
+  }
+  h->rows_pass = cfg->gbs_max < MAX_ROWS_PER_PASS ? cfg->gbs_max : MAX_ROWS_PER_PASS;
+  // every row count the passes can use must have a shared-memory plan
+  for (int B = 1; B <= h->rows_pass; ++B) {
+    if (!plan_gemv(B, cfg->H, cfg->V, cfg->k, h->nslab, h->max_smem).ok) {
+      delete h;
+      return TAIL_ERR_UNSUPPORTED;
+    }
+  }
+  if (merge2_smem_bytes(h->G, cfg->k) > static_cast<size_t>(h->max_smem) ||
+      merge1_smem_bytes(h->nslab, h->G, cfg->k) > static_cast<size_t>(h->max_smem)) {
+    delete h;
+    return TAIL_ERR_UNSUPPORTED;
+  }
+  if (prepare_gemv(h->max_smem) != cudaSuccess || prepare_merge(h->max_smem) != cudaSuccess) {
+    delete h;
+    return TAIL_ERR_CUDA;
+  }
+
+  const int R = h->rows_pass;
+  const int Rpad = ((R + 7) / 8) * 8 < 8 ? 8 : ((R + 7) / 8) * 8;
+  const int mt_max = Rpad / 8 <= 1 ? 1 : Rpad / 8 <= 2 ? 2 : Rpad / 8 <= 4 ? 4 : 8;
+  const size_t ksteps = cfg->H / KSTEP;
+  const size_t K = cfg->k;
+  int64_t tot = 0;
+  cudaError_t e = cudaSuccess;
+  e = e ? e : dalloc(&h->apack, ksteps * mt_max * APACK_TILE_BYTES / 4, &tot);
+  e = e ? e : dalloc(&h->row_scale, static_cast<size_t>(mt_max) * 8, &tot);
+  e = e ? e : dalloc(&h->cand_key, static_cast<size_t>(R) * h->nslab * K, &tot);
+  e = e ? e : dalloc(&h->cand_idx, static_cast<size_t>(R) * h->nslab * K, &tot);
+  e = e ? e : dalloc(&h->logit_scratch, static_cast<size_t>(R) * cfg->V, &tot);
+  e = e ? e : dalloc(&h->m1_key, static_cast<size_t>(R) * h->G * K, &tot);
+  e = e ? e : dalloc(&h->m1_idx, static_cast<size_t>(R) * h->G * K, &tot);
+  e = e ? e : dalloc(&h->m1_cnt, static_cast<size_t>(R) * h->G, &tot);
+  e = e ? e : dalloc(&h->topk_val, static_cast<size_t>(cfg->gbs_max) * K, &tot);
+  e = e ? e : dalloc(&h->topk_idx, static_cast<size_t>(cfg->gbs_max) * K, &tot);
+  e = e ? e : dalloc(&h->err, 1, &tot);
+  e = e ? e : dalloc(reinterpret_cast<uint8_t**>(&h->st_hidden),
+                     static_cast<size_t>(cfg->gbs_max) * cfg->H * elem_bytes(cfg->hidden_dtype), &tot);
+  e = e ? e : dalloc(&h->st_params, static_cast<size_t>(cfg->gbs_max) * 4, &tot);
+  e = e ? e : dalloc(&h->st_tokens, static_cast<size_t>(cfg->gbs_max), &tot);
+  if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(h->apack, 0, ksteps * mt_max * APACK_TILE_BYTES);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_all(h);
+    delete h;
+    cudaGetLastError();
+    return e == cudaErrorMemoryAllocation ? TAIL_ERR_OOM : TAIL_ERR_CUDA;
+  }
+  h->scratch_bytes = tot;
+  h->wait_limit_ns = DEFAULT_TIMEOUT_NS;
+  *out = h;
+  return TAIL_OK;
+}
+
+static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t,
+                    const float* params, int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits,
+                    float* out_topk_vals, int32_t* out_topk_idx, cudaStream_t stream) {
+  const tail_config& c = h->cfg;
+  const int K = c.k;
+  const int64_t npairs = c.V / 16;
+  cudaError_t e = cudaSuccess;
+  for (int r0 = 0; r0 < gbs && e == cudaSuccess; r0 += h->rows_pass) {
+    const int B = gbs - r0 < h->rows_pass ? gbs - r0 : h->rows_pass;
+    const GemvPlan plan = plan_gemv(B, c.H, c.V, K, h->nslab, h->max_smem);
+    cudaEvent_t* ev = (h->prof_on && h->prof_n < PROF_MAX) ? h->prof_ev + h->prof_n * PROF_EV : nullptr;
+    if (ev) {
+      ++h->prof_n;
+      cudaEventRecord(ev[0], stream);
+    }
+
+    RmsArgs ra;
+    ra.hidden = static_cast<const uint8_t*>(hidden) + static_cast<int64_t>(r0) * c.H * elem_bytes(c.hidden_dtype);
+    ra.dtype = c.hidden_dtype;
+    ra.gamma = gamma;
+    ra.B = B;
+    ra.mt = plan.mt;
+    ra.B_pad = plan.mt * MTILE_ROWS;
+    ra.H = c.H;
+    ra.Hu = c.hidden_actual;
+    ra.eps = c.eps;
+    ra.zero_pad = c.zero_interleaved_pad ? 1 : 0;
+    ra.deferred = c.deferred_rms ? 1 : 0;
+    ra.apack = h->apack;
+    ra.row_scale = h->row_scale;
+    e = launch_rms_pack(ra, stream);
+    if (e != cudaSuccess) break;
+    if (ev) cudaEventRecord(ev[1], stream);
+
+    GemvArgs ga;
+    ga.w = w_t;
+    ga.apack = reinterpret_cast<const uint8_t*>(h->apack);
+    ga.row_scale = h->row_scale;
+    ga.logits_out = out_logits ? out_logits + static_cast<int64_t>(r0) * c.V : nullptr;
+    ga.logits_out_ld = c.V;
+    ga.logits_scratch = h->logit_scratch;
+    ga.cand_key = h->cand_key;
+    ga.cand_idx = h->cand_idx;
+    ga.err = h->err;
+    ga.B = B;
+    ga.H = c.H;
+    ga.V = c.V;
+    ga.K = K;
+    ga.ksteps = c.H / KSTEP;
+    ga.mt = plan.mt;
+    ga.nslab = h->nslab;
+    ga.npairs = npairs;
+    ga.cb_pairs = plan.cb_pairs;
+    ga.pitch = plan.pitch;
+    ga.stage_bytes = plan.stage_bytes;
+    ga.nstages = plan.nstages;
+    ga.logits_in_smem = plan.logits_in_smem;
+    ga.max_slab_cols = plan.max_slab_cols;
+    ga.smem_bytes = plan.smem_bytes;
+    ga.timeout_ns = h->wait_limit_ns;
+    e = launch_gemv(ga, stream);
+    if (e != cudaSuccess) break;
+    if (ev) cudaEventRecord(ev[2], stream);
+
+    MergeArgs ma;
+    ma.cand_key = h->cand_key;
+    ma.cand_idx = h->cand_idx;
+    ma.m1_key = h->m1_key;
+    ma.m1_idx = h->m1_idx;
+    ma.m1_cnt = h->m1_cnt;
+    ma.topk_val = (out_topk_vals ? out_topk_vals : h->topk_val) + static_cast<int64_t>(r0) * K;
+    ma.topk_idx = (out_topk_idx ? out_topk_idx : h->topk_idx) + static_cast<int64_t>(r0) * K;
+    ma.topk_ld = K;
+    ma.params = params ? params + static_cast<int64_t>(r0) * ncols : nullptr;
+    ma.ncols = ncols;
+    ma.tokens = params ? out_tokens + r0 : nullptr;
+    ma.B = B;
+    ma.V = c.V;
+    ma.K = K;
+    ma.nslab = h->nslab;
+    ma.G = h->G;
+    ma.npairs = npairs;
+    ma.err = h->err;
+    e = launch_merge1(ma, stream);
+    if (e != cudaSuccess) break;
+    if (ev) cudaEventRecord(ev[3], stream);
+    e = launch_merge2_sample(ma, stream);
+    if (e == cudaSuccess && ev) cudaEventRecord(ev[4], stream);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return TAIL_ERR_CUDA;
+  }
+  return TAIL_OK;
+}
+
+static int validate_run(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t,
+                        const float* params, int32_t ncols, int32_t gbs, int32_t* out_tokens,
+                        const float* out_logits, const float* tv, const int32_t* ti) {
+  if (!h) return TAIL_ERR_INVALID_ARG;
+  if (gbs < 0 || gbs > h->cfg.gbs_max) return TAIL_ERR_INVALID_ARG;
+  if (gbs == 0) return TAIL_OK;
+  if (!hidden || !gamma || !w_t) return TAIL_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(w_t, 16) || !aligned(gamma, 4)) return TAIL_ERR_INVALID_ARG;
+  if (params) {
+    if (ncols != 3 && ncols != 4) return TAIL_ERR_INVALID_ARG;
+    if (!out_tokens || !aligned(params, 4) || !aligned(out_tokens, 4)) return TAIL_ERR_INVALID_ARG;
+  }
+  if (out_logits && !aligned(out_logits, 16)) return TAIL_ERR_INVALID_ARG;
+  if ((tv && !aligned(tv, 4)) || (ti && !aligned(ti, 4))) return TAIL_ERR_INVALID_ARG;
+  return TAIL_OK;
+}
+
+int tail_run_ex(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
+                int32_t n_param_cols, int32_t gbs, int32_t* out_tokens, float* out_logits_opt,
+                float* out_topk_vals_opt, int32_t* out_topk_idx_opt, void* stream) {
+  int rc = validate_run(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt,
+                        out_topk_vals_opt, out_topk_idx_opt);
+  if (rc || gbs == 0) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return TAIL_ERR_CUDA;
+  return run_impl(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt,
+                  out_topk_vals_opt, out_topk_idx_opt, static_cast<cudaStream_t>(stream));
+}
+
+int tail_run(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
+             int32_t n_param_cols, int32_t gbs, int32_t* out_tokens, float* out_logits_opt, void* stream) {
+  return tail_run_ex(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, nullptr,
+                     nullptr, stream);
+}
+
+int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const uint16_t* w_t,
+                  const float* params_host, int32_t n_param_cols, int32_t gbs, int32_t* out_tokens_host,
+                  float* out_logits_host_opt, void* stream) {
+  if (!h) return TAIL_ERR_INVALID_ARG;
+  if (gbs < 0 || gbs > h->cfg.gbs_max) return TAIL_ERR_INVALID_ARG;
+  if (gbs == 0) return TAIL_OK;
+  if (!hidden_host || (params_host && !out_tokens_host)) return TAIL_ERR_INVALID_ARG;
+  if (params_host && n_param_cols != 3 && n_param_cols != 4) return TAIL_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return TAIL_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const tail_config& c = h->cfg;
+  cudaError_t e = cudaSuccess;
+  if (out_logits_host_opt && !h->st_logits) {
+    e = cudaMalloc(reinterpret_cast<void**>(&h->st_logits), static_cast<size_t>(c.gbs_max) * c.V * 4);
+    if (e != cudaSuccess) {
+      h->st_logits = nullptr;
+      cudaGetLastError();
+      return TAIL_ERR_OOM;
+    }
+    h->scratch_bytes += static_cast<int64_t>(c.gbs_max) * c.V * 4;
+  }
+  const size_t hbytes = static_cast<size_t>(gbs) * c.H * elem_bytes(c.hidden_dtype);
+  e = cudaMemcpyAsync(h->st_hidden, hidden_host, hbytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && params_host)
+    e = cudaMemcpyAsync(h->st_params, params_host, static_cast<size_t>(gbs) * n_param_cols * 4,
+                        cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return TAIL_ERR_CUDA;
+  }
+  int rc = tail_run_ex(h, h->st_hidden, gamma, w_t, params_host ? h->st_params : nullptr, n_param_cols, gbs,
+                       h->st_tokens, out_logits_host_opt ? h->st_logits : nullptr, nullptr, nullptr, stream);
+  if (rc) return rc;
+  if (params_host)
+    e = cudaMemcpyAsync(out_tokens_host, h->st_tokens, static_cast<size_t>(gbs) * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && out_logits_host_opt)
+    e = cudaMemcpyAsync(out_logits_host_opt, h->st_logits, static_cast<size_t>(gbs) * c.V * 4,
+                        cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return TAIL_ERR_CUDA;
+  }
+  return TAIL_OK;
+}
+
+int tail_check(tail_t* h) {
+  if (!h) return TAIL_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return TAIL_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return TAIL_ERR_CUDA;
+  }
+  int flag = 0;
+  if (cudaMemcpy(&flag, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TAIL_ERR_CUDA;
+  if (flag != 0) {
+    cudaMemset(h->err, 0, sizeof(int));
+    cudaDeviceSynchronize();
+    return TAIL_ERR_DEVICE;
+  }
+  return TAIL_OK;
+}
+
+int tail_profile_enable(tail_t* h, int enable) {
+  if (!h) return TAIL_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return TAIL_ERR_CUDA;
+  if (enable && !h->prof_ev) {
+    h->prof_ev = static_cast<cudaEvent_t*>(calloc(PROF_MAX * PROF_EV, sizeof(cudaEvent_t)));
+    if (!h->prof_ev) return TAIL_ERR_OOM;
+    for (int i = 0; i < PROF_MAX * PROF_EV; ++i) {
+      if (cudaEventCreate(&h->prof_ev[i]) != cudaSuccess) {
+        cudaGetLastError();
+        return TAIL_ERR_CUDA;
+      }
+    }
+  }
+  h->prof_on = enable ? 1 : 0;
+  if (enable) h->prof_n = 0;
+  return TAIL_OK;
+}
+
+int tail_profile_read(tail_t* h, float* kernel_ms, int32_t* passes) {
+  if (!h || !kernel_ms || !passes) return TAIL_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return TAIL_ERR_CUDA;
+  for (int j = 0; j < PROF_EV - 1; ++j) kernel_ms[j] = 0.f;
+  for (int i = 0; i < h->prof_n; ++i) {
+    cudaEvent_t* ev = h->prof_ev + i * PROF_EV;
+    if (cudaEventSynchronize(ev[PROF_EV - 1]) != cudaSuccess) {
+      cudaGetLastError();
+      return TAIL_ERR_CUDA;
+    }
+    for (int j = 0; j < PROF_EV - 1; ++j) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, ev[j], ev[j + 1]) != cudaSuccess) {
+        cudaGetLastError();
+        return TAIL_ERR_CUDA;
+      }
+      kernel_ms[j] += ms;
+    }
+  }
+  *passes = h->prof_n;
+  return TAIL_OK;
+}
+
+int tail_set_wait_limit(tail_t* h, uint64_t ns) {
+  if (!h) return TAIL_ERR_INVALID_ARG;
+  h->wait_limit_ns = ns;
+  return TAIL_OK;
+}
+
+int tail_get_info(const tail_t* h, tail_info* out) {
+  if (!h || !out) return TAIL_ERR_INVALID_ARG;
+  out->num_sms = h->num_sms;
+  out->nslab = h->nslab;
+  out->merge_groups = h->G;
+  out->lmhead_path = 1;
+  out->rows_per_pass = h->rows_pass;
+  out->kernels_per_run = 4;
+  out->scratch_bytes = h->scratch_bytes;
+  return TAIL_OK;
+}
+
+void tail_destroy(tail_t* h) {
+  if (!h) return;
+  {
+    DeviceGuard guard(h->device);
+    cudaDeviceSynchronize();
+    free_all(h);
+    if (h->prof_ev) {
+      for (int i = 0; i < PROF_MAX * PROF_EV; ++i)
+        if (h->prof_ev[i]) cudaEventDestroy(h->prof_ev[i]);
+      free(h->prof_ev);
+    }
+  }
+  delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,174 @@
+/*
+ * decode_sampling_tail_gb300: the GPT-OSS decode sampling tail on one GB300.
+ *
+ * One call runs the whole tail for a batch of gbs rows:
+ *   final RMSNorm -> bf16 lm_head -> global top-k -> sampler -> one token per row.
+ *
+ * The operation is the one defined by "GPT-OSS Tail Chunked Megakernel Kernel
+ * API Reference" (nkilib.experimental.gpt_oss_tail, function
+ * gpt_oss_tail_chunked_megakernel): section "Background" names the four steps;
+ * the parameter entries `hidden_states`, `gamma`, `lm_head_weight_t`, `eps`,
+ * `hidden_actual`, `zero_interleaved_pad`, `k`, `emit_logits`,
+ * `sampling_params` and `deferred_rms` define the inputs, options and outputs
+ * mirrored below.  On one GPU the whole vocabulary is local (V_s = V), so the
+ * page's all-to-all, its bf16 logits mirror and the hop/row-ownership helpers
+ * have no counterpart here.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are caller-owned memory on the handle's device.  The
+ *     library owns only its scratch, sized at create time from gbs_max.
+ *   - Runs are asynchronous on the caller's stream (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).  No host synchronisation
+ *     happens except in tail_run_host, tail_check and tail_destroy.
+ *   - One run per handle at a time: concurrent runs on one handle share its
+ *     scratch and race.
+ *   - Every call returns TAIL_OK (0) or a negative tail_status.  Nothing
+ *     aborts, traps or prints.
+ */
+#ifndef DECODE_SAMPLING_TAIL_GB300_TAIL_H
+#define DECODE_SAMPLING_TAIL_GB300_TAIL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tail_s tail_t;
+
+/* Element type of `hidden` (parameter `hidden_states`: fp32, fp16 or bf16). */
+typedef enum { TAIL_F32 = 0, TAIL_F16 = 1, TAIL_BF16 = 2 } tail_dtype;
+
+typedef enum {
+  TAIL_OK = 0,
+  TAIL_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, bad size, gbs > gbs_max, bad n_param_cols */
+  TAIL_ERR_UNSUPPORTED = -2,  /* shape, dtype or device this build cannot run: caller falls back */
+  TAIL_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
+  TAIL_ERR_OOM = -4,          /* scratch allocation failed at create */
+  TAIL_ERR_DEVICE = -5        /* a kernel raised its error flag (a bounded wait ran out) */
+} tail_status;
+
+typedef struct {
+  int32_t H;                    /* stored hidden width: row length of hidden, rows of w_t; H % 16 == 0 */
+  int32_t hidden_actual;        /* H_u, the unpadded hidden; <= 0 means H; 1 <= H_u <= H */
+  int32_t V;                    /* vocabulary: columns of w_t; V % 16 == 0 */
+  int32_t k;                    /* candidates kept by the global top-k: 1 <= k <= min(V, 1024) */
+  int32_t gbs_max;              /* largest gbs a run may pass: 1 .. 4096 */
+  float eps;                    /* RMSNorm epsilon (1e-5 for GPT-OSS) */
+  int32_t hidden_dtype;         /* tail_dtype of hidden */
+  int32_t zero_interleaved_pad; /* 1: pad lanes are zero in hidden, gamma and w_t wherever they sit,
+                                      so all H lanes are summed; 0: lanes [H_u, H) are ignored */
+  int32_t deferred_rms;         /* 1 (default): rstd scales the GEMM output per row;
+                                   0: legacy form, (x * rstd) * gamma feeds the GEMM */
+} tail_config;
+
+/* Static facts about a handle, for benchmarks and tests. */
+typedef struct {
+  int32_t num_sms;          /* SMs of the device */
+  int32_t nslab;            /* vocabulary slabs = CTAs of the lm_head kernel */
+  int32_t merge_groups;     /* CTAs per row of the first merge stage */
+  int32_t lmhead_path;      /* 1: mma.sync skinny GEMM */
+  int32_t rows_per_pass;    /* rows one lm_head pass covers (larger gbs runs several passes) */
+  int32_t kernels_per_run;  /* kernel launches of one tail_run with gbs <= rows_per_pass */
+  int64_t scratch_bytes;    /* device scratch owned by the handle */
+} tail_info;
+
+/*
+ * Create a handle on CUDA device `device`; validates the config and allocates
+ * the scratch (activation pack, per-row scale, top-k candidates, logits
+ * staging, error flag).  The caller's current device is restored on return.
+ * Returns TAIL_ERR_INVALID_ARG for a bad config, TAIL_ERR_UNSUPPORTED when the
+ * device is not sm_103, TAIL_ERR_OOM when scratch cannot be allocated.
+ */
+int tail_create(const tail_config* cfg, int device, tail_t** out);
+
+/*
+ * One decode step of the tail.
+ *   hidden         [gbs, H] row-major, element type cfg.hidden_dtype, 16-byte aligned.
+ *                  16-bit inputs are widened exactly to fp32 (`hidden_states`).
+ *   gamma          [H] fp32 final RMSNorm weight (`gamma`).
+ *   w_t            [H, V] bf16 bit patterns, C-contiguous, V fastest (`lm_head_weight_t`),
+ *                  16-byte aligned.  Read once per step; never modified.
+ *   params         [gbs, n_param_cols] fp32 rows [top_k, top_p, temperature(, u)]
+ *                  (`sampling_params`), or NULL: the sampler is skipped and
+ *                  out_tokens is not written.  n_param_cols is 3 (u = 0.5) or 4.
+ *   gbs            rows in this call, 0 <= gbs <= gbs_max (0 is a no-op).
+ *   out_tokens     [gbs] int32 sampled vocabulary ids (may be NULL only if params is NULL).
+ *   out_logits_opt [gbs, V] fp32 logits, or NULL (`emit_logits` off).
+ * Inputs must not alias outputs.  Results are deterministic: repeated runs on
+ * the same inputs give bitwise-equal outputs.  NaN inputs are outside the
+ * method's domain (`skip_nan_fold`); +-inf logits are ordered normally.
+ */
+int tail_run(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t,
+             const float* params, int32_t n_param_cols, int32_t gbs, int32_t* out_tokens,
+             float* out_logits_opt, void* stream);
+
+/*
+ * tail_run plus the sorted global top-k (the analogue of the page's
+ * `debug_taps`, exposing the stage that feeds the sampler):
+ *   out_topk_vals_opt [gbs, k] fp32 logits in (value desc, index asc) order, or NULL;
+ *   out_topk_idx_opt  [gbs, k] int32 vocabulary ids in the same order, or NULL.
+ */
+int tail_run_ex(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t,
+                const float* params, int32_t n_param_cols, int32_t gbs, int32_t* out_tokens,
+                float* out_logits_opt, float* out_topk_vals_opt, int32_t* out_topk_idx_opt,
+                void* stream);
+
+/*
+ * End-to-end form for callers holding the per-step inputs in host memory:
+ * copies hidden_host [gbs, H] and params_host [gbs, n_param_cols] into
+ * handle-owned device staging, runs the tail on `stream`, copies the tokens
+ * (and the logits, when out_logits_host_opt is non-NULL) back to host memory
+ * and synchronises the stream before returning.  gamma and w_t stay device
+ * pointers (model weights are resident).  Pinned host buffers make the copies
+ * asynchronous; pageable ones work too.
+ */
+int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const uint16_t* w_t,
+                  const float* params_host, int32_t n_param_cols, int32_t gbs,
+                  int32_t* out_tokens_host, float* out_logits_host_opt, void* stream);
+
+/*
+ * Synchronises the handle's device work and reads the device error flag that
+ * kernels raise when a bounded wait runs out.  Returns TAIL_ERR_DEVICE (and
+ * clears the flag) if it was set, TAIL_ERR_CUDA on a sticky CUDA error, else
+ * TAIL_OK.
+ */
+int tail_check(tail_t* h);
+
+/*
+ * Per-kernel device timing, for benchmarks.  While enabled, every run records
+ * CUDA events on its stream before and after each of its kernel launches
+ * (this gives up the programmatic overlap between the kernels, so enable it
+ * only in a measuring loop of its own).  Enabling (again) starts a new
+ * record of up to 256 lm_head passes.
+ * tail_profile_read synchronises on the recorded events and returns, for the
+ * passes recorded since enabling, the summed device milliseconds of each
+ * kernel in kernel_ms[4] = {rms_rows, lm_head, merge1, merge2 + sampler} and
+ * their count in *passes.
+ */
+int tail_profile_enable(tail_t* h, int enable);
+int tail_profile_read(tail_t* h, float* kernel_ms, int32_t* passes);
+
+/*
+ * Bounds every device-side wait of later runs to `ns` nanoseconds of GPU
+ * global time (default 1e9).  A wait that runs out raises the device error
+ * flag, the kernel drains its copies in flight and returns, and tail_check
+ * reports TAIL_ERR_DEVICE.  A limit of 0 makes the first wait that is not
+ * already satisfied run out: the failure-path test uses it.
+ */
+int tail_set_wait_limit(tail_t* h, uint64_t ns);
+
+/* Fills *out with the handle's static facts. */
+int tail_get_info(const tail_t* h, tail_info* out);
+
+/* Frees the handle and its scratch after synchronising its device.  NULL is a no-op. */
+void tail_destroy(tail_t* h);
+
+/* Static string for a status code. */
+const char* tail_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DECODE_SAMPLING_TAIL_GB300_TAIL_H */

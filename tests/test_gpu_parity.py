@@ -1,0 +1,241 @@
+"""GPU parity of the CUDA tail (through the C ABI) against the fp64 oracle.
+
+Small shapes span several slabs, ragged slab widths and every batch template;
+the named workloads run at full size in the launch configuration the bench
+uses.  All inputs come from the seeded generators in ``gen``.
+"""
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from tests import tailcheck as tc
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import decode_sampling_tail_gb300 as dst  # noqa: E402
+
+
+def make_tail(w, gbs_max=None, **kw):
+    return dst.Tail(w.H, w.V, w.k, gbs_max or w.B, hidden_actual=w.Hu, eps=w.eps,
+                    hidden_dtype=w.hidden_dtype, zero_interleaved_pad=bool(w.zero_pad), **kw)
+
+
+def full_check(w, res, rows=None, params=None):
+    rows = np.arange(w.B) if rows is None else np.asarray(rows)
+    L, ov, oi = tc.oracle_rows(w, rows)
+    if res.logits is not None:
+        tc.check_logits(res.logits[rows], L)
+    tc.check_topk(res.topk_vals[rows], res.topk_idx[rows], L, ov, oi, w.k,
+                  None if res.logits is None else res.logits[rows])
+    p = w.params if params is None else params
+    return tc.check_tokens(res.tokens[rows], res.topk_vals[rows], res.topk_idx[rows], L, ov, oi, p[rows], w.k)
+
+
+# ------------------------------------------------------------------ small shapes
+
+SMALL = [
+    # B, H, V, k, dtype, Hu, zero_pad
+    (1, 256, 4096, 16, "f32", None, 1),
+    (3, 64, 2016, 40, "bf16", None, 1),
+    (5, 128, 1024, 200, "f16", None, 1),     # k above the slab width: whole slabs kept
+    (8, 96, 4800, 64, "bf16", 90, 1),        # zero pads at interleaved lanes
+    (9, 80, 3200, 33, "f32", 72, 0),         # lanes beyond hidden_actual ignored
+    (16, 160, 6400, 128, "bf16", None, 1),
+    (17, 64, 2048, 17, "f16", None, 1),
+    (33, 48, 1600, 50, "bf16", None, 1),
+    (64, 64, 2400, 256, "bf16", None, 1),
+    (70, 32, 1024, 8, "f32", None, 1),       # two lm_head passes
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: f"B{s[0]}_H{s[1]}_V{s[2]}_k{s[3]}_{s[4]}")
+def test_small_shapes_match_oracle(shape):
+    B, H, V, k, dt, Hu, zp = shape
+    w = gen.custom(B, H, V, k, hidden_dtype=dt, Hu=Hu, zero_pad=zp, seed=1000 + B)
+    if Hu is not None and not zp:
+        # garbage beyond hidden_actual must be ignored
+        if dt == "f32":
+            w.hidden[:, Hu:] = 3.0
+        else:
+            w.hidden[:, Hu:] = 0x4040
+    with make_tail(w) as t:
+        res = tc.run_gpu(t, w, torch)
+    exact, exempt = full_check(w, res)
+    assert exact + exempt == B and exact >= B - max(1, B // 8)
+
+
+@pytest.mark.parametrize("ncols", ["3col", "none"])
+def test_param_column_forms(ncols):
+    w = gen.custom(6, 64, 2048, 32, hidden_dtype="bf16", seed=77)
+    with make_tail(w) as t:
+        res = tc.run_gpu(t, w, torch, params=ncols)
+    if ncols == "none":
+        assert np.all(res.tokens == -7), "tokens written although params is NULL"
+        L, ov, oi = tc.oracle_rows(w, np.arange(w.B))
+        tc.check_topk(res.topk_vals, res.topk_idx, L, ov, oi, w.k, res.logits)
+    else:
+        exact, exempt = full_check(w, res, params=w.params[:, :3])
+        assert exact >= 5
+
+
+def test_legacy_rms_realization_matches_oracle():
+    w = gen.custom(8, 256, 8192, 64, hidden_dtype="bf16", seed=55)
+    with make_tail(w, deferred_rms=False) as t:
+        legacy = tc.run_gpu(t, w, torch)
+    with make_tail(w) as t:
+        deferred = tc.run_gpu(t, w, torch)
+    full_check(w, legacy)
+    assert np.max(np.abs(legacy.logits - deferred.logits)) < 1e-5
+
+
+def test_sixteen_bit_input_equals_prewidened_fp32():
+    w16 = gen.custom(8, 128, 4096, 64, hidden_dtype="bf16", seed=56)
+    w32 = gen.custom(8, 128, 4096, 64, hidden_dtype="bf16", seed=56)
+    w32.hidden = gen.bf16_bits_to_f32(w16.hidden)
+    w32.hidden_dtype = "f32"
+    with make_tail(w16) as t:
+        a = tc.run_gpu(t, w16, torch)
+    with make_tail(w32) as t:
+        b = tc.run_gpu(t, w32, torch)
+    assert np.array_equal(a.logits.view(np.uint32), b.logits.view(np.uint32))
+    assert np.array_equal(a.topk_idx, b.topk_idx) and np.array_equal(a.tokens, b.tokens)
+
+
+def test_repeat_runs_bitwise_identical_and_rows_independent_of_batch():
+    w = gen.custom(8, 128, 4096, 64, hidden_dtype="bf16", seed=57)
+    with make_tail(w) as t:
+        r1 = tc.run_gpu(t, w, torch)
+        r2 = tc.run_gpu(t, w, torch)
+    assert np.array_equal(r1.logits.view(np.uint32), r2.logits.view(np.uint32))
+    assert np.array_equal(r1.tokens, r2.tokens) and np.array_equal(r1.topk_idx, r2.topk_idx)
+    for nb in (1, 4):
+        sub = gen.custom(8, 128, 4096, 64, hidden_dtype="bf16", seed=57)
+        sub.hidden = np.ascontiguousarray(w.hidden[:nb])
+        sub.params = np.ascontiguousarray(w.params[:nb])
+        sub.B = nb
+        with make_tail(sub) as t:
+            rs = tc.run_gpu(t, sub, torch)
+        assert np.array_equal(rs.logits.view(np.uint32), r1.logits[:nb].view(np.uint32))
+        assert np.array_equal(rs.tokens, r1.tokens[:nb])
+
+
+def test_outputs_untouched_outside_their_rows():
+    w = gen.custom(5, 64, 2048, 32, hidden_dtype="bf16", seed=58)
+    hidden, gamma, w_t, p = tc.to_device(w, torch)
+    dev = hidden.device
+    guard = 4096
+    tok = torch.full((w.B + 2 * guard,), 12345, dtype=torch.int32, device=dev)
+    lg = torch.full((w.B * w.V + 2 * guard,), 7.5, dtype=torch.float32, device=dev)
+    with make_tail(w) as t:
+        t.run(hidden, gamma, w_t, p, out_tokens=tok[guard:guard + w.B],
+              out_logits=lg[guard:guard + w.B * w.V].view(w.B, w.V))
+        torch.cuda.synchronize()
+    tok_h, lg_h = tok.cpu().numpy(), lg.cpu().numpy()
+    assert np.all(tok_h[:guard] == 12345) and np.all(tok_h[guard + w.B:] == 12345)
+    assert np.all(lg_h[:guard] == 7.5) and np.all(lg_h[guard + w.B * w.V:] == 7.5)
+
+
+def test_host_entry_point_matches_device_entry_point():
+    w = gen.custom(4, 64, 2048, 32, hidden_dtype="bf16", seed=59)
+    hidden, gamma, w_t, p = tc.to_device(w, torch)
+    with make_tail(w) as t:
+        dev = tc.run_gpu(t, w, torch, dev_tensors=(hidden, gamma, w_t, p))
+        toks = np.zeros(w.B, np.int32)
+        logits = np.zeros((w.B, w.V), np.float32)
+        t.run_host(w.hidden, gamma, w_t, w.params, toks, logits)
+    assert np.array_equal(toks, dev.tokens)
+    assert np.array_equal(logits.view(np.uint32), dev.logits.view(np.uint32))
+
+
+def test_invalid_arguments_return_status_codes():
+    w = gen.custom(4, 64, 2048, 32, hidden_dtype="bf16", seed=60)
+    hidden, gamma, w_t, p = tc.to_device(w, torch)
+    tok = torch.zeros(8, dtype=torch.int32, device=hidden.device)
+    with make_tail(w) as t:
+        s = t._stream(None)
+        P = dst._ptr
+        # gbs beyond gbs_max
+        assert dst.tail_run(t.h, P(hidden), P(gamma), P(w_t), P(p), 4, 5, P(tok), None, s) == dst.TAIL_ERR_INVALID_ARG
+        # bad column count
+        assert dst.tail_run(t.h, P(hidden), P(gamma), P(w_t), P(p), 5, 4, P(tok), None, s) == dst.TAIL_ERR_INVALID_ARG
+        # misaligned weight pointer
+        bad = hidden.view(torch.int16)[1:]
+        assert dst.tail_run(t.h, P(hidden), P(gamma), P(bad), P(p), 4, 4, P(tok), None, s) == dst.TAIL_ERR_INVALID_ARG
+        # params without tokens
+        assert dst.tail_run(t.h, P(hidden), P(gamma), P(w_t), P(p), 4, 4, None, None, s) == dst.TAIL_ERR_INVALID_ARG
+        # gbs == 0 is a no-op
+        assert dst.tail_run(t.h, None, None, None, None, 4, 0, None, None, s) == dst.TAIL_OK
+        assert dst.tail_check(t.h) == dst.TAIL_OK
+    bad_cfg = dst.tail_config(100, 0, 2048, 32, 4, 1e-5, 2, 1, 1)  # H % 16 != 0
+    with pytest.raises(dst.TailError) as ei:
+        dst.tail_create(bad_cfg, 0)
+    assert ei.value.status == dst.TAIL_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ named workloads at full size
+
+@pytest.fixture(scope="module")
+def g8():
+    return gen.make("gptoss_g8")
+
+
+@pytest.mark.parametrize("emit", [True, False], ids=["emit_on", "emit_off"])
+def test_gptoss_g8_full(g8, emit):
+    with make_tail(g8) as t:
+        res = tc.run_gpu(t, g8, torch, emit=emit)
+        # emit on and off produce the same top-k and tokens
+        other = tc.run_gpu(t, g8, torch, emit=not emit)
+    assert np.array_equal(res.topk_idx, other.topk_idx) and np.array_equal(res.tokens, other.tokens)
+    exact, exempt = full_check(g8, res if emit else other)
+    assert exact >= 7
+
+
+def test_tiny_full():
+    w = gen.make("tiny")
+    with make_tail(w) as t:
+        res = tc.run_gpu(t, w, torch)
+    exact, exempt = full_check(w, res)
+    assert exact == 1
+
+
+def test_padded_g64_full():
+    w = gen.make("padded_g64")
+    with make_tail(w) as t:
+        res = tc.run_gpu(t, w, torch)
+    exact, exempt = full_check(w, res)
+    assert exact >= 60
+    greedy = np.arange(w.B) % 4 == 0
+    assert np.all(res.tokens[greedy] == res.topk_idx[greedy, 0])
+
+
+def test_adversarial_g32_full():
+    w = gen.make("adversarial_g32")
+    with make_tail(w) as t:
+        res = tc.run_gpu(t, w, torch)
+    # duplicated columns give bitwise-equal fp32 logits
+    groups = res.logits.view(np.uint32).reshape(w.B, -1, 4)
+    assert np.all(groups == groups[:, :, :1])
+    exact, exempt = full_check(w, res)
+    assert exact >= 28
+    # u = 0.0 always draws the first candidate
+    even = np.arange(w.B) % 2 == 0
+    assert np.all(res.tokens[even] == res.topk_idx[even, 0])
+
+
+def test_large_g1024_sampled_rows():
+    w = gen.make("large_g1024")
+    with make_tail(w, gbs_max=1024) as t:
+        res = tc.run_gpu(t, w, torch)
+    rows = np.unique(np.concatenate([np.arange(0, 1024, 97), [1, 63, 64, 511, 1023]]))
+    exact, exempt = full_check(w, res, rows=rows)
+    assert exact >= len(rows) - 2
+    # properties that hold at any size, on every row
+    assert np.all(np.diff(res.topk_vals, axis=1) <= 0)
+    assert np.all((res.tokens >= 0) & (res.tokens < w.V))
+    top1 = np.argmax(res.logits, axis=1)
+    assert np.array_equal(res.topk_idx[:, 0], top1)
