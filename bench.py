@@ -323,7 +323,7 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "step_hbm_gbs": step_gbs,
         "step_frac_of_spec_8tbs": step_gbs / SPEC_HBM_GBS,
-        "roofline": {"bound": "hbm", "kernel": "lmhead_gemv_kernel", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "lmhead_tail_kernel", "achieved": achieved,
                      "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                      "peak_kind": f"{pk_kind} copy bandwidth", "frac_of_spec_8tbs": achieved / SPEC_HBM_GBS,
                      "algorithmic_bytes_per_launch": ab["lm_head"], "launch_us": lm_ms * 1e3,

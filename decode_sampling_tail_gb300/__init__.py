@@ -29,8 +29,8 @@ TAIL_ERR_DEVICE = -5
 
 EXPORTS = ("tail_create", "tail_run", "tail_run_ex", "tail_run_host", "tail_check", "tail_get_info",
            "tail_destroy", "tail_status_string", "tail_profile_enable", "tail_profile_read",
-           "tail_set_wait_limit")
-KERNELS = ("rms_rows", "lm_head", "merge1", "merge2_sample")
+           "tail_set_wait_limit", "tail_debug_drop_stage", "tail_last_error")
+KERNELS = ("rms_rows", "lm_head")
 
 
 class TailLibraryMissing(RuntimeError):
@@ -40,7 +40,13 @@ class TailLibraryMissing(RuntimeError):
 class TailError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {status_string(status)} ({status})")
+        detail = ""
+        if status in (TAIL_ERR_CUDA, TAIL_ERR_OOM):
+            try:
+                detail = " [" + lib().tail_last_error().decode() + "]"
+            except TailLibraryMissing:
+                pass
+        super().__init__(f"{what}: {status_string(status)} ({status}){detail}")
 
 
 class tail_config(ctypes.Structure):
@@ -91,6 +97,10 @@ def lib(path: str | None = None):
         L.tail_profile_read.restype = ctypes.c_int
         L.tail_set_wait_limit.argtypes = [P, ctypes.c_uint64]
         L.tail_set_wait_limit.restype = ctypes.c_int
+        L.tail_debug_drop_stage.argtypes = [P, ctypes.c_int32]
+        L.tail_debug_drop_stage.restype = ctypes.c_int
+        L.tail_last_error.argtypes = []
+        L.tail_last_error.restype = ctypes.c_char_p
         L.tail_status_string.argtypes = [ctypes.c_int]
         L.tail_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -148,7 +158,7 @@ def tail_profile_enable(h, enable: bool) -> int:
 
 def tail_profile_read(h):
     """Returns ({kernel name: summed ms}, passes recorded)."""
-    ms = (ctypes.c_float * 4)()
+    ms = (ctypes.c_float * len(KERNELS))()
     n = ctypes.c_int32()
     rc = lib().tail_profile_read(h, ms, ctypes.byref(n))
     if rc != TAIL_OK:
@@ -158,6 +168,10 @@ def tail_profile_read(h):
 
 def tail_set_wait_limit(h, ns: int) -> int:
     return lib().tail_set_wait_limit(h, ctypes.c_uint64(ns))
+
+
+def tail_debug_drop_stage(h, iteration: int) -> int:
+    return lib().tail_debug_drop_stage(h, iteration)
 
 
 def tail_destroy(h) -> None:

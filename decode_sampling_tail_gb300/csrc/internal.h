@@ -12,9 +12,13 @@ constexpr int APACK_TILE_BYTES = 512;  // one 16x16 bf16 A fragment set: 32 lane
 constexpr int MAX_ROWS_PER_PASS = 64;  // rows one lm_head pass covers (mt <= 8)
 constexpr int GEMV_CONSUMER_WARPS = 8;
 constexpr int GEMV_THREADS = (GEMV_CONSUMER_WARPS + 1) * 32;
-constexpr int HIST_BINS = 2048;      // radix digit histogram of the selections (11-bit digits)
+constexpr int GEMV_KPB = 2;          // ring stage = 32 rows of W
+constexpr int GEMV_MAX_STAGES = 8;
 constexpr int MAX_K = 1024;
-constexpr int MERGE_THREADS = 256;
+constexpr int MAX_SLABS = 160;       // vocabulary slabs (lm_head CTAs) at most
+constexpr int TAIL_PUB_PER_SLAB = 4; // lane maxima each (row, slab) publishes for the global bound
+constexpr int PHASE_C_CAP = 16384;   // candidates of one row held in shared memory at once
+constexpr int RANK_SORT_MAX = 640;   // up to this many candidates phase C ranks them all directly
 constexpr uint64_t DEFAULT_TIMEOUT_NS = 1000000000ull;  // 1 s bound on every device wait
 
 // Slab c of nslab covers column pairs [pair_lo(c), pair_lo(c+1)) of V/16 pairs.
@@ -42,53 +46,50 @@ struct GemvArgs {
   float* logits_out;        // [B, V] caller logits for this pass, or null
   int64_t logits_out_ld;    // row stride of logits_out in floats
   float* logits_scratch;    // [B, V] staging when the slab logits do not fit in shared memory
-  uint32_t* cand_key;       // [B][nslab][K] order keys
-  int32_t* cand_idx;        // [B][nslab][K] vocabulary ids
+  uint32_t* pub;            // [B][nslab][TAIL_PUB_PER_SLAB] published lane maxima
+  uint32_t* cand_key;       // [B][nslab][K] order keys of the emitted candidates
+  int32_t* cand_idx;        // [B][nslab][K] their vocabulary ids
+  int32_t* cand_cnt;        // [B][nslab] candidates emitted per (row, slab)
+  unsigned long long* bar;  // grid barrier arrival counter (grows monotonically)
+  float* topk_val;          // [B][topk_ld] sorted top-k logits
+  int32_t* topk_idx;        // [B][topk_ld] their vocabulary ids
+  int64_t topk_ld;
+  const float* params;      // [B][ncols] sampling parameters, or null
+  int ncols;
+  int32_t* tokens;          // [B], or null
   int* err;
   int B, H, V, K, ksteps, mt, nslab;
   int64_t npairs;
   int cb_pairs;             // column-block width in 16-column pairs
+  int kpb;                  // k-steps of 16 rows per ring stage
   int pitch;                // shared-memory row pitch of a W stage, bytes
   int stage_bytes, nstages;
   int logits_in_smem;
   int max_slab_cols;
   int smem_bytes;
+  int capc;                 // phase C candidate capacity (shared memory)
+  int sortP;                // composite buffer entries: max(next power of two >= K, RANK_SORT_MAX)
   uint64_t timeout_ns;
+  int drop_iter;            // test hook: ring iteration the producer never issues (-1: none)
 };
 
-struct MergeArgs {
-  const uint32_t* cand_key;  // stage-1 output
-  const int32_t* cand_idx;
-  uint32_t* m1_key;          // [B][G][K]
-  int32_t* m1_idx;
-  int32_t* m1_cnt;           // [B][G]
-  float* topk_val;           // [B][K] sorted output (caller or scratch)
-  int32_t* topk_idx;
-  int64_t topk_ld;           // row stride of topk outputs
-  const float* params;       // [B][ncols] or null
-  int ncols;
-  int32_t* tokens;           // [B] or null
-  int B, V, K, nslab, G;
-  int64_t npairs;
-  int* err;
-};
-
-// Launchers (all enqueue on `stream` with programmatic dependent launch).
+// Launchers (all enqueue on `stream`; the lm_head tail is a cooperative launch,
+// chained to the RMSNorm kernel with programmatic dependent launch when pdl).
 cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream);
-cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t stream);
-cudaError_t prepare_gemv(int max_smem);  // per device: opt the lm_head kernels into max_smem bytes
-cudaError_t prepare_merge(int max_smem);
-cudaError_t launch_merge1(const MergeArgs& a, cudaStream_t stream);
-cudaError_t launch_merge2_sample(const MergeArgs& a, cudaStream_t stream);
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t stream, bool pdl);
+// per device: opt the lm_head kernels into the largest dynamic shared memory
+// the opt-in limit leaves after their static shared memory
+cudaError_t prepare_gemv(int max_smem_optin, int* max_dynamic);
 
 // Shared-memory plan of the lm_head kernel for a pass of B rows.
 struct GemvPlan {
-  int mt, pw, cb_pairs, pitch, stage_bytes, nstages, logits_in_smem, max_slab_cols, smem_bytes;
+  int mt, pw, cb_pairs, pitch, kpb, stage_bytes, nstages, logits_in_smem, max_slab_cols, smem_bytes;
+  int capc, sortP;
   bool ok;
 };
-GemvPlan plan_gemv(int B, int H, int V, int K, int nslab, int max_smem);
-int merge_groups(int nslab, int K);
-size_t merge1_smem_bytes(int nslab, int G, int K);
-size_t merge2_smem_bytes(int G, int K);
+// kpb: k-steps per ring stage (1 or 2); max_stages caps the ring depth
+GemvPlan plan_gemv(int B, int H, int V, int K, int nslab, int max_smem, int kpb = GEMV_KPB,
+                   int max_stages = GEMV_MAX_STAGES);
+constexpr int SEL_NPL = 48;          // register keys per lane of the slab selects: slabs up to 1536 columns
 
 }  // namespace tail

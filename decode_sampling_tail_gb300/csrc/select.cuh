@@ -1,4 +1,4 @@
-// Exact top-k selection by radix select on order-preserving 32-bit keys.
+// Exact top-k selection on order-preserving 32-bit keys.
 //
 // Order: key descending, then position ascending.  Callers lay elements out in
 // ascending vocabulary order, so "position ascending" is the page's tie-break
@@ -7,8 +7,15 @@
 //
 // A selection returns (T, take_eq): every element with key > T is selected,
 // plus the first take_eq elements (in position order) whose key equals T.
-// The digits are 11, 11 and 10 bits wide, most significant first; a pass that
-// finds its boundary bin exactly full stops early.
+//
+// T, the want-th largest key, is the largest t with count(key >= t) >= want.
+// It is built one bit at a time from the most significant bit; each step is a
+// counting pass (compare + add, then a warp or block sum).  The first 12 bits
+// run over every element; the remaining 20 run over the boundary bucket only
+// (elements whose top 12 bits equal T's), which is small unless the input
+// piles up on a few values, in which case the search simply continues over
+// every element.  No atomics and no histograms: the cost does not depend on
+// how the values are distributed.
 #pragma once
 
 #include "common.cuh"
@@ -18,237 +25,280 @@ namespace tail {
 
 struct Threshold {
   uint32_t key;
-  int take_eq;   // elements equal to key that are taken (lowest positions first); -1: take all >= key
+  int take_eq;  // elements equal to key that are taken (lowest positions first)
 };
 
-__device__ __forceinline__ int digit_shift(int pass) { return pass == 0 ? 21 : (pass == 1 ? 10 : 0); }
-__device__ __forceinline__ int digit_bins(int pass) { return pass == 2 ? 1024 : 2048; }
-__device__ __forceinline__ uint32_t digit_prefix_mask(int pass) {
-  return pass == 0 ? 0u : (pass == 1 ? 0xFFE00000u : 0xFFFFFC00u);
+constexpr int SEL_HI_BITS = 12;       // bits searched over every element
+constexpr int SEL_BUCKET_MAX = 64;    // warp path: bucket held two keys per lane
+constexpr int SEL_BLOCK_BUCKET_MAX = 256;
+
+// Number of register keys >= c, summed over four independent chains.
+template <int NPL>
+__device__ __forceinline__ uint32_t count_ge(const uint32_t (&k)[NPL], uint32_t c) {
+  uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; i += 4) {
+    a0 += k[i] >= c ? 1u : 0u;
+    if (i + 1 < NPL) a1 += k[i + 1] >= c ? 1u : 0u;
+    if (i + 2 < NPL) a2 += k[i + 2] >= c ? 1u : 0u;
+    if (i + 3 < NPL) a3 += k[i + 3] >= c ? 1u : 0u;
+  }
+  return (a0 + a1) + (a2 + a3);
 }
 
-// ------------------------------------------------------------------ warp-level
-// One warp selects the top `want` of n keys given by get(i).  `hist` is this
-// warp's private shared-memory histogram of HIST_BINS words.  Requires
-// 1 <= want <= n.
-template <typename GetKey>
-__device__ Threshold warp_select(GetKey get, int n, int want, uint32_t* hist) {
+// ------------------------------------------------------------------ warp level, keys in registers
+// Lane l holds the keys of positions l, l+32, l+64, ... in k[0..NPL); unused
+// slots hold 0, which is below every non-NaN key.  `list` is per-warp shared
+// scratch of SEL_BUCKET_MAX words.  Requires 1 <= want <= n.
+template <int NPL>
+__device__ __forceinline__ Threshold warp_select_regs(const uint32_t (&k)[NPL], int want, uint32_t* list) {
   const int lane = threadIdx.x & 31;
-  uint32_t prefix = 0;
-  int need = want;
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = digit_shift(pass), nb = digit_bins(pass);
-    const uint32_t pmask = digit_prefix_mask(pass);
-    for (int i = lane; i < nb; i += 32) hist[i] = 0u;
-    __syncwarp();
-    for (int base = 0; base < n; base += 32) {
-      const int i = base + lane;
-      uint32_t d = 0xFFFFFFFFu;
-      if (i < n) {
-        const uint32_t k = get(i);
-        if ((k & pmask) == prefix) d = (k >> shift) & static_cast<uint32_t>(nb - 1);
-      }
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
-    }
-    __syncwarp();
-    // Lane l owns bins [nb - (l+1)*bpl, nb - l*bpl): lane 0 holds the largest digits.
-    const int bpl = nb / 32;
-    const int top = nb - lane * bpl;
-    uint32_t s = 0;
-    for (int j = 0; j < bpl; ++j) s += hist[top - 1 - j];
-    uint32_t incl = s;
+  uint32_t T = 0;
+#pragma unroll 1
+  for (int bit = 31; bit >= 32 - SEL_HI_BITS; --bit) {
+    const uint32_t c = T | (1u << bit);
+    if (__reduce_add_sync(0xffffffffu, count_ge(k, c)) >= static_cast<uint32_t>(want)) T = c;
+  }
+  // elements strictly above the bucket, and the bucket itself
+  const uint32_t hi = T >> (32 - SEL_HI_BITS);
+  uint32_t above = 0, inb = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+  for (int i = 0; i < NPL; ++i) {
+    const uint32_t h = k[i] >> (32 - SEL_HI_BITS);
+    above += h > hi ? 1u : 0u;
+    inb += h == hi ? 1u : 0u;
+  }
+  above = __reduce_add_sync(0xffffffffu, above);
+  inb = __reduce_add_sync(0xffffffffu, inb);
+  const int need = want - static_cast<int>(above);  // 1 <= need <= inb
+  if (inb <= SEL_BUCKET_MAX) {
+    // gather the bucket (order is irrelevant for the value search)
+    int base = 0;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const bool in = (k[i] >> (32 - SEL_HI_BITS)) == hi;
+      const uint32_t b = __ballot_sync(0xffffffffu, in);
+      if (in) list[base + __popc(b & lanemask_lt())] = k[i];
+      base += __popc(b);
     }
-    const uint32_t excl = incl - s;
-    const uint32_t hit = __ballot_sync(0xffffffffu, excl < static_cast<uint32_t>(need) &&
-                                                        static_cast<uint32_t>(need) <= incl);
-    const int L = __ffs(hit) - 1;
-    // Lane L walks its bins from the top to find the boundary digit.
-    uint32_t dstar = 0, gt = 0, cnt = 0;
-    if (lane == L) {
-      uint32_t c = excl;
-      for (int j = 0; j < bpl; ++j) {
-        const int bin = top - 1 - j;
-        const uint32_t hb = hist[bin];
-        if (c + hb >= static_cast<uint32_t>(need)) {
-          dstar = static_cast<uint32_t>(bin);
-          gt = c;
-          cnt = hb;
-          break;
-        }
-        c += hb;
-      }
-    }
-    dstar = __shfl_sync(0xffffffffu, dstar, L);
-    gt = __shfl_sync(0xffffffffu, gt, L);
-    cnt = __shfl_sync(0xffffffffu, cnt, L);
     __syncwarp();
-    need -= static_cast<int>(gt);
-    prefix |= dstar << shift;
-    if (cnt == static_cast<uint32_t>(need) && pass < 2) {
-      // the whole boundary bin is taken: select every key whose high bits >= prefix
-      return Threshold{prefix, -1};
+    const uint32_t l0 = lane < static_cast<int>(inb) ? list[lane] : 0u;
+    const uint32_t l1 = lane + 32 < static_cast<int>(inb) ? list[lane + 32] : 0u;
+    __syncwarp();
+#pragma unroll 1
+    for (int bit = 31 - SEL_HI_BITS; bit >= 0; --bit) {
+      const uint32_t c = T | (1u << bit);
+      const uint32_t cnt = (l0 >= c ? 1u : 0u) + (l1 >= c ? 1u : 0u);
+      if (__reduce_add_sync(0xffffffffu, cnt) >= static_cast<uint32_t>(need)) T = c;
+    }
+  } else {
+#pragma unroll 1
+    for (int bit = 31 - SEL_HI_BITS; bit >= 0; --bit) {
+      const uint32_t c = T | (1u << bit);
+      if (__reduce_add_sync(0xffffffffu, count_ge(k, c)) >= static_cast<uint32_t>(want)) T = c;
     }
   }
-  return Threshold{prefix, need};
+  uint32_t gt = 0;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) gt += k[i] > T ? 1u : 0u;
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  return Threshold{T, want - static_cast<int>(gt)};
 }
 
-// Emits, in position order, the elements a Threshold selects.  emit(pos, i, key)
-// receives the output slot pos (0-based) and the element position i.
-template <typename GetKey, typename Emit>
-__device__ int warp_compact(GetKey get, int n, Threshold th, Emit emit) {
+// A lower bound x for the want-th largest key (count(key >= x) >= want),
+// exact in its top 16 bits: the search stops after 16 counting steps, so x is
+// at most one 2^-7-octave step below the exact key.  Requires want <= the
+// number of real (nonzero) keys.
+template <int NPL>
+__device__ __forceinline__ uint32_t warp_bound16_regs(const uint32_t (&k)[NPL], int want) {
+  uint32_t T = 0;
+#pragma unroll 1
+  for (int bit = 31; bit >= 16; --bit) {
+    const uint32_t c = T | (1u << bit);
+    if (__reduce_add_sync(0xffffffffu, count_ge(k, c)) >= static_cast<uint32_t>(want)) T = c;
+  }
+  return T;
+}
+
+// Emits, in position order, the elements a Threshold selects among the n
+// register-held keys.  emit(pos, i, key): output slot pos, element position i.
+template <int NPL, typename Emit>
+__device__ __forceinline__ void warp_compact_regs(const uint32_t (&k)[NPL], int n, Threshold th, Emit emit) {
   const int lane = threadIdx.x & 31;
   int out = 0, eq_seen = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    uint32_t k = 0;
-    bool gt = false, eq = false;
-    if (i < n) {
-      k = get(i);
-      if (th.take_eq < 0) {
-        gt = k >= th.key;
-      } else {
-        gt = k > th.key;
-        eq = k == th.key;
-      }
-    }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int pos = i * 32 + lane;
+    const bool valid = pos < n;
+    const bool gt = valid && k[i] > th.key;
+    const bool eq = valid && k[i] == th.key;
     const uint32_t beq = __ballot_sync(0xffffffffu, eq);
     const int eq_rank = eq_seen + __popc(beq & lanemask_lt());
     const bool take = gt || (eq && eq_rank < th.take_eq);
     const uint32_t bt = __ballot_sync(0xffffffffu, take);
-    if (take) emit(out + __popc(bt & lanemask_lt()), i, k);
+    if (take) emit(out + __popc(bt & lanemask_lt()), pos, k[i]);
     out += __popc(bt);
     eq_seen += __popc(beq);
   }
-  return out;
 }
 
-// ------------------------------------------------------------------ block-level
-// All MERGE_THREADS threads select the top `want` of n keys held in shared
-// memory (keys[0..n)).  `hist` holds HIST_BINS words; `scan` MERGE_THREADS words.
-__device__ __forceinline__ Threshold block_select(const uint32_t* keys, int n, int want, uint32_t* hist,
-                                  uint32_t* scan) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int NW = MERGE_THREADS / 32;
-  __shared__ uint32_t s_dstar, s_gt, s_cnt;
-  uint32_t prefix = 0;
-  int need = want;
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = digit_shift(pass), nb = digit_bins(pass);
-    const uint32_t pmask = digit_prefix_mask(pass);
-    for (int i = tid; i < nb; i += MERGE_THREADS) hist[i] = 0u;
+// ------------------------------------------------------------------ block level, keys in shared memory
+// Every thread of the CTA takes part (any blockDim that is a multiple of 32,
+// at most 1024).  `red` holds 64 words, `list` SEL_BLOCK_BUCKET_MAX words,
+// `misc` 4 words, all in shared memory.
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* red, int parity) {
+  const int nw = blockDim.x >> 5;
+  v = __reduce_add_sync(0xffffffffu, v);
+  if ((threadIdx.x & 31) == 0) red[parity * 32 + (threadIdx.x >> 5)] = v;
+  __syncthreads();
+  uint32_t s = 0;
+  for (int w = 0; w < nw; ++w) s += red[parity * 32 + w];
+  return s;
+}
+
+// T = the want-th largest key of keys[0..n) (1 <= want <= n) and the number
+// of keys strictly above it.
+struct KthKey {
+  uint32_t key;
+  int above;
+};
+
+__device__ __forceinline__ KthKey block_kth_key(const uint32_t* keys, int n, int want, uint32_t* red, uint32_t* list,
+                                                uint32_t* misc) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  int parity = 0;
+  uint32_t T = 0;
+#pragma unroll 1
+  for (int bit = 31; bit >= 32 - SEL_HI_BITS; --bit) {
+    const uint32_t c = T | (1u << bit);
+    uint32_t cnt = 0;
+    for (int i = tid; i < n; i += nt) cnt += keys[i] >= c ? 1u : 0u;
+    if (block_sum(cnt, red, parity) >= static_cast<uint32_t>(want)) T = c;
+    parity ^= 1;
+  }
+  const uint32_t hi = T >> (32 - SEL_HI_BITS);
+  uint32_t above = 0, inb = 0;
+  for (int i = tid; i < n; i += nt) {
+    const uint32_t h = keys[i] >> (32 - SEL_HI_BITS);
+    above += h > hi ? 1u : 0u;
+    inb += h == hi ? 1u : 0u;
+  }
+  above = block_sum(above, red, parity);
+  parity ^= 1;
+  inb = block_sum(inb, red, parity);
+  parity ^= 1;
+  const int need = want - static_cast<int>(above);
+  if (inb <= SEL_BLOCK_BUCKET_MAX) {
+    if (tid == 0) misc[0] = 0u;
     __syncthreads();
-    for (int base = 0; base < n; base += MERGE_THREADS) {
-      const int i = base + tid;
-      uint32_t d = 0xFFFFFFFFu;
-      if (i < n) {
-        const uint32_t k = keys[i];
-        if ((k & pmask) == prefix) d = (k >> shift) & static_cast<uint32_t>(nb - 1);
-      }
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (d != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+    for (int i = tid; i < n; i += nt) {
+      const uint32_t kv = keys[i];
+      if ((kv >> (32 - SEL_HI_BITS)) == hi) list[atomicAdd(&misc[0], 1u)] = kv;
     }
     __syncthreads();
-    // thread t owns bins [nb - (t+1)*bpt, nb - t*bpt), thread 0 the largest digits
-    const int bpt = nb / MERGE_THREADS;
-    const int top = nb - tid * bpt;
-    uint32_t s = 0;
-    for (int j = 0; j < bpt; ++j) s += hist[top - 1 - j];
-    uint32_t incl = s;
+    if (tid < 32) {
+      uint32_t l[SEL_BLOCK_BUCKET_MAX / 32];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (lane == 31) scan[warp] = incl;
-    __syncthreads();
-    uint32_t woff = 0;
-    for (int w = 0; w < warp; ++w) woff += scan[w];
-    incl += woff;
-    const uint32_t excl = incl - s;
-    if (excl < static_cast<uint32_t>(need) && static_cast<uint32_t>(need) <= incl) {
-      uint32_t c = excl;
-      for (int j = 0; j < bpt; ++j) {
-        const int bin = top - 1 - j;
-        const uint32_t hb = hist[bin];
-        if (c + hb >= static_cast<uint32_t>(need)) {
-          s_dstar = static_cast<uint32_t>(bin);
-          s_gt = c;
-          s_cnt = hb;
-          break;
-        }
-        c += hb;
+      for (int j = 0; j < SEL_BLOCK_BUCKET_MAX / 32; ++j) {
+        const int p = j * 32 + tid;
+        l[j] = p < static_cast<int>(inb) ? list[p] : 0u;
       }
+#pragma unroll 1
+      for (int bit = 31 - SEL_HI_BITS; bit >= 0; --bit) {
+        const uint32_t c = T | (1u << bit);
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int j = 0; j < SEL_BLOCK_BUCKET_MAX / 32; ++j) cnt += l[j] >= c ? 1u : 0u;
+        if (__reduce_add_sync(0xffffffffu, cnt) >= static_cast<uint32_t>(need)) T = c;
+      }
+      if (tid == 0) misc[1] = T;
     }
     __syncthreads();
-    const uint32_t dstar = s_dstar, gt = s_gt, cnt = s_cnt;
-    __syncthreads();  // s_* and scan are rewritten by the next pass
-    need -= static_cast<int>(gt);
-    prefix |= dstar << shift;
-    if (cnt == static_cast<uint32_t>(need) && pass < 2) return Threshold{prefix, -1};
+    T = misc[1];
+  } else {
+#pragma unroll 1
+    for (int bit = 31 - SEL_HI_BITS; bit >= 0; --bit) {
+      const uint32_t c = T | (1u << bit);
+      uint32_t cnt = 0;
+      for (int i = tid; i < n; i += nt) cnt += keys[i] >= c ? 1u : 0u;
+      if (block_sum(cnt, red, parity) >= static_cast<uint32_t>(want)) T = c;
+      parity ^= 1;
+    }
   }
-  (void)NW;
-  return Threshold{prefix, need};
+  uint32_t gt = 0;
+  for (int i = tid; i < n; i += nt) gt += keys[i] > T ? 1u : 0u;
+  gt = block_sum(gt, red, parity);
+  __syncthreads();  // red is reused by the caller
+  return KthKey{T, static_cast<int>(gt)};
 }
 
-// Block compaction in position order.  Thread t handles the contiguous chunk
-// [t*E, (t+1)*E) with E = ceil(n / MERGE_THREADS).  `scan` holds 2*MERGE_THREADS words.
-template <typename Emit>
-__device__ int block_compact(const uint32_t* keys, int n, Threshold th, uint32_t* scan, Emit emit) {
-  const int tid = threadIdx.x;
-  const int E = (n + MERGE_THREADS - 1) / MERGE_THREADS;
-  const int i0 = min(n, tid * E), i1 = min(n, i0 + E);
-  uint32_t ngt = 0, neq = 0;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t k = keys[i];
-    if (th.take_eq < 0) {
-      ngt += k >= th.key;
-    } else {
-      ngt += k > th.key;
-      neq += k == th.key;
-    }
-  }
-  scan[tid] = ngt;
-  scan[MERGE_THREADS + tid] = neq;
+// Composite sort key: descending order of it is (value desc, index asc).
+__device__ __forceinline__ uint64_t composite(uint32_t key, int32_t idx) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(idx));
+}
+__device__ __forceinline__ uint32_t composite_key(uint64_t c) { return static_cast<uint32_t>(c >> 32); }
+__device__ __forceinline__ int32_t composite_idx(uint64_t c) {
+  return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(c & 0xFFFFFFFFull));
+}
+
+// Keeps the top `want` of the n candidates (keys[i], idx[i]) in the order
+// (key desc, vocabulary index asc), whatever order they sit in, and writes
+// them as composites to out[0..want) in no particular order.  Ties at the
+// boundary key are settled by a second bitwise search over the indices.
+__device__ __forceinline__ void block_top_composites(const uint32_t* keys, const int32_t* idx, int n, int want,
+                                                     uint64_t* out, uint32_t* red, uint32_t* list,
+                                                     uint32_t* misc) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const KthKey kt = block_kth_key(keys, n, want, red, list, misc);
+  const uint32_t T = kt.key;
+  const int need_eq = want - kt.above;
+  uint32_t neq = 0;
+  for (int i = tid; i < n; i += nt) neq += keys[i] == T ? 1u : 0u;
+  neq = block_sum(neq, red, 0);
   __syncthreads();
-  // exclusive prefix (serial over warps' totals is fine at 256 threads)
-  uint32_t gt_before = 0, eq_before = 0, gt_total = 0, eq_total = 0;
-  {
-    // every thread sums the entries below it; 256 adds, done once per merge
-    for (int t = 0; t < MERGE_THREADS; ++t) {
-      const uint32_t g = scan[t], e = scan[MERGE_THREADS + t];
-      if (t < tid) {
-        gt_before += g;
-        eq_before += e;
+  // the need_eq-th smallest index among the keys equal to T (only when ties exceed the need)
+  uint32_t cut = 0x7FFFFFFFu;
+  if (static_cast<int>(neq) > need_eq) {
+    uint32_t lo = 0;
+    int parity = 1;
+#pragma unroll 1
+    for (int bit = 30; bit >= 0; --bit) {
+      const uint32_t c = lo | (1u << bit);
+      uint32_t cnt = 0;
+      for (int i = tid; i < n; i += nt) cnt += (keys[i] == T && static_cast<uint32_t>(idx[i]) < c) ? 1u : 0u;
+      if (block_sum(cnt, red, parity) < static_cast<uint32_t>(need_eq)) lo = c;
+      parity ^= 1;
+    }
+    cut = lo;
+    __syncthreads();
+  }
+  if (tid == 0) misc[2] = 0u;
+  __syncthreads();
+  for (int i = tid; i < n; i += nt) {
+    const uint32_t kv = keys[i];
+    if (kv > T || (kv == T && static_cast<uint32_t>(idx[i]) <= cut)) out[atomicAdd(&misc[2], 1u)] = composite(kv, idx[i]);
+  }
+  __syncthreads();
+}
+
+// Sorts comp[0..P) descending (P a power of two) with all threads of the CTA.
+__device__ __forceinline__ void block_bitonic_desc(uint64_t* comp, int P) {
+  const int nt = blockDim.x;
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += nt) {
+        const int lo = (i / stride) * (2 * stride) + (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const uint64_t x = comp[lo], y = comp[hi];
+        if ((x < y) == desc) {
+          comp[lo] = y;
+          comp[hi] = x;
+        }
       }
-      gt_total += g;
-      eq_total += e;
+      __syncthreads();
     }
   }
-  const uint32_t take_eq = th.take_eq < 0 ? 0u : static_cast<uint32_t>(th.take_eq);
-  uint32_t pos = gt_before + min(eq_before, take_eq);
-  uint32_t eq_rank = eq_before;
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t k = keys[i];
-    bool take;
-    if (th.take_eq < 0) {
-      take = k >= th.key;
-    } else if (k > th.key) {
-      take = true;
-    } else if (k == th.key) {
-      take = eq_rank < take_eq;
-      ++eq_rank;
-    } else {
-      take = false;
-    }
-    if (take) emit(static_cast<int>(pos++), i, k);
-  }
-  __syncthreads();
-  return static_cast<int>(gt_total + min(eq_total, take_eq));
 }
 
 }  // namespace tail

@@ -1,9 +1,10 @@
 // C ABI of the decode sampling tail: handle lifetime, argument validation,
 // scratch ownership and the launch sequence of one step
-//   rms_rows -> lm_head (+ stage-1 top-k) -> merge1 -> merge2 + sampler,
-// all on the caller's stream, chained with programmatic dependent launch.
+//   rms_rows -> lm_head + global top-k + sampler (one cooperative launch),
+// on the caller's stream, chained with programmatic dependent launch.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -20,8 +21,8 @@ struct tail_s {
   int num_sms;
   int max_smem;
   int nslab;
-  int G;
   int rows_pass;  // rows per lm_head pass
+  int pdl_ok;     // 0 once a cooperative launch with programmatic serialization was refused
   int64_t scratch_bytes;
   // device scratch
   uint32_t* apack;
@@ -29,9 +30,9 @@ struct tail_s {
   uint32_t* cand_key;
   int32_t* cand_idx;
   float* logit_scratch;
-  uint32_t* m1_key;
-  int32_t* m1_idx;
-  int32_t* m1_cnt;
+  uint32_t* pub;
+  int32_t* cand_cnt;
+  unsigned long long* bar;
   float* topk_val;
   int32_t* topk_idx;
   int* err;
@@ -40,18 +41,28 @@ struct tail_s {
   float* st_params;
   int32_t* st_tokens;
   float* st_logits;
-  // wait bound of the kernels
+  // wait bound of the kernels and the dropped-stage test hook
   uint64_t wait_limit_ns;
+  int drop_iter;
   // per-kernel profiling
   int prof_on;
   int prof_n;
-  cudaEvent_t* prof_ev;  // [PROF_MAX][5]
+  cudaEvent_t* prof_ev;  // [PROF_MAX][PROF_EV]
 };
 
 static constexpr int PROF_MAX = 256;
-static constexpr int PROF_EV = 5;
+static constexpr int PROF_EV = 3;
 
 namespace {
+
+thread_local char g_last_error[256] = "";
+
+// Records the failing call for tail_last_error() and clears CUDA's sticky-free error state.
+int cuda_fail(cudaError_t e, const char* what) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
+  cudaGetLastError();
+  return e == cudaErrorMemoryAllocation ? TAIL_ERR_OOM : TAIL_ERR_CUDA;
+}
 
 struct DeviceGuard {
   int prev = -1;
@@ -78,9 +89,9 @@ cudaError_t dalloc(T** p, size_t n, int64_t* total) {
 }
 
 void free_all(tail_t* h) {
-  void* ptrs[] = {h->apack,    h->row_scale, h->cand_key,  h->cand_idx,   h->logit_scratch,
-                  h->m1_key,   h->m1_idx,    h->m1_cnt,    h->topk_val,   h->topk_idx,
-                  h->err,      h->st_hidden, h->st_params, h->st_tokens,  h->st_logits};
+  void* ptrs[] = {h->apack,    h->row_scale, h->cand_key,  h->cand_idx,  h->logit_scratch, h->pub,
+                  h->cand_cnt, h->bar,       h->topk_val,  h->topk_idx,  h->err,           h->st_hidden,
+                  h->st_params, h->st_tokens, h->st_logits};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -102,6 +113,8 @@ int validate_config(const tail_config* c) {
 
 extern "C" {
 
+const char* tail_last_error(void) { return g_last_error; }
+
 const char* tail_status_string(int s) {
   switch (s) {
     case TAIL_OK: return "ok";
@@ -122,9 +135,10 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return TAIL_ERR_INVALID_ARG;
   DeviceGuard guard(device);
-  if (!guard.ok) return TAIL_ERR_CUDA;
+  if (!guard.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
   cudaDeviceProp prop;
-  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return TAIL_ERR_CUDA;
+  cudaError_t pe = cudaGetDeviceProperties(&prop, device);
+  if (pe != cudaSuccess) return cuda_fail(pe, "cudaGetDeviceProperties");
   if (prop.major != 10 || prop.minor != 3) return TAIL_ERR_UNSUPPORTED;  // built for sm_103a only
 
   tail_t* h = new (std::nothrow) tail_t();
@@ -140,13 +154,20 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   int64_t nslab = npairs / 8;
   if (nslab < 1) nslab = 1;
   if (nslab > h->num_sms) nslab = h->num_sms;
+  if (nslab > MAX_SLABS) nslab = MAX_SLABS;
   h->nslab = static_cast<int>(nslab);
-  h->G = merge_groups(h->nslab, cfg->k);
-  if (h->G < 1) {
+  h->rows_pass = cfg->gbs_max < MAX_ROWS_PER_PASS ? cfg->gbs_max : MAX_ROWS_PER_PASS;
+  if (!prop.cooperativeLaunch) {
     delete h;
     return TAIL_ERR_UNSUPPORTED;
   }
-  h->rows_pass = cfg->gbs_max < MAX_ROWS_PER_PASS ? cfg->gbs_max : MAX_ROWS_PER_PASS;
+  int max_dyn = 0;
+  cudaError_t pe2 = prepare_gemv(h->max_smem, &max_dyn);
+  if (pe2 != cudaSuccess) {
+    delete h;
+    return cuda_fail(pe2, "cudaFuncSetAttribute (shared memory opt-in)");
+  }
+  h->max_smem = max_dyn;
   // every row count the passes can use must have a shared-memory plan
   for (int B = 1; B <= h->rows_pass; ++B) {
     if (!plan_gemv(B, cfg->H, cfg->V, cfg->k, h->nslab, h->max_smem).ok) {
@@ -154,15 +175,12 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
       return TAIL_ERR_UNSUPPORTED;
     }
   }
-  if (merge2_smem_bytes(h->G, cfg->k) > static_cast<size_t>(h->max_smem) ||
-      merge1_smem_bytes(h->nslab, h->G, cfg->k) > static_cast<size_t>(h->max_smem)) {
+  // the slab selects hold a slab row in registers: at most SEL_NPL keys per lane
+  if ((npairs + h->nslab - 1) / h->nslab * 16 > 32 * SEL_NPL) {
     delete h;
     return TAIL_ERR_UNSUPPORTED;
   }
-  if (prepare_gemv(h->max_smem) != cudaSuccess || prepare_merge(h->max_smem) != cudaSuccess) {
-    delete h;
-    return TAIL_ERR_CUDA;
-  }
+  h->pdl_ok = 1;
 
   const int R = h->rows_pass;
   const int Rpad = ((R + 7) / 8) * 8 < 8 ? 8 : ((R + 7) / 8) * 8;
@@ -176,9 +194,9 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   e = e ? e : dalloc(&h->cand_key, static_cast<size_t>(R) * h->nslab * K, &tot);
   e = e ? e : dalloc(&h->cand_idx, static_cast<size_t>(R) * h->nslab * K, &tot);
   e = e ? e : dalloc(&h->logit_scratch, static_cast<size_t>(R) * cfg->V, &tot);
-  e = e ? e : dalloc(&h->m1_key, static_cast<size_t>(R) * h->G * K, &tot);
-  e = e ? e : dalloc(&h->m1_idx, static_cast<size_t>(R) * h->G * K, &tot);
-  e = e ? e : dalloc(&h->m1_cnt, static_cast<size_t>(R) * h->G, &tot);
+  e = e ? e : dalloc(&h->pub, static_cast<size_t>(R) * h->nslab * TAIL_PUB_PER_SLAB, &tot);
+  e = e ? e : dalloc(&h->cand_cnt, static_cast<size_t>(R) * h->nslab, &tot);
+  e = e ? e : dalloc(&h->bar, 1, &tot);
   e = e ? e : dalloc(&h->topk_val, static_cast<size_t>(cfg->gbs_max) * K, &tot);
   e = e ? e : dalloc(&h->topk_idx, static_cast<size_t>(cfg->gbs_max) * K, &tot);
   e = e ? e : dalloc(&h->err, 1, &tot);
@@ -187,16 +205,17 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   e = e ? e : dalloc(&h->st_params, static_cast<size_t>(cfg->gbs_max) * 4, &tot);
   e = e ? e : dalloc(&h->st_tokens, static_cast<size_t>(cfg->gbs_max), &tot);
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(h->bar, 0, sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(h->apack, 0, ksteps * mt_max * APACK_TILE_BYTES);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     free_all(h);
     delete h;
-    cudaGetLastError();
-    return e == cudaErrorMemoryAllocation ? TAIL_ERR_OOM : TAIL_ERR_CUDA;
+    return cuda_fail(e, "scratch allocation");
   }
   h->scratch_bytes = tot;
   h->wait_limit_ns = DEFAULT_TIMEOUT_NS;
+  h->drop_iter = -1;
   *out = h;
   return TAIL_OK;
 }
@@ -254,46 +273,38 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     ga.nslab = h->nslab;
     ga.npairs = npairs;
     ga.cb_pairs = plan.cb_pairs;
+    ga.kpb = plan.kpb;
     ga.pitch = plan.pitch;
     ga.stage_bytes = plan.stage_bytes;
     ga.nstages = plan.nstages;
     ga.logits_in_smem = plan.logits_in_smem;
     ga.max_slab_cols = plan.max_slab_cols;
     ga.smem_bytes = plan.smem_bytes;
+    ga.pub = h->pub;
+    ga.cand_cnt = h->cand_cnt;
+    ga.bar = h->bar;
+    ga.topk_val = (out_topk_vals ? out_topk_vals : h->topk_val) + static_cast<int64_t>(r0) * K;
+    ga.topk_idx = (out_topk_idx ? out_topk_idx : h->topk_idx) + static_cast<int64_t>(r0) * K;
+    ga.topk_ld = K;
+    ga.params = params ? params + static_cast<int64_t>(r0) * ncols : nullptr;
+    ga.ncols = ncols;
+    ga.tokens = params ? out_tokens + r0 : nullptr;
+    ga.capc = plan.capc;
+    ga.sortP = plan.sortP;
     ga.timeout_ns = h->wait_limit_ns;
-    e = launch_gemv(ga, stream);
+    ga.drop_iter = h->drop_iter;
+    if (h->pdl_ok) {
+      e = launch_gemv(ga, stream, true);
+      if (e != cudaSuccess) {  // this runtime refuses cooperative + programmatic: launch without the overlap
+        cudaGetLastError();
+        h->pdl_ok = 0;
+      }
+    }
+    if (!h->pdl_ok) e = launch_gemv(ga, stream, false);
     if (e != cudaSuccess) break;
     if (ev) cudaEventRecord(ev[2], stream);
-
-    MergeArgs ma;
-    ma.cand_key = h->cand_key;
-    ma.cand_idx = h->cand_idx;
-    ma.m1_key = h->m1_key;
-    ma.m1_idx = h->m1_idx;
-    ma.m1_cnt = h->m1_cnt;
-    ma.topk_val = (out_topk_vals ? out_topk_vals : h->topk_val) + static_cast<int64_t>(r0) * K;
-    ma.topk_idx = (out_topk_idx ? out_topk_idx : h->topk_idx) + static_cast<int64_t>(r0) * K;
-    ma.topk_ld = K;
-    ma.params = params ? params + static_cast<int64_t>(r0) * ncols : nullptr;
-    ma.ncols = ncols;
-    ma.tokens = params ? out_tokens + r0 : nullptr;
-    ma.B = B;
-    ma.V = c.V;
-    ma.K = K;
-    ma.nslab = h->nslab;
-    ma.G = h->G;
-    ma.npairs = npairs;
-    ma.err = h->err;
-    e = launch_merge1(ma, stream);
-    if (e != cudaSuccess) break;
-    if (ev) cudaEventRecord(ev[3], stream);
-    e = launch_merge2_sample(ma, stream);
-    if (e == cudaSuccess && ev) cudaEventRecord(ev[4], stream);
   }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return TAIL_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return TAIL_OK;
 }
 
@@ -390,7 +401,9 @@ int tail_check(tail_t* h) {
   int flag = 0;
   if (cudaMemcpy(&flag, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TAIL_ERR_CUDA;
   if (flag != 0) {
+    // a wait that ran out may leave the grid barrier counter off its generation boundary
     cudaMemset(h->err, 0, sizeof(int));
+    cudaMemset(h->bar, 0, sizeof(unsigned long long));
     cudaDeviceSynchronize();
     return TAIL_ERR_DEVICE;
   }
@@ -446,14 +459,20 @@ int tail_set_wait_limit(tail_t* h, uint64_t ns) {
   return TAIL_OK;
 }
 
+int tail_debug_drop_stage(tail_t* h, int32_t iteration) {
+  if (!h || iteration < -1) return TAIL_ERR_INVALID_ARG;
+  h->drop_iter = iteration;
+  return TAIL_OK;
+}
+
 int tail_get_info(const tail_t* h, tail_info* out) {
   if (!h || !out) return TAIL_ERR_INVALID_ARG;
   out->num_sms = h->num_sms;
   out->nslab = h->nslab;
-  out->merge_groups = h->G;
-  out->lmhead_path = 1;
+  out->merge_groups = 0;
+  out->lmhead_path = h->pdl_ok ? 2 : 1;
   out->rows_per_pass = h->rows_pass;
-  out->kernels_per_run = 4;
+  out->kernels_per_run = 2;
   out->scratch_bytes = h->scratch_bytes;
   return TAIL_OK;
 }

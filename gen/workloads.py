@@ -121,8 +121,9 @@ def custom(B: int, H: int, V: int, k: int, *, hidden_dtype: str = "bf16", Hu: in
            threads: int | None = None, name: str | None = None) -> Workload:
     """A synthetic tail input of any shape (same distributions as the named workloads).
 
-    Hu < H places zero pad lanes (x, gamma and W rows) at the interleaved positions
-    of ``pad_lanes``.  dup_cols > 1 repeats each drawn W column that many times
+    Hu < H with zero_pad=1 places zero pad lanes (x, gamma and W rows) at the
+    interleaved positions of ``pad_lanes``; with zero_pad=0 the lanes [Hu, H) are
+    simply not part of the hidden state and keep whatever was drawn.  dup_cols > 1 repeats each drawn W column that many times
     consecutively, planting exact logit ties.
     """
     threads = threads or min(16, os.cpu_count() or 1)
@@ -134,7 +135,7 @@ def custom(B: int, H: int, V: int, k: int, *, hidden_dtype: str = "bf16", Hu: in
     w = _normal_bf16_matrix(seed, H, V // dup_cols, w_std, threads)
     if dup_cols > 1:
         w = np.repeat(w, dup_cols, axis=1)
-    if Hu < H:
+    if Hu < H and zero_pad:
         pads = pad_lanes(H, Hu)
         if hidden_dtype == "f32":
             x[:, pads] = 0.0

@@ -66,8 +66,9 @@ typedef struct {
 typedef struct {
   int32_t num_sms;          /* SMs of the device */
   int32_t nslab;            /* vocabulary slabs = CTAs of the lm_head kernel */
-  int32_t merge_groups;     /* CTAs per row of the first merge stage */
-  int32_t lmhead_path;      /* 1: mma.sync skinny GEMM */
+  int32_t merge_groups;     /* 0: the top-k merge runs inside the lm_head launch */
+  int32_t lmhead_path;      /* 1: cooperative mma.sync lm_head + top-k + sampler launch;
+                               2: the same, overlapped with the RMSNorm kernel (programmatic launch) */
   int32_t rows_per_pass;    /* rows one lm_head pass covers (larger gbs runs several passes) */
   int32_t kernels_per_run;  /* kernel launches of one tail_run with gbs <= rows_per_pass */
   int64_t scratch_bytes;    /* device scratch owned by the handle */
@@ -143,8 +144,8 @@ int tail_check(tail_t* h);
  * record of up to 256 lm_head passes.
  * tail_profile_read synchronises on the recorded events and returns, for the
  * passes recorded since enabling, the summed device milliseconds of each
- * kernel in kernel_ms[4] = {rms_rows, lm_head, merge1, merge2 + sampler} and
- * their count in *passes.
+ * kernel in kernel_ms[2] = {rms_rows, lm_head + top-k + sampler} and their
+ * count in *passes.
  */
 int tail_profile_enable(tail_t* h, int enable);
 int tail_profile_read(tail_t* h, float* kernel_ms, int32_t* passes);
@@ -152,11 +153,18 @@ int tail_profile_read(tail_t* h, float* kernel_ms, int32_t* passes);
 /*
  * Bounds every device-side wait of later runs to `ns` nanoseconds of GPU
  * global time (default 1e9).  A wait that runs out raises the device error
- * flag, the kernel drains its copies in flight and returns, and tail_check
- * reports TAIL_ERR_DEVICE.  A limit of 0 makes the first wait that is not
- * already satisfied run out: the failure-path test uses it.
+ * flag; the kernel stops issuing copies, waits (bounded) for the copies it
+ * already issued, and returns; tail_check then reports TAIL_ERR_DEVICE.
  */
 int tail_set_wait_limit(tail_t* h, uint64_t ns);
+
+/*
+ * Test hook for the bounded-wait path: while iteration >= 0, the lm_head
+ * kernel of later runs never issues the copies of that ring iteration, so
+ * the consumers' wait on it runs out after the wait limit (outputs of such a
+ * run are undefined; nothing faults).  -1 turns the hook off.
+ */
+int tail_debug_drop_stage(tail_t* h, int32_t iteration);
 
 /* Fills *out with the handle's static facts. */
 int tail_get_info(const tail_t* h, tail_info* out);
@@ -166,6 +174,10 @@ void tail_destroy(tail_t* h);
 
 /* Static string for a status code. */
 const char* tail_status_string(int status);
+
+/* The CUDA call behind this thread's last TAIL_ERR_CUDA / TAIL_ERR_OOM, as text
+   ("" when none); valid until the thread's next failing call. */
+const char* tail_last_error(void);
 
 #ifdef __cplusplus
 }

@@ -1,7 +1,8 @@
 """Failure path of the bounded device waits, exercised without any GPU fault.
 
-A wait limit of 0 makes the lm_head kernel's first unsatisfied wait run out:
-the kernel raises its error flag, drains the copies it issued and returns.
+The test hook makes the lm_head producer skip one ring iteration, so the
+consumers' wait on it can only run out (after a 2 ms limit): the kernel raises
+its error flag, drains the copies it did issue and returns.
 tail_check must report TAIL_ERR_DEVICE, clear the flag, and the next run with
 the normal limit must be correct again.
 """
@@ -24,10 +25,12 @@ def test_wait_that_runs_out_is_reported_and_recoverable():
     hidden, gamma, w_t, p = tc.to_device(w, torch)
     tok = torch.zeros(w.B, dtype=torch.int32, device=hidden.device)
     with dst.Tail(w.H, w.V, w.k, w.B) as t:
-        assert dst.tail_set_wait_limit(t.h, 0) == dst.TAIL_OK
+        assert dst.tail_set_wait_limit(t.h, 2_000_000) == dst.TAIL_OK
+        assert dst.tail_debug_drop_stage(t.h, 3) == dst.TAIL_OK
         t.run(hidden, gamma, w_t, p, out_tokens=tok)
         assert dst.tail_check(t.h) == dst.TAIL_ERR_DEVICE
         assert dst.tail_check(t.h) == dst.TAIL_OK  # the flag was cleared
+        assert dst.tail_debug_drop_stage(t.h, -1) == dst.TAIL_OK
         assert dst.tail_set_wait_limit(t.h, 1_000_000_000) == dst.TAIL_OK
         res = tc.run_gpu(t, w, torch, dev_tensors=(hidden, gamma, w_t, p))
     L, ov, oi = tc.oracle_rows(w, np.arange(w.B))

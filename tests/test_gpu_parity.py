@@ -164,7 +164,7 @@ def test_invalid_arguments_return_status_codes():
         # bad column count
         assert dst.tail_run(t.h, P(hidden), P(gamma), P(w_t), P(p), 5, 4, P(tok), None, s) == dst.TAIL_ERR_INVALID_ARG
         # misaligned weight pointer
-        bad = hidden.view(torch.int16)[1:]
+        bad = w_t.view(torch.int16).view(-1)[1:]  # 2-byte offset
         assert dst.tail_run(t.h, P(hidden), P(gamma), P(bad), P(p), 4, 4, P(tok), None, s) == dst.TAIL_ERR_INVALID_ARG
         # params without tokens
         assert dst.tail_run(t.h, P(hidden), P(gamma), P(w_t), P(p), 4, 4, None, None, s) == dst.TAIL_ERR_INVALID_ARG
