@@ -266,7 +266,7 @@ def main():
             step()
     kms, npass = dst.tail_profile_read(t.h)
     dst.tail_profile_enable(t.h, False)
-    lm_ms = kms["lm_head"] / max(1, npass)
+    lm_ms = kms["lm_head"] / max(1, npass)  # the dominant kernel: lm_head + top-k + sampler
     kshare = {k: v / max(1e-9, sum(kms.values())) for k, v in kms.items()}
 
     # ---------------- end to end through the host-buffer entry point
