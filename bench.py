@@ -62,13 +62,16 @@ def algorithmic_bytes(w, emit: bool) -> dict:
     return {"lm_head": lm_head, "step": step}
 
 
+# the translation unit of the dominant (lm_head + top-k + sampler) kernel and the headers it includes
+ROOFLINE_KERNEL_SOURCES = ("common.cuh", "internal.h", "lmhead_tail.cu", "sampler.cuh", "select.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_sampling_tail_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in ROOFLINE_KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
