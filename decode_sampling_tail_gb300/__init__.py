@@ -29,7 +29,7 @@ TAIL_ERR_DEVICE = -5
 
 EXPORTS = ("tail_create", "tail_run", "tail_run_ex", "tail_run_host", "tail_check", "tail_get_info",
            "tail_destroy", "tail_status_string", "tail_profile_enable", "tail_profile_read",
-           "tail_set_wait_limit", "tail_debug_drop_stage", "tail_last_error")
+           "tail_set_wait_limit", "tail_debug_drop_stage", "tail_last_error", "tail_run_noalloc")
 KERNELS = ("rms_rows", "lm_head")
 
 
@@ -85,6 +85,8 @@ def lib(path: str | None = None):
         L.tail_run_ex.restype = ctypes.c_int
         L.tail_run_host.argtypes = [P, P, P, P, P, i32, i32, P, P, P]
         L.tail_run_host.restype = ctypes.c_int
+        L.tail_run_noalloc.argtypes = [ctypes.POINTER(tail_config), P, P, P, P, i32, i32, P, P, P, P]
+        L.tail_run_noalloc.restype = ctypes.c_int
         L.tail_check.argtypes = [P]
         L.tail_check.restype = ctypes.c_int
         L.tail_get_info.argtypes = [P, ctypes.POINTER(tail_info)]
@@ -140,6 +142,12 @@ def tail_run_host(h, hidden_host, gamma, w_t, params_host, n_param_cols, gbs, ou
                                out_logits_host_opt, stream)
 
 
+def tail_run_noalloc(cfg: tail_config, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens,
+                     out_logits_opt, out_status_opt, stream) -> int:
+    return lib().tail_run_noalloc(ctypes.byref(cfg), hidden, gamma, w_t, params, n_param_cols, gbs,
+                                  out_tokens, out_logits_opt, out_status_opt, stream)
+
+
 def tail_check(h) -> int:
     return lib().tail_check(h)
 
@@ -186,6 +194,37 @@ _DTYPES = {"f32": TAIL_F32, "f16": TAIL_F16, "bf16": TAIL_BF16}
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream, device):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def run_noalloc(hidden, gamma, w_t, params=None, out_tokens=None, out_logits=None, out_status=None, *,
+                k: int = 256, hidden_actual: int = 0, eps: float = 1e-5, hidden_dtype: str = "bf16",
+                zero_interleaved_pad: bool = True, deferred_rms: bool = True, stream=None):
+    """tail_run_noalloc on the current device with torch CUDA tensors (see ``Tail`` for their layout).
+
+    No handle and no device allocation: the library's static per-device scratch is used, so
+    calls whose kernels may overlap must be serialised by the caller.  ``out_status`` is an
+    optional int32 CUDA tensor of one element receiving the kernels' error word.
+    """
+    gbs, H = int(hidden.shape[0]), int(hidden.shape[1])
+    V = int(w_t.shape[1])
+    cfg = tail_config(H, hidden_actual, V, k, max(gbs, 1), eps, _DTYPES[hidden_dtype],
+                      int(zero_interleaved_pad), int(deferred_rms))
+    ncols = int(params.shape[1]) if params is not None else 4
+    rc = tail_run_noalloc(cfg, _ptr(hidden), _ptr(gamma), _ptr(w_t), _ptr(params), ncols, gbs,
+                          _ptr(out_tokens), _ptr(out_logits), _ptr(out_status),
+                          _stream_ptr(stream, hidden.device))
+    if rc == TAIL_ERR_UNSUPPORTED:
+        raise TailError(rc, "tail_run_noalloc [" + lib().tail_last_error().decode() + "]")
+    if rc != TAIL_OK:
+        raise TailError(rc, "tail_run_noalloc")
+    return out_tokens
 
 
 class Tail:

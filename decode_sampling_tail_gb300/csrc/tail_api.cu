@@ -11,6 +11,7 @@
 #include <new>
 
 #include "../../include/tail.h"
+#include "abi_common.h"
 #include "internal.h"
 
 using namespace tail;
@@ -53,16 +54,34 @@ struct tail_s {
 static constexpr int PROF_MAX = 256;
 static constexpr int PROF_EV = 3;
 
-namespace {
+namespace tail {
 
-thread_local char g_last_error[256] = "";
+static thread_local char g_last_error[256] = "";
 
-// Records the failing call for tail_last_error() and clears CUDA's sticky-free error state.
 int cuda_fail(cudaError_t e, const char* what) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
   cudaGetLastError();
   return e == cudaErrorMemoryAllocation ? TAIL_ERR_OOM : TAIL_ERR_CUDA;
 }
+
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+
+int validate_config(const tail_config* c) {
+  if (!c) return TAIL_ERR_INVALID_ARG;
+  const int Hu = c->hidden_actual <= 0 ? c->H : c->hidden_actual;
+  if (c->H <= 0 || c->V <= 0 || Hu < 1 || Hu > c->H) return TAIL_ERR_INVALID_ARG;
+  if (c->k < 1 || c->k > MAX_K || c->k > c->V) return TAIL_ERR_INVALID_ARG;
+  if (c->gbs_max < 1 || c->gbs_max > 4096) return TAIL_ERR_INVALID_ARG;
+  if (c->hidden_dtype < TAIL_F32 || c->hidden_dtype > TAIL_BF16) return TAIL_ERR_INVALID_ARG;
+  if (!(c->eps >= 0.0f)) return TAIL_ERR_INVALID_ARG;
+  if (c->H % KSTEP != 0 || c->V % 16 != 0) return TAIL_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(c->H) * c->V >= (int64_t(1) << 40)) return TAIL_ERR_UNSUPPORTED;
+  return TAIL_OK;
+}
+
+}  // namespace tail
+
+namespace {
 
 struct DeviceGuard {
   int prev = -1;
@@ -75,10 +94,6 @@ struct DeviceGuard {
     if (prev >= 0) cudaSetDevice(prev);
   }
 };
-
-int elem_bytes(int dtype) { return dtype == TAIL_F32 ? 4 : 2; }
-
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 template <typename T>
 cudaError_t dalloc(T** p, size_t n, int64_t* total) {
@@ -94,19 +109,6 @@ void free_all(tail_t* h) {
                   h->st_params, h->st_tokens, h->st_logits};
   for (void* p : ptrs)
     if (p) cudaFree(p);
-}
-
-int validate_config(const tail_config* c) {
-  if (!c) return TAIL_ERR_INVALID_ARG;
-  const int Hu = c->hidden_actual <= 0 ? c->H : c->hidden_actual;
-  if (c->H <= 0 || c->V <= 0 || Hu < 1 || Hu > c->H) return TAIL_ERR_INVALID_ARG;
-  if (c->k < 1 || c->k > MAX_K || c->k > c->V) return TAIL_ERR_INVALID_ARG;
-  if (c->gbs_max < 1 || c->gbs_max > 4096) return TAIL_ERR_INVALID_ARG;
-  if (c->hidden_dtype < TAIL_F32 || c->hidden_dtype > TAIL_BF16) return TAIL_ERR_INVALID_ARG;
-  if (!(c->eps >= 0.0f)) return TAIL_ERR_INVALID_ARG;
-  if (c->H % KSTEP != 0 || c->V % 16 != 0) return TAIL_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(c->H) * c->V >= (int64_t(1) << 40)) return TAIL_ERR_UNSUPPORTED;
-  return TAIL_OK;
 }
 
 }  // namespace
@@ -150,12 +152,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   h->num_sms = prop.multiProcessorCount;
   h->max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
   const int64_t npairs = cfg->V / 16;
-  // one slab per SM, at least 8 pairs (128 columns) per slab
-  int64_t nslab = npairs / 8;
-  if (nslab < 1) nslab = 1;
-  if (nslab > h->num_sms) nslab = h->num_sms;
-  if (nslab > MAX_SLABS) nslab = MAX_SLABS;
-  h->nslab = static_cast<int>(nslab);
+  h->nslab = slab_count(npairs, h->num_sms, MAX_SLABS);
   h->rows_pass = cfg->gbs_max < MAX_ROWS_PER_PASS ? cfg->gbs_max : MAX_ROWS_PER_PASS;
   if (!prop.cooperativeLaunch) {
     delete h;

@@ -129,6 +129,57 @@ int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const 
                   int32_t* out_tokens_host, float* out_logits_host_opt, void* stream);
 
 /*
+ * Allocation-free form of tail_run, for callers that must not allocate device
+ * memory: a serving runtime that hands nearly all of HBM to its own pools up
+ * front and refuses any cudaMalloc behind its back, code that cannot keep a
+ * handle alive between steps (an op or plugin called without lifetime hooks),
+ * or a decode loop that cannot afford the device-wide synchronisation that
+ * cudaMalloc and cudaFree may imply.  The page has no counterpart: it is a
+ * calling convention of this library, not a step of the method.
+ *
+ * It runs the same kernels and gives the same results as tail_run with the
+ * same config (bitwise equal when gbs <= 8 at GPT-OSS sizes; larger batches
+ * run as several passes and agree within the logit tolerance).  Instead of
+ * handle scratch it uses one static device array of 4 MiB per device, part of
+ * this library's device image; no call allocates, frees or calls a routine
+ * that allocates.
+ *   cfg            the config tail_create would take (validated on every call);
+ *                  gbs <= cfg->gbs_max.
+ *   device         the caller's current CUDA device; `stream` must belong to it.
+ *   hidden ... out_logits_opt, stream: as in tail_run.
+ *   out_status_opt device int32, or NULL: receives (in stream order, after
+ *                  the call's last kernel) 0, or the nonzero code of a
+ *                  bounded device wait that ran out, in which case the
+ *                  outputs are undefined.
+ * Size limit: one pass of B rows needs, each part rounded up to 256 bytes,
+ * 256 (barrier counter and error word) + 32 * H * mt (activation pack; mt = 1,
+ * 2, 4 or 8 for B up to 8, 16, 32, 64) + 32 * mt (row scales)
+ * + 20 * B * nslab (published maxima, counts) + 8 * B * nslab * k (per-slab
+ * candidates) + 8 * B * k (top-k staging) + 4 * B * V (logits staging, only
+ * when a slab's logits do not fit in shared memory) bytes, nslab being the
+ * vocabulary slab count (min(SMs, V / 128), at least 1).  Batches run in
+ * passes of as many rows (at most 64) as fit in 4 MiB.  At H = 2880, V = 201088, k = 256
+ * that is 8 rows per pass.  When not even one row fits, the call returns
+ * TAIL_ERR_UNSUPPORTED before launching anything, and tail_last_error()
+ * states the bytes needed and the 4 MiB limit.
+ * Zeroing: every call clears the grid-barrier counter and the error word with
+ * one cudaMemsetAsync on `stream`; the rest of the scratch is fully written
+ * by the kernels before it is read.
+ * First call on a device: sets up that device (looks up the static array's
+ * address with cudaGetSymbolAddress, which loads the library's device image
+ * if it is not loaded yet, and opts the lm_head kernels into their shared
+ * memory size).  Make it once before any stream capture on that device.
+ * Overlapping calls race: all calls on one device share the one static
+ * array, so two calls whose kernels may overlap (different streams, threads
+ * or processes sharing a context, without ordering between them) corrupt
+ * each other's results.  Serialise them on one stream.  Handles created with
+ * tail_create own separate scratch and do not race with this call.
+ */
+int tail_run_noalloc(const tail_config* cfg, const void* hidden, const float* gamma, const uint16_t* w_t,
+                     const float* params, int32_t n_param_cols, int32_t gbs, int32_t* out_tokens,
+                     float* out_logits_opt, int32_t* out_status_opt, void* stream);
+
+/*
  * Synchronises the handle's device work and reads the device error flag that
  * kernels raise when a bounded wait runs out.  Returns TAIL_ERR_DEVICE (and
  * clears the flag) if it was set, TAIL_ERR_CUDA on a sticky CUDA error, else
