@@ -30,7 +30,7 @@ TAIL_ERR_DEVICE = -5
 EXPORTS = ("tail_create", "tail_run", "tail_run_ex", "tail_run_host", "tail_check", "tail_get_info",
            "tail_destroy", "tail_status_string", "tail_profile_enable", "tail_profile_read",
            "tail_set_wait_limit", "tail_debug_drop_stage", "tail_last_error", "tail_run_noalloc")
-KERNELS = ("rms_rows", "lm_head")
+KERNELS = ("rms_rows", "lm_head", "merge")
 
 
 class TailLibraryMissing(RuntimeError):
@@ -59,7 +59,8 @@ class tail_config(ctypes.Structure):
 class tail_info(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("nslab", ctypes.c_int32), ("merge_groups", ctypes.c_int32),
                 ("lmhead_path", ctypes.c_int32), ("rows_per_pass", ctypes.c_int32),
-                ("kernels_per_run", ctypes.c_int32), ("scratch_bytes", ctypes.c_int64)]
+                ("kernels_per_run", ctypes.c_int32), ("scratch_bytes", ctypes.c_int64),
+                ("tc_min_rows", ctypes.c_int32)]
 
 
 _lock = threading.Lock()

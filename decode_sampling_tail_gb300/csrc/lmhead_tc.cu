@@ -1,0 +1,374 @@
+// Tensor-core lm_head of the tail for batches above 8 rows ("GPT-OSS Tail
+// Chunked Megakernel Kernel API Reference", parameters `lm_head_weight_t`,
+// `deferred_rms`, `emit_logits`, and section "Background": a stage-1 top-k
+// per vocabulary chunk feeding one global top-k).
+//
+// logit[b][v] = row_scale[b] * sum_h (hi[b][h] + lo[b][h]) * W[h][v], with
+// hi + lo the two-bf16 split of the RMSNorm output, on tcgen05 tensor cores
+// with fp32 accumulation in tensor memory.
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0     TMA producer: per ring stage one 64-wide k slice of the
+//              activation tile (hi and lo: two 128 x 64 boxes, or one box
+//              holding both when the batch fits in 64 rows) and of the weight
+//              tile (three 64 x 64 boxes, N = 192 columns), 128-byte swizzle.
+//   warp 1     tensor-memory owner and MMA issuer: M = 128, N = 192, K = 16
+//              per instruction, A K-major, B (the weight, V contiguous)
+//              MN-major; two accumulators of 256 columns so the epilogue of
+//              one tile overlaps the MMAs of the next.
+//   warps 2-5  epilogue, one batch row per thread (tensor-memory lane): row
+//              scale, the fp32 logits row to global memory, and the tile's
+//              top TC_LIST candidates (value desc, index asc) for the merge.
+// Tiles are (column tile n, m-block m) pairs taken round robin by the CTAs,
+// m varying fastest, so the CTAs that share a weight tile run it together and
+// the weight is read from HBM once.
+//
+// Every wait is bounded (the error flag is raised and the CTA winds down:
+// no copy or MMA is left in flight and the tensor memory is released).
+#include "common.cuh"
+#include "internal.h"
+#include "select.cuh"
+#include "tc_common.cuh"
+#include "tc_internal.h"
+
+namespace tail {
+
+namespace {
+
+constexpr int TC_THREADS = 192;
+constexpr uint32_t TC_ACC_COLS = 256;               // tensor-memory columns per accumulator
+constexpr uint32_t TC_TMEM_COLS = 2 * TC_ACC_COLS;  // two accumulators
+constexpr uint32_t W_BOX_BYTES = 64 * 64 * 2;
+constexpr uint32_t A_BOX_BYTES = 128 * 64 * 2;
+constexpr int XBUF_PITCH = 33;                      // floats per row of the stacked hi/lo exchange
+constexpr int TC_CHUNKS = TC_N / 32;
+
+template <bool STACKED>
+struct TcGeom {
+  static constexpr uint32_t A_BYTES = STACKED ? A_BOX_BYTES : 2 * A_BOX_BYTES;
+  static constexpr uint32_t STAGE = A_BYTES + 3 * W_BOX_BYTES;
+  static constexpr int NST = STACKED ? 4 : 3;
+  static constexpr uint32_t XBUF_BYTES = 64 * XBUF_PITCH * 4;
+  static constexpr uint32_t CTL_BYTES = 256;
+  static constexpr uint32_t SMEM = 1024 /* alignment slack */ + NST * STAGE + XBUF_BYTES + CTL_BYTES;
+};
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void fail(int* err, int code, volatile int* abort_flag) {
+  if (!*abort_flag) raise_error(err, code);
+  *abort_flag = 1;
+}
+
+// Inserts c into the descending list l (kept in registers: fully unrolled).
+__device__ __forceinline__ void list_insert(uint64_t (&l)[TC_LIST], uint64_t c) {
+  if (c <= l[TC_LIST - 1]) return;
+  l[TC_LIST - 1] = c;
+#pragma unroll
+  for (int i = TC_LIST - 1; i > 0; --i) {
+    const uint64_t x = l[i - 1], y = l[i];
+    const bool sw = y > x;
+    l[i - 1] = sw ? y : x;
+    l[i] = sw ? x : y;
+  }
+}
+
+template <bool STACKED>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
+                     const TcArgs a) {
+  using G = TcGeom<STACKED>;
+  constexpr int NST = G::NST;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  const uint32_t base_u = (raw_u + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base_u - raw_u);
+  const uint32_t ring_u = base_u;
+  float* xbuf = reinterpret_cast<float*>(sm + NST * G::STAGE);
+  uint8_t* ctl = sm + NST * G::STAGE + G::XBUF_BYTES;
+  const uint32_t ctl_u = base_u + NST * G::STAGE + G::XBUF_BYTES;
+  auto full_bar = [&](int s) { return ctl_u + 8u * s; };
+  auto empty_bar = [&](int s) { return ctl_u + 8u * (NST + s); };
+  auto tfull_bar = [&](int acc) { return ctl_u + 8u * (2 * NST + acc); };
+  auto tempty_bar = [&](int acc) { return ctl_u + 8u * (2 * NST + 2 + acc); };
+  const uint32_t done_bar = ctl_u + 8u * (2 * NST + 4);
+  int* cw = reinterpret_cast<int*>(ctl + 8 * (2 * NST + 5));
+  volatile int* s_abort = cw;
+  volatile int* s_go = cw + 1;  // [2]: epilogue go flags, by tile parity
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(cw + 3);
+  int* s_issued = cw + 4;
+  int* s_consumed = cw + 5;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntiles = a.ntn * a.n_mb;
+  const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+  const int total_it = my_tiles * a.kblocks;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int acc = 0; acc < 2; ++acc) {
+      mbar_init(tfull_bar(acc), 1);
+      mbar_init(tempty_bar(acc), 4);
+    }
+    mbar_init(done_bar, 1);
+    *s_abort = 0;
+    s_go[0] = 0;
+    s_go[1] = 0;
+    *s_issued = 0;
+    *s_consumed = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(s_tmem), TC_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  auto tile_coords = [&](int tile_i, int& n, int& m) {
+    const int t = static_cast<int>(blockIdx.x) + tile_i * static_cast<int>(gridDim.x);
+    n = t / a.n_mb;
+    m = t - n * a.n_mb;
+  };
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      tma_prefetch_map(&mapA);
+      tma_prefetch_map(&mapW);
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      auto issue_w = [&](int it) {
+        int n, m;
+        tile_coords(it / a.kblocks, n, m);
+        const int kb = it % a.kblocks;
+        const int s = it % NST;
+        const uint32_t st = ring_u + static_cast<uint32_t>(s) * G::STAGE;
+        const int x0 = n * TC_N;
+        int nbox = 0;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) nbox += (x0 + 64 * j < a.V) ? 1 : 0;
+        mbar_arrive_expect_tx(full_bar(s), G::A_BYTES + static_cast<uint32_t>(nbox) * W_BOX_BYTES);
+        for (int j = 0; j < nbox; ++j)
+          tma_load_2d(st + G::A_BYTES + j * W_BOX_BYTES, &mapW, x0 + 64 * j, kb * TC_KB, full_bar(s), pol_w);
+      };
+      auto issue_a = [&](int it) {
+        int n, m;
+        tile_coords(it / a.kblocks, n, m);
+        const int kb = it % a.kblocks;
+        const int s = it % NST;
+        const uint32_t st = ring_u + static_cast<uint32_t>(s) * G::STAGE;
+        if (STACKED) {
+          tma_load_2d(st, &mapA, kb * TC_KB, 0, full_bar(s), pol_a);
+        } else {
+          tma_load_2d(st, &mapA, kb * TC_KB, m * 2 * TC_M, full_bar(s), pol_a);
+          tma_load_2d(st + A_BOX_BYTES, &mapA, kb * TC_KB, m * 2 * TC_M + TC_M, full_bar(s), pol_a);
+        }
+      };
+      const int npre = min(NST, total_it);
+      for (int it = 0; it < npre; ++it) issue_w(it);
+      pdl_wait();  // the activations come from the split kernel
+      for (int it = 0; it < npre; ++it) issue_a(it);
+      int issued = npre;
+      for (int it = npre; it < total_it; ++it) {
+        if (*s_abort) break;
+        const uint32_t par = static_cast<uint32_t>((it / NST) - 1) & 1u;
+        if (!wait_or_abort(empty_bar(it % NST), par, a.timeout_ns, s_abort)) {
+          fail(a.err, DEV_TIMEOUT_EMPTY, s_abort);
+          break;
+        }
+        issue_w(it);
+        issue_a(it);
+        issued = it + 1;
+      }
+      *s_issued = issued;
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(TC_M, TC_N);
+      int it = 0;
+      bool ok = true;
+      for (int tile_i = 0; tile_i < my_tiles && ok; ++tile_i) {
+        const int acc = tile_i & 1, use = tile_i >> 1;
+        if (use >= 1 && !wait_or_abort(tempty_bar(acc), static_cast<uint32_t>(use - 1) & 1u, a.timeout_ns, s_abort)) {
+          fail(a.err, DEV_TIMEOUT_EMPTY, s_abort);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * TC_ACC_COLS;
+        for (int kb = 0; kb < a.kblocks; ++kb, ++it) {
+          const int s = it % NST;
+          if (!wait_or_abort(full_bar(s), static_cast<uint32_t>(it / NST) & 1u, a.timeout_ns, s_abort)) {
+            fail(a.err, DEV_TIMEOUT_FULL, s_abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = ring_u + static_cast<uint32_t>(s) * G::STAGE;
+#pragma unroll
+          for (int ks = 0; ks < TC_KB / 16; ++ks) {
+            const uint64_t bd = sdesc_sw128(st + G::A_BYTES + ks * 2048u, W_BOX_BYTES, 1024u);
+            const uint64_t ah = sdesc_sw128(st + ks * 32u, 16u, 1024u);
+            tc_mma(d, ah, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+            if (!STACKED) {
+              const uint64_t al = sdesc_sw128(st + A_BOX_BYTES + ks * 32u, 16u, 1024u);
+              tc_mma(d, al, bd, idesc, 1u);
+            }
+          }
+          tc_commit(empty_bar(s));  // the stage is free once these MMAs have read it
+        }
+        if (ok) tc_commit(tfull_bar(acc));
+      }
+      *s_consumed = it;
+      // nothing of ours may still run on the tensor cores when the memory is released
+      tc_commit(done_bar);
+      if (!mbar_wait_bounded(done_bar, 0u, DEFAULT_TIMEOUT_NS)) raise_error(a.err, DEV_TIMEOUT_DRAIN);
+    }
+  } else {
+    // ================================================================ epilogue (128 threads)
+    pdl_wait();  // row_scale comes from the split kernel
+    const int et = tid - 64;
+    const int wq = warp & 3;  // tensor-memory lane quarter this warp may read
+    for (int tile_i = 0; tile_i < my_tiles; ++tile_i) {
+      const int acc = tile_i & 1, use = tile_i >> 1;
+      if (et == 0) {
+        bool ok = wait_or_abort(tfull_bar(acc), static_cast<uint32_t>(use) & 1u, a.timeout_ns, s_abort);
+        if (!ok) fail(a.err, DEV_TIMEOUT_FULL, s_abort);
+        s_go[tile_i & 1] = ok ? 1 : 0;
+      }
+      named_sync(1, 128);
+      if (!s_go[tile_i & 1]) break;  // uniform across the epilogue warps
+      tc_fence_after();
+      int n, m;
+      tile_coords(tile_i, n, m);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * wq) << 16) + static_cast<uint32_t>(acc) * TC_ACC_COLS;
+      const bool owner = STACKED ? (wq < 2) : true;  // stacked: lanes 64..127 hold the lo parts
+      const int row = STACKED ? 32 * wq + lane : m * TC_M + 32 * wq + lane;
+      const bool valid = owner && row < a.B;
+      const float rs = valid ? a.row_scale[row] : 0.f;
+      uint64_t lst[TC_LIST];
+#pragma unroll
+      for (int i = 0; i < TC_LIST; ++i) lst[i] = 0ull;
+      float* lrow = a.logits + static_cast<int64_t>(valid ? row : 0) * a.ld;
+#pragma unroll 1
+      for (int c = 0; c < TC_CHUNKS; ++c) {
+        float v[32];
+        tmem_ld32(taddr + 32u * c, v);
+        if (STACKED) {
+          if (wq >= 2) {
+            float* xr = xbuf + (32 * (wq - 2) + lane) * XBUF_PITCH;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xr[j] = v[j];
+          }
+          named_sync(2, 128);
+          if (wq < 2) {
+            const float* xr = xbuf + (32 * wq + lane) * XBUF_PITCH;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] += xr[j];
+          }
+          named_sync(2, 128);
+        }
+        const int col0 = n * TC_N + 32 * c;
+        if (valid && col0 < a.V) {
+          const int nv = min(32, a.V - col0);  // 16 or 32: V is a multiple of 16
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= rs;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            if (j < nv) *reinterpret_cast<float4*>(lrow + col0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < nv) list_insert(lst, composite(float_key(v[j]), col0 + j));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(a.lists + (static_cast<int64_t>(row) * a.ntn + n) * TC_LIST);
+#pragma unroll
+        for (int i = 0; i < TC_LIST / 2; ++i)
+          dst[i] = make_uint4(static_cast<uint32_t>(lst[2 * i]), static_cast<uint32_t>(lst[2 * i] >> 32),
+                              static_cast<uint32_t>(lst[2 * i + 1]), static_cast<uint32_t>(lst[2 * i + 1] >> 32));
+      }
+    }
+  }
+
+  // ================================================================ wind down
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    // copies issued for stages the MMA warp never consumed must land before the CTA leaves
+    for (int it = *s_consumed; it < *s_issued; ++it) {
+      if (!mbar_wait_bounded(full_bar(it % NST), static_cast<uint32_t>(it / NST) & 1u, DEFAULT_TIMEOUT_NS)) {
+        raise_error(a.err, DEV_TIMEOUT_DRAIN);
+        break;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, TC_TMEM_COLS);
+  }
+  pdl_launch_dependents();
+}
+
+template <bool STACKED>
+cudaError_t launch_tc_t(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, int grid,
+                        cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = TcGeom<STACKED>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<STACKED>, mapA, mapW, a);
+}
+
+}  // namespace
+
+cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, int stacked, int grid,
+                      cudaStream_t stream, bool pdl) {
+  return stacked ? launch_tc_t<true>(a, mapA, mapW, grid, stream, pdl)
+                 : launch_tc_t<false>(a, mapA, mapW, grid, stream, pdl);
+}
+
+cudaError_t prepare_tc_gemm(int max_smem_optin) {
+  if (static_cast<int>(TcGeom<false>::SMEM) > max_smem_optin || static_cast<int>(TcGeom<true>::SMEM) > max_smem_optin)
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(lmhead_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(TcGeom<false>::SMEM));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(lmhead_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(TcGeom<true>::SMEM));
+}
+
+}  // namespace tail

@@ -1,0 +1,262 @@
+// Global top-k and sampler of the tensor-core path ("GPT-OSS Tail Chunked
+// Megakernel Kernel API Reference", section "Background" — stage-1 top-k per
+// vocabulary chunk, then one top-k over the chunk results — and parameters `k`
+// and `sampling_params`).
+//
+// One CTA per batch row.  Input: for every column tile the row's top TC_LIST
+// composites (value desc, index asc), written by the tensor-core lm_head, and
+// the row's fp32 logits.
+//   1. x = the K-th largest key among the first q = ceil(K / ntn) entries of
+//      every list.  These are K distinct elements, so the row's K-th largest
+//      element has key >= x.  (If q exceeds the list length, x = 0.)
+//   2. Every element with key >= x is gathered: from a list whose last entry
+//      is below x, the list holds all of its tile's elements >= x; a list whose
+//      last entry is >= x (a tile with more than TC_LIST elements at or above
+//      x) is replaced by a scan of that tile's logits row.
+//   3. The exact top K of the gathered set, sorted by (value desc, index asc),
+//      is written out and the row's token is drawn from it.
+#include "common.cuh"
+#include "internal.h"
+#include "sampler.cuh"
+#include "select.cuh"
+#include "tc_internal.h"
+
+namespace tail {
+
+namespace {
+
+int next_pow2_host(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+__global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ uint32_t s_red[64];
+  __shared__ uint32_t s_list[SEL_BLOCK_BUCKET_MAX];
+  __shared__ uint32_t s_misc[4];
+  __shared__ int s_nsat;
+  pdl_wait();  // lists and logits come from the lm_head kernel
+
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  const int K = a.K, ntn = a.ntn;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+  int32_t* idx = reinterpret_cast<int32_t*>(keys + a.capc);
+  uint64_t* comp = reinterpret_cast<uint64_t*>(idx + a.capc);
+  uint64_t* sorted = comp + a.sortP;
+  float* ebuf = reinterpret_cast<float*>(sorted + K);
+  int* cnt = reinterpret_cast<int*>(ebuf + K);  // [ntn]: list entries >= x (0 for a saturated list)
+  int* off = cnt + ntn;                         // [ntn + 1]: exclusive scan of the counts
+  int* sat = off + ntn + 1;                     // [ntn]: saturated lists
+
+  // keeps the top K of keys/idx[0..n) (n > K), in place; returns K
+  auto fold = [&](int n) {
+    for (int j = tid; j < a.sortP; j += nt) comp[j] = 0ull;
+    __syncthreads();
+    block_top_composites(keys, idx, n, K, comp, s_red, s_list, s_misc);
+    for (int j = tid; j < K; j += nt) {
+      keys[j] = composite_key(comp[j]);
+      idx[j] = composite_idx(comp[j]);
+    }
+    __syncthreads();
+    return K;
+  };
+
+  for (int row = blockIdx.x; row < a.B; row += gridDim.x) {
+    const uint64_t* L = a.lists + static_cast<int64_t>(row) * ntn * TC_LIST;
+    const float* lg = a.logits + static_cast<int64_t>(row) * a.ld;
+
+    // ---- 1. the bound x from the first q entries of every list (when the lists
+    // hold fewer than K entries, x = 0 makes every list saturated: all logits are scanned)
+    const int q = (K + ntn - 1) / ntn;
+    uint32_t x = 0u;
+    if (tid == 0) s_nsat = 0;
+    if (q <= TC_LIST) {
+      const int nh = q * ntn;
+      for (int j = tid; j < nh; j += nt) keys[j] = composite_key(__ldcg(L + (j / q) * TC_LIST + (j % q)));
+      __syncthreads();
+      x = block_kth_key(keys, nh, K, s_red, s_list, s_misc).key;
+    }
+    __syncthreads();
+
+    // ---- 2a. per list: how many entries reach x, or saturated
+    for (int j = tid; j < ntn; j += nt) {
+      const uint4* src = reinterpret_cast<const uint4*>(L + static_cast<int64_t>(j) * TC_LIST);
+      int c = 0;
+      uint32_t last = 0;
+#pragma unroll
+      for (int i = 0; i < TC_LIST / 2; ++i) {
+        const uint4 w = __ldcg(src + i);
+        c += w.y >= x ? 1 : 0;  // composite key = high word
+        c += w.w >= x ? 1 : 0;
+        last = w.w;
+      }
+      if (last >= x) {
+        cnt[j] = 0;
+        sat[atomicAdd(&s_nsat, 1)] = j;
+      } else {
+        cnt[j] = c;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive scan of cnt into off
+      const int per = (ntn + 31) / 32;
+      const int s0 = min(ntn, lane * per), s1 = min(ntn, s0 + per);
+      int loc = 0;
+      for (int s = s0; s < s1; ++s) loc += cnt[s];
+      int incl = loc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      int run = incl - loc;
+      for (int s = s0; s < s1; ++s) {
+        off[s] = run;
+        run += cnt[s];
+      }
+      if (lane == 31) off[ntn] = incl;
+    }
+    __syncthreads();
+
+    // ---- 2b. gather the list entries >= x (in capacity-sized runs of lists, folding between runs)
+    int ncand = 0;
+    int start = 0;
+    while (start < ntn) {
+      // lists [start, end) whose entries fit behind the ncand already held
+      int lo = start, hi = ntn;
+      while (lo < hi) {  // largest end with off[end] - off[start] + ncand <= capc
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] - off[start] + ncand <= a.capc) lo = mid; else hi = mid - 1;
+      }
+      const int end = lo > start ? lo : start + 1;  // one list (<= TC_LIST entries) always fits after a fold
+      for (int j = start + tid; j < end; j += nt) {
+        const int c = cnt[j];
+        const int p = ncand + off[j] - off[start];
+        const uint64_t* src = L + static_cast<int64_t>(j) * TC_LIST;
+        for (int i = 0; i < c; ++i) {
+          const uint64_t e = __ldcg(src + i);
+          keys[p + i] = composite_key(e);
+          idx[p + i] = composite_idx(e);
+        }
+      }
+      ncand += off[end] - off[start];
+      __syncthreads();
+      start = end;
+      if (start < ntn && ncand > K) ncand = fold(ncand);
+    }
+
+    // ---- 2c. saturated lists: scan their tiles' logits
+    const int nsat = s_nsat;
+    for (int si = 0; si < nsat; ++si) {
+      if (ncand + TC_N > a.capc) ncand = fold(ncand);
+      const int j = sat[si];
+      const int c0 = j * TC_N, c1 = min(a.V, c0 + TC_N);
+      if (tid == 0) s_misc[3] = 0u;
+      __syncthreads();
+      for (int cidx = c0 + tid; cidx < c1; cidx += nt) {
+        const uint32_t kv = float_key(__ldcg(lg + cidx));
+        if (kv >= x) {
+          const int p = ncand + static_cast<int>(atomicAdd(&s_misc[3], 1u));
+          keys[p] = kv;
+          idx[p] = cidx;
+        }
+      }
+      __syncthreads();
+      ncand += static_cast<int>(s_misc[3]);
+      __syncthreads();
+    }
+
+    // ---- 3. exact top K, sorted; tokens
+    const int want = min(K, ncand);
+    int nr = ncand;
+    if (ncand <= RANK_SORT_MAX) {
+      for (int j = tid; j < ncand; j += nt) comp[j] = composite(keys[j], idx[j]);
+      __syncthreads();
+    } else {
+      for (int j = tid; j < a.sortP; j += nt) comp[j] = 0ull;
+      __syncthreads();
+      block_top_composites(keys, idx, ncand, want, comp, s_red, s_list, s_misc);
+      nr = want;
+    }
+    // composites are distinct: rank(i) = #{j : comp[j] > comp[i]} is i's position
+    for (int i = tid; i < nr; i += nt) {
+      const uint64_t ci = comp[i];
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+      int j = 0;
+      for (; j + 4 <= nr; j += 4) {
+        r0 += comp[j] > ci;
+        r1 += comp[j + 1] > ci;
+        r2 += comp[j + 2] > ci;
+        r3 += comp[j + 3] > ci;
+      }
+      for (; j < nr; ++j) r0 += comp[j] > ci;
+      const int rank = (r0 + r1) + (r2 + r3);
+      if (rank < want) sorted[rank] = ci;
+    }
+    __syncthreads();
+    for (int j = tid; j < want; j += nt) {
+      a.topk_val[static_cast<int64_t>(row) * a.topk_ld + j] = key_float(composite_key(sorted[j]));
+      a.topk_idx[static_cast<int64_t>(row) * a.topk_ld + j] = composite_idx(sorted[j]);
+    }
+    if (a.params != nullptr && a.tokens != nullptr && warp == 0) {
+      const int32_t tok = sample_sorted_row(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols, sorted, want, ebuf);
+      if (lane == 0) a.tokens[row] = tok;
+    }
+    __syncthreads();
+  }
+  pdl_launch_dependents();
+}
+
+}  // namespace
+
+bool plan_merge(int K, int ntn, int dyn_max, int* capc, int* sortP, int* smem_bytes) {
+  const int sp = next_pow2_host(K) > RANK_SORT_MAX ? next_pow2_host(K) : RANK_SORT_MAX;
+  const int fixed = sp * 8 + K * 8 + K * 4 + (3 * ntn + 1) * 4;
+  const int q = (K + ntn - 1) / ntn;
+  const int heads = q <= TC_LIST ? q * ntn : 0;
+  // the candidate buffer also holds the heads, and must take K plus one saturated tile
+  int want = (TC_LIST - 1) * ntn + TC_N + K;
+  if (want < heads) want = heads;
+  if (want < 2 * K) want = 2 * K;
+  want = (want + 3) & ~3;
+  int cap = (dyn_max - fixed) / 8;
+  cap &= ~3;
+  if (cap > want) cap = want;
+  if (cap < heads || cap < K + TC_N || cap < 2 * K) return false;
+  *capc = cap;
+  *sortP = sp;
+  *smem_bytes = fixed + cap * 8;
+  return true;
+}
+
+cudaError_t launch_merge(const MergeArgs& a, int grid, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(MERGE_THREADS);
+  cfg.dynamicSmemBytes = a.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, merge_lists_kernel, a);
+}
+
+cudaError_t prepare_tc(int max_smem_optin, int* merge_dyn_max) {
+  cudaError_t e = prepare_tc_gemm(max_smem_optin);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, merge_lists_kernel);
+  if (e != cudaSuccess) return e;
+  // at most half the opt-in limit, so two rows' merges share an SM
+  int dyn = (max_smem_optin - static_cast<int>(fa.sharedSizeBytes)) / 2 - 1024;
+  e = cudaFuncSetAttribute(merge_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+  if (e != cudaSuccess) return e;
+  *merge_dyn_max = dyn;
+  return cudaSuccess;
+}
+
+}  // namespace tail

@@ -16,6 +16,7 @@
 // Rows in [B, B_pad) are written as zeros so the last m-tile is complete.
 #include "common.cuh"
 #include "internal.h"
+#include "tc_internal.h"
 
 namespace tail {
 
@@ -112,7 +113,76 @@ __global__ void __launch_bounds__(RMS_THREADS) rms_pack_kernel(RmsArgs a) {
   if (threadIdx.x == 0) a.row_scale[b] = a.deferred ? rstd : 1.0f;
 }
 
+// The same RMSNorm for the tensor-core path: the hi and lo parts of row b go
+// to two plain bf16 rows of the activation buffer (K contiguous), laid out as
+// tc_act_rows describes.  rstd is computed exactly as in rms_pack_kernel.
+template <int DT>
+__global__ void __launch_bounds__(RMS_THREADS) rms_split_kernel(SplitArgs a) {
+  pdl_wait();  // the activation buffer is reused across steps
+  pdl_launch_dependents();
+  __shared__ float red[RMS_THREADS / 32];
+  __shared__ float s_rstd;
+  const int b = blockIdx.x;
+  const int H = a.H;
+  const int64_t row = static_cast<int64_t>(b) * H;
+  const int active_end = a.zero_pad ? H : a.Hu;
+  float ss = 0.f;
+  for (int h = threadIdx.x; h < active_end; h += RMS_THREADS) {
+    const float v = load_widen<DT>(a.hidden, row + h);
+    ss = fmaf(v, v, ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < RMS_THREADS / 32; ++w) t += red[w];
+    s_rstd = 1.0f / sqrtf(t / static_cast<float>(a.Hu) + a.eps);
+  }
+  __syncthreads();
+  const float rstd = s_rstd;
+  const float pre = a.deferred ? 1.0f : rstd;
+  const int64_t hi_row = a.stacked ? b : static_cast<int64_t>(b / 128) * 256 + (b % 128);
+  const int64_t lo_row = a.stacked ? 64 + b : hi_row + 128;
+  uint32_t* hi_dst = reinterpret_cast<uint32_t*>(a.act + hi_row * H);
+  uint32_t* lo_dst = reinterpret_cast<uint32_t*>(a.act + lo_row * H);
+  for (int h2 = 2 * threadIdx.x; h2 < H; h2 += 2 * RMS_THREADS) {
+    uint32_t hi[2], lo[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = h2 + j;
+      float v = 0.f;
+      if (h < active_end) v = (load_widen<DT>(a.hidden, row + h) * pre) * a.gamma[h];
+      hi[j] = bf16_bits(v);
+      lo[j] = bf16_bits(v - __uint_as_float(hi[j] << 16));
+    }
+    hi_dst[h2 >> 1] = hi[0] | (hi[1] << 16);
+    lo_dst[h2 >> 1] = lo[0] | (lo[1] << 16);
+  }
+  if (threadIdx.x == 0) a.row_scale[b] = a.deferred ? rstd : 1.0f;
+}
+
 }  // namespace
+
+cudaError_t launch_split(const SplitArgs& a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B);
+  cfg.blockDim = dim3(RMS_THREADS);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  switch (a.dtype) {
+    case 0: return cudaLaunchKernelEx(&cfg, rms_split_kernel<0>, a);
+    case 1: return cudaLaunchKernelEx(&cfg, rms_split_kernel<1>, a);
+    case 2: return cudaLaunchKernelEx(&cfg, rms_split_kernel<2>, a);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};

@@ -10,9 +10,14 @@
 
 #include <new>
 
+#include <cuda.h>
+
+#include <mutex>
+
 #include "../../include/tail.h"
 #include "abi_common.h"
 #include "internal.h"
+#include "tc_internal.h"
 
 using namespace tail;
 
@@ -37,6 +42,18 @@ struct tail_s {
   float* topk_val;
   int32_t* topk_idx;
   int* err;
+  // tensor-core path (gbs >= TC_MIN_ROWS)
+  uint16_t* tc_act;     // [tc_act_rows(gbs_max)][H] bf16 hi/lo rows
+  float* tc_rs;         // [gbs_max] row scales
+  uint64_t* tc_lists;   // [gbs_max][ntn][TC_LIST]
+  float* tc_logits;     // [gbs_max][V] fp32 logits when the caller passes none
+  int tc_ntn;
+  int merge_dyn;
+  int merge_capc, merge_sortP, merge_smem;
+  const void* tc_map_w_ptr;  // tensor maps cached for (w_t pointer, batch rows)
+  int tc_map_rows;
+  CUtensorMap tc_map_w;
+  CUtensorMap tc_map_a;
   // staging of tail_run_host
   void* st_hidden;
   float* st_params;
@@ -52,7 +69,7 @@ struct tail_s {
 };
 
 static constexpr int PROF_MAX = 256;
-static constexpr int PROF_EV = 3;
+static constexpr int PROF_EV = 4;  // before the RMSNorm kernel, after it, after the lm_head, after the merge
 
 namespace tail {
 
@@ -106,9 +123,43 @@ cudaError_t dalloc(T** p, size_t n, int64_t* total) {
 void free_all(tail_t* h) {
   void* ptrs[] = {h->apack,    h->row_scale, h->cand_key,  h->cand_idx,  h->logit_scratch, h->pub,
                   h->cand_cnt, h->bar,       h->topk_val,  h->topk_idx,  h->err,           h->st_hidden,
-                  h->st_params, h->st_tokens, h->st_logits};
+                  h->st_params, h->st_tokens, h->st_logits, h->tc_act,   h->tc_rs,         h->tc_lists,
+                  h->tc_logits};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime (the library links no driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows][cols] (cols contiguous), box box_cols x box_rows, 128-byte swizzle, zero fill outside.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                    uint32_t box_rows) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -153,7 +204,10 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   h->max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
   const int64_t npairs = cfg->V / 16;
   h->nslab = slab_count(npairs, h->num_sms, MAX_SLABS);
-  h->rows_pass = cfg->gbs_max < MAX_ROWS_PER_PASS ? cfg->gbs_max : MAX_ROWS_PER_PASS;
+  // batches of TC_MIN_ROWS rows or more run on the tensor-core path in one pass;
+  // smaller ones on the mma.sync lm_head
+  h->rows_pass = cfg->gbs_max < TC_MIN_ROWS - 1 ? cfg->gbs_max : TC_MIN_ROWS - 1;
+  const bool use_tc = cfg->gbs_max >= TC_MIN_ROWS;
   if (!prop.cooperativeLaunch) {
     delete h;
     return TAIL_ERR_UNSUPPORTED;
@@ -178,6 +232,19 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
     return TAIL_ERR_UNSUPPORTED;
   }
   h->pdl_ok = 1;
+  if (use_tc) {
+    cudaError_t te = prepare_tc(static_cast<int>(prop.sharedMemPerBlockOptin), &h->merge_dyn);
+    if (te != cudaSuccess) {
+      delete h;
+      return cuda_fail(te, "cudaFuncSetAttribute (tensor-core kernels)");
+    }
+    h->tc_ntn = tc_col_tiles(cfg->V);
+    if (!encode_tiled() ||
+        !plan_merge(cfg->k, h->tc_ntn, h->merge_dyn, &h->merge_capc, &h->merge_sortP, &h->merge_smem)) {
+      delete h;
+      return TAIL_ERR_UNSUPPORTED;
+    }
+  }
 
   const int R = h->rows_pass;
   const int Rpad = ((R + 7) / 8) * 8 < 8 ? 8 : ((R + 7) / 8) * 8;
@@ -201,6 +268,16 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
                      static_cast<size_t>(cfg->gbs_max) * cfg->H * elem_bytes(cfg->hidden_dtype), &tot);
   e = e ? e : dalloc(&h->st_params, static_cast<size_t>(cfg->gbs_max) * 4, &tot);
   e = e ? e : dalloc(&h->st_tokens, static_cast<size_t>(cfg->gbs_max), &tot);
+  if (use_tc) {
+    const size_t G = static_cast<size_t>(cfg->gbs_max);
+    e = e ? e : dalloc(&h->tc_act, static_cast<size_t>(tc_act_rows(cfg->gbs_max)) * cfg->H, &tot);
+    e = e ? e : dalloc(&h->tc_rs, G, &tot);
+    e = e ? e : dalloc(&h->tc_lists, G * h->tc_ntn * TC_LIST, &tot);
+    e = e ? e : dalloc(&h->tc_logits, G * cfg->V, &tot);
+    // rows of the activation buffer past a batch's rows still feed the MMA: keep them finite
+    if (e == cudaSuccess)
+      e = cudaMemset(h->tc_act, 0, static_cast<size_t>(tc_act_rows(cfg->gbs_max)) * cfg->H * sizeof(uint16_t));
+  }
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->bar, 0, sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(h->apack, 0, ksteps * mt_max * APACK_TILE_BYTES);
@@ -217,10 +294,93 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   return TAIL_OK;
 }
 
+// Batches of TC_MIN_ROWS rows or more: split -> tensor-core lm_head -> merge + sampler, one pass.
+static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
+                  int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits, float* out_topk_vals,
+                  int32_t* out_topk_idx, cudaStream_t stream) {
+  const tail_config& c = h->cfg;
+  const int stacked = tc_stacked(gbs);
+  const int n_mb = tc_mblocks(gbs);
+  if (h->tc_map_w_ptr != w_t || h->tc_map_rows != gbs) {
+    if (!encode_bf16_2d(&h->tc_map_w, w_t, static_cast<uint64_t>(c.V), static_cast<uint64_t>(c.H), 64, 64) ||
+        !encode_bf16_2d(&h->tc_map_a, h->tc_act, static_cast<uint64_t>(c.H),
+                        static_cast<uint64_t>(tc_act_rows(gbs)), 64, TC_M)) {
+      h->tc_map_w_ptr = nullptr;
+      set_last_error("cuTensorMapEncodeTiled rejected a tensor map of the tensor-core lm_head");
+      return TAIL_ERR_CUDA;
+    }
+    h->tc_map_w_ptr = w_t;
+    h->tc_map_rows = gbs;
+  }
+  cudaEvent_t* ev = (h->prof_on && h->prof_n < PROF_MAX) ? h->prof_ev + h->prof_n * PROF_EV : nullptr;
+  if (ev) {
+    ++h->prof_n;
+    cudaEventRecord(ev[0], stream);
+  }
+  SplitArgs sa;
+  sa.hidden = hidden;
+  sa.dtype = c.hidden_dtype;
+  sa.gamma = gamma;
+  sa.B = gbs;
+  sa.H = c.H;
+  sa.Hu = c.hidden_actual;
+  sa.eps = c.eps;
+  sa.zero_pad = c.zero_interleaved_pad ? 1 : 0;
+  sa.deferred = c.deferred_rms ? 1 : 0;
+  sa.stacked = stacked;
+  sa.act = h->tc_act;
+  sa.row_scale = h->tc_rs;
+  cudaError_t e = launch_split(sa, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch (split)");
+  if (ev) cudaEventRecord(ev[1], stream);
+
+  TcArgs ta;
+  ta.row_scale = h->tc_rs;
+  ta.logits = out_logits ? out_logits : h->tc_logits;
+  ta.ld = c.V;
+  ta.lists = h->tc_lists;
+  ta.err = h->err;
+  ta.B = gbs;
+  ta.V = c.V;
+  ta.ntn = h->tc_ntn;
+  ta.n_mb = n_mb;
+  ta.kblocks = (c.H + TC_KB - 1) / TC_KB;
+  ta.timeout_ns = h->wait_limit_ns;
+  const int ntiles = h->tc_ntn * n_mb;
+  e = launch_tc(ta, h->tc_map_a, h->tc_map_w, stacked, ntiles < h->num_sms ? ntiles : h->num_sms, stream, true);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch (tensor-core lm_head)");
+  if (ev) cudaEventRecord(ev[2], stream);
+
+  MergeArgs ma;
+  ma.lists = h->tc_lists;
+  ma.logits = ta.logits;
+  ma.ld = c.V;
+  ma.topk_val = out_topk_vals ? out_topk_vals : h->topk_val;
+  ma.topk_idx = out_topk_idx ? out_topk_idx : h->topk_idx;
+  ma.topk_ld = c.k;
+  ma.params = params;
+  ma.ncols = ncols;
+  ma.tokens = params ? out_tokens : nullptr;
+  ma.B = gbs;
+  ma.V = c.V;
+  ma.K = c.k;
+  ma.ntn = h->tc_ntn;
+  ma.capc = h->merge_capc;
+  ma.sortP = h->merge_sortP;
+  ma.smem_bytes = h->merge_smem;
+  e = launch_merge(ma, gbs, stream, true);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch (merge)");
+  if (ev) cudaEventRecord(ev[3], stream);
+  return TAIL_OK;
+}
+
 static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t,
                     const float* params, int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits,
                     float* out_topk_vals, int32_t* out_topk_idx, cudaStream_t stream) {
   const tail_config& c = h->cfg;
+  if (gbs >= TC_MIN_ROWS)
+    return run_tc(h, hidden, gamma, w_t, params, ncols, gbs, out_tokens, out_logits, out_topk_vals, out_topk_idx,
+                  stream);
   const int K = c.k;
   const int64_t npairs = c.V / 16;
   cudaError_t e = cudaSuccess;
@@ -299,7 +459,10 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     }
     if (!h->pdl_ok) e = launch_gemv(ga, stream, false);
     if (e != cudaSuccess) break;
-    if (ev) cudaEventRecord(ev[2], stream);
+    if (ev) {
+      cudaEventRecord(ev[2], stream);
+      cudaEventRecord(ev[3], stream);  // the merge runs inside the lm_head launch
+    }
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return TAIL_OK;
@@ -471,6 +634,7 @@ int tail_get_info(const tail_t* h, tail_info* out) {
   out->rows_per_pass = h->rows_pass;
   out->kernels_per_run = 2;
   out->scratch_bytes = h->scratch_bytes;
+  out->tc_min_rows = h->tc_lists ? TC_MIN_ROWS : 0;
   return TAIL_OK;
 }
 

@@ -69,9 +69,12 @@ typedef struct {
   int32_t merge_groups;     /* 0: the top-k merge runs inside the lm_head launch */
   int32_t lmhead_path;      /* 1: cooperative mma.sync lm_head + top-k + sampler launch;
                                2: the same, overlapped with the RMSNorm kernel (programmatic launch) */
-  int32_t rows_per_pass;    /* rows one lm_head pass covers (larger gbs runs several passes) */
-  int32_t kernels_per_run;  /* kernel launches of one tail_run with gbs <= rows_per_pass */
+  int32_t rows_per_pass;    /* rows one mma.sync lm_head pass covers */
+  int32_t kernels_per_run;  /* kernel launches of one tail_run on the mma.sync path */
   int64_t scratch_bytes;    /* device scratch owned by the handle */
+  int32_t tc_min_rows;      /* runs with gbs >= this take the tensor-core path (split, tcgen05
+                               lm_head with per-tile candidate lists, merge + sampler: 3 kernels,
+                               one pass); 0 when gbs_max is below it */
 } tail_info;
 
 /*
@@ -195,8 +198,9 @@ int tail_check(tail_t* h);
  * record of up to 256 lm_head passes.
  * tail_profile_read synchronises on the recorded events and returns, for the
  * passes recorded since enabling, the summed device milliseconds of each
- * kernel in kernel_ms[2] = {rms_rows, lm_head + top-k + sampler} and their
- * count in *passes.
+ * kernel in kernel_ms[3] = {RMSNorm, lm_head, merge + sampler} and their count
+ * in *passes.  On the mma.sync path the top-k and sampler run inside the
+ * lm_head launch, so the third entry is 0.
  */
 int tail_profile_enable(tail_t* h, int enable);
 int tail_profile_read(tail_t* h, float* kernel_ms, int32_t* passes);

@@ -1,8 +1,9 @@
 """tail_run_noalloc (static scratch, no handle, no device allocation) against tail_run.
 
-The allocation-free entry point launches the same kernels as the handle path, so
-on the same inputs it must give the same logits (within the logit tolerance,
-bitwise when both run one pass) and the same tokens.  Each comparison makes two
+The allocation-free entry point launches the same mma.sync kernels as the
+handle path does for batches of up to 8 rows, so there the results must be
+bitwise equal; larger batches (several passes here, the tensor-core path in
+the handle) must agree within the logit tolerance, with the same tokens.  Each comparison makes two
 calls in a row on one stream, with different inputs, before synchronising, so
 the second call also proves that the per-call reset of the shared scratch
 works.  The file is collected last so that it also runs after every other GPU
@@ -85,6 +86,7 @@ def compare(ref, got, bitwise):
 SMALL = [
     # B, H, V, k, dtype, Hu, zero_pad
     (5, 128, 1024, 200, "f16", None, 1),     # k above the slab width
+    (8, 96, 4800, 64, "bf16", 90, 1),        # zero pads at interleaved lanes
     (9, 80, 3200, 33, "f32", 72, 0),         # lanes beyond hidden_actual ignored
     (17, 64, 2048, 17, "bf16", None, 1),
     (70, 32, 1024, 8, "f32", None, 1),       # more rows than one pass
@@ -100,7 +102,8 @@ def test_noalloc_small_shapes_match_handle(shape):
     refs = [run_handle(w, hidden, gamma, w_t, params), run_handle(w, b[0], gamma, w_t, b[1])]
     gots = run_noalloc_twice(w, (hidden, params), b, gamma, w_t)
     for ref, got in zip(refs, gots):
-        compare(ref, got, bitwise=True)  # same rows per pass as the handle: same plan
+        # up to 8 rows both run the same mma.sync kernel; larger batches take the handle's tensor-core path
+        compare(ref, got, bitwise=B <= 8)
 
 
 @pytest.fixture(scope="module")
