@@ -62,20 +62,24 @@ def algorithmic_bytes(w, emit: bool) -> dict:
     return {"lm_head": lm_head, "step": step}
 
 
-# the translation unit of the dominant (lm_head + top-k + sampler) kernel and the headers it includes
-ROOFLINE_KERNEL_SOURCES = ("common.cuh", "internal.h", "lmhead_tail.cu", "sampler.cuh", "select.cuh")
+# per dominant kernel: its translation unit and the headers it includes
+ROOFLINE_KERNEL_SOURCES = {
+    "lmhead_tail_kernel": ("common.cuh", "internal.h", "lmhead_tail.cu", "sampler.cuh", "select.cuh"),
+    "lmhead_tc_kernel": ("common.cuh", "internal.h", "lmhead_tc.cu", "select.cuh", "tc_common.cuh",
+                         "tc_internal.h"),
+}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str = "lmhead_tail_kernel") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_sampling_tail_gb300", "csrc")
-    for f in ROOFLINE_KERNEL_SOURCES:
+    for f in ROOFLINE_KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str, emit: bool):
+def ncu_traffic(workload: str, emit: bool, kernel: str):
     """DRAM bytes per lm_head launch from the committed ncu summary, when it matches these sources."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
@@ -83,7 +87,9 @@ def ncu_traffic(workload: str, emit: bool):
     with open(p) as f:
         d = json.load(f)
     ent = d.get(f"{workload}{'_emit' if emit else ''}")
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("kernel", "lmhead_tail_kernel") != kernel:
+        return None
+    if ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -141,10 +147,16 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+CPU_SAMPLE_ROWS = 64  # larger batches are timed on their first 64 rows (the metric is per row)
+
+
 def cpu_oracle_step(w, nthreads):
+    """One oracle pass over the workload's first min(B, CPU_SAMPLE_ROWS) rows; returns the rows done."""
     import oracle
-    oracle.tail(w.hidden, w.hidden_dtype, w.gamma, w.w_t, w.Hu, w.k, w.eps, w.zero_pad, w.params,
+    n = min(w.B, CPU_SAMPLE_ROWS)
+    oracle.tail(w.hidden[:n], w.hidden_dtype, w.gamma, w.w_t, w.Hu, w.k, w.eps, w.zero_pad, w.params[:n],
                 nthreads=nthreads)
+    return n
 
 
 def cpu_baseline(w, budget_s=12.0, max_steps=20):
@@ -153,14 +165,16 @@ def cpu_baseline(w, budget_s=12.0, max_steps=20):
     nthreads = oracle.default_threads()
     times = []
     t_all = time.perf_counter()
+    rows = w.B
     while len(times) < max_steps and time.perf_counter() - t_all < budget_s:
         t0 = time.perf_counter()
-        cpu_oracle_step(w, nthreads)
+        rows = cpu_oracle_step(w, nthreads)
         times.append(time.perf_counter() - t0)
     sec = statistics.median(times)
-    return {"value": w.B / sec, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
-            "us_per_step": sec * 1e6,
-            "sample": f"{len(times)} whole steps of the {w.name} workload ({w.B} rows x V={w.V}), median"}
+    what = "whole steps" if rows == w.B else f"passes over the first {rows} of its {w.B} rows"
+    return {"value": rows / sec, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
+            "us_per_step": sec * 1e6 * w.B / rows,
+            "sample": f"{len(times)} {what} of the {w.name} workload (V={w.V}), median"}
 
 
 def run_reference(args, w):
@@ -170,12 +184,13 @@ def run_reference(args, w):
     for _ in range(max(0, args.warmup if args.warmup < 2 else 1)):
         cpu_oracle_step(w, nthreads)
     times = []
+    rows = w.B
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        cpu_oracle_step(w, nthreads)
+        rows = cpu_oracle_step(w, nthreads)
         times.append(time.perf_counter() - t0)
     total = sum(times)
-    value = w.B * args.steps / total
+    value = rows * args.steps / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
@@ -183,7 +198,7 @@ def run_reference(args, w):
         "config": {"workload": w.name, "gbs": w.B, "H": w.H, "V": w.V, "k": w.k, "emit_logits": False,
                    "hidden_dtype": w.hidden_dtype},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
-                         "sample": f"{args.steps} whole steps of {w.name}"},
+                         "sample": f"{args.steps} passes over {rows} of the {w.B} rows of {w.name}"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -223,8 +238,12 @@ def main():
     t = dst.Tail(w.H, w.V, w.k, w.B, hidden_actual=w.Hu, eps=w.eps, hidden_dtype=w.hidden_dtype,
                  zero_interleaved_pad=bool(w.zero_pad), device=local_rank)
     stream = torch.cuda.Stream(dev)
-    passes = (w.B + t.info.rows_per_pass - 1) // t.info.rows_per_pass
-    launches_per_step = t.info.kernels_per_run * passes
+    tc_path = t.info.tc_min_rows > 0 and w.B >= t.info.tc_min_rows
+    if tc_path:  # split -> tensor-core lm_head -> merge + sampler, one pass
+        passes, launches_per_step, kernel = 1, 3, "lmhead_tc_kernel"
+    else:        # rms_rows -> cooperative lm_head + top-k + sampler, per pass
+        passes = (w.B + t.info.rows_per_pass - 1) // t.info.rows_per_pass
+        launches_per_step, kernel = t.info.kernels_per_run * passes, "lmhead_tail_kernel"
 
     def step():
         t.run(hidden, gamma, w_t, params, out_tokens=tokens, out_logits=logits, stream=stream)
@@ -269,7 +288,7 @@ def main():
             step()
     kms, npass = dst.tail_profile_read(t.h)
     dst.tail_profile_enable(t.h, False)
-    lm_ms = kms["lm_head"] / max(1, npass)  # the dominant kernel: lm_head + top-k + sampler
+    lm_ms = kms["lm_head"] / max(1, npass)  # the dominant kernel (per pass)
     kshare = {k: v / max(1e-9, sum(kms.values())) for k, v in kms.items()}
 
     # ---------------- end to end through the host-buffer entry point
@@ -310,8 +329,29 @@ def main():
 
     pk, pk_kind = peaks()
     ab = algorithmic_bytes(w, emit)
-    achieved = ab["lm_head"] / (lm_ms / 1e3) / 1e9
+    lm_bytes = ab["lm_head"] if passes == 1 else 2 * w.H * w.V + (4 * (w.B // passes) * w.V if emit else 0)
+    achieved = lm_bytes / (lm_ms / 1e3) / 1e9
     step_gbs = ab["step"] / (ms_step / 1e3) / 1e9
+    # algorithmic flops of one lm_head launch (the hi + lo split executes twice as many on the tensor cores)
+    flops = 2.0 * (w.B if passes == 1 else w.B // passes) * w.H * w.V
+    tflops = flops / (lm_ms / 1e3) / 1e12
+    t_hbm = lm_bytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops_sustained"] * 1e12)
+    if tc_path and t_tc > t_hbm:
+        roof = {"bound": "tensor", "kernel": kernel, "achieved": tflops, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": tflops / pk["bf16_tflops_sustained"],
+                "peak_kind": f"{pk_kind} sustained cuBLAS bf16 (the kernel is timed in a seconds-long loop)",
+                "algorithmic_flops_per_launch": flops,
+                "executed_tensor_tflops": 2 * tflops,
+                "executed_frac": 2 * tflops / pk["bf16_tflops_sustained"],
+                "hbm_gbs": achieved, "hbm_frac": achieved / pk["hbm_gbs"],
+                "launch_us": lm_ms * 1e3, "traffic": ncu_traffic(w.name, emit, kernel)}
+    else:
+        roof = {"bound": "hbm", "kernel": kernel, "achieved": achieved,
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                "peak_kind": f"{pk_kind} copy bandwidth", "frac_of_spec_8tbs": achieved / SPEC_HBM_GBS,
+                "algorithmic_bytes_per_launch": lm_bytes, "launch_us": lm_ms * 1e3,
+                "tensor_tflops": tflops, "traffic": ncu_traffic(w.name, emit, kernel)}
     line = {
         "metric": METRIC, "value": rows_s, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
@@ -326,11 +366,7 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "step_hbm_gbs": step_gbs,
         "step_frac_of_spec_8tbs": step_gbs / SPEC_HBM_GBS,
-        "roofline": {"bound": "hbm", "kernel": "lmhead_tail_kernel", "achieved": achieved,
-                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                     "peak_kind": f"{pk_kind} copy bandwidth", "frac_of_spec_8tbs": achieved / SPEC_HBM_GBS,
-                     "algorithmic_bytes_per_launch": ab["lm_head"], "launch_us": lm_ms * 1e3,
-                     "traffic": ncu_traffic(w.name, emit)},
+        "roofline": roof,
         "kernel_us": {k: 1e3 * v / max(1, npass) for k, v in kms.items()},
         "kernel_share": kshare,
         "gpu_launches": launches_per_step * args.steps,

@@ -11,14 +11,16 @@
 //   warp 0     TMA producer: per ring stage one 64-wide k slice of the
 //              activation tile (hi and lo: two 128 x 64 boxes, or one box
 //              holding both when the batch fits in 64 rows) and of the weight
-//              tile (three 64 x 64 boxes, N = 192 columns), 128-byte swizzle.
-//   warp 1     tensor-memory owner and MMA issuer: M = 128, N = 192, K = 16
+//              tile (TC_N / 64 boxes of 64 x 64), 128-byte swizzle.
+//   warp 1     tensor-memory owner and MMA issuer: M = 128, N = TC_N, K = 16
 //              per instruction, A K-major, B (the weight, V contiguous)
 //              MN-major; two accumulators of 256 columns so the epilogue of
 //              one tile overlaps the MMAs of the next.
 //   warps 2-5  epilogue, one batch row per thread (tensor-memory lane): row
-//              scale, the fp32 logits row to global memory, and the tile's
-//              top TC_LIST candidates (value desc, index asc) for the merge.
+//              scale, the fp32 logits (each warp's 32 x 32 block staged in
+//              shared memory and written by a TMA tensor store), and the
+//              tile's top TC_LIST candidates (value desc, index asc) for the
+//              merge.
 // Tiles are (column tile n, m-block m) pairs taken round robin by the CTAs,
 // m varying fastest, so the CTAs that share a weight tile run it together and
 // the weight is read from HBM once.
@@ -42,15 +44,20 @@ constexpr uint32_t W_BOX_BYTES = 64 * 64 * 2;
 constexpr uint32_t A_BOX_BYTES = 128 * 64 * 2;
 constexpr int XBUF_PITCH = 33;                      // floats per row of the stacked hi/lo exchange
 constexpr int TC_CHUNKS = TC_N / 32;
+constexpr int TC_WBOX = TC_N / 64;                  // 64-column weight boxes per stage
+static_assert(TC_N % 64 == 0 && TC_N <= 256, "tile width: whole 64-column boxes, one accumulator");
 
 template <bool STACKED>
 struct TcGeom {
   static constexpr uint32_t A_BYTES = STACKED ? A_BOX_BYTES : 2 * A_BOX_BYTES;
-  static constexpr uint32_t STAGE = A_BYTES + 3 * W_BOX_BYTES;
-  static constexpr int NST = STACKED ? 4 : 3;
-  static constexpr uint32_t XBUF_BYTES = 64 * XBUF_PITCH * 4;
+  static constexpr uint32_t STAGE = A_BYTES + TC_WBOX * W_BOX_BYTES;
+  static constexpr uint32_t TBUF_BYTES = 4 * 2 * 4096;  // per epilogue warp: two 32 x 32 fp32 store boxes
+  static constexpr int NST_FIT =
+      (227 * 1024 - 1024 - (STACKED ? (64 * XBUF_PITCH * 4 + 1023) / 1024 * 1024 : 0) - TBUF_BYTES - 256) / STAGE;
+  static constexpr int NST = NST_FIT < 5 ? NST_FIT : 5;
+  static constexpr uint32_t XBUF_BYTES = STACKED ? (64 * XBUF_PITCH * 4 + 1023) / 1024 * 1024 : 0;
   static constexpr uint32_t CTL_BYTES = 256;
-  static constexpr uint32_t SMEM = 1024 /* alignment slack */ + NST * STAGE + XBUF_BYTES + CTL_BYTES;
+  static constexpr uint32_t SMEM = 1024 /* alignment slack */ + NST * STAGE + XBUF_BYTES + TBUF_BYTES + CTL_BYTES;
 };
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
@@ -74,23 +81,28 @@ __device__ __forceinline__ void fail(int* err, int code, volatile int* abort_fla
   *abort_flag = 1;
 }
 
-// Inserts c into the descending list l (kept in registers: fully unrolled).
-__device__ __forceinline__ void list_insert(uint64_t (&l)[TC_LIST], uint64_t c) {
-  if (c <= l[TC_LIST - 1]) return;
-  l[TC_LIST - 1] = c;
+// Inserts (kc, ic) into the list (lk, li), kept in (key desc, column asc) order
+// in registers.  Columns arrive in increasing order, so a key equal to a
+// listed one goes after it (strict compares).  Every slot takes its new entry
+// from the old list in parallel (no serial bubble chain); a key at or below
+// the last one leaves the list unchanged.
+__device__ __forceinline__ void list_push(uint32_t (&lk)[TC_LIST], int32_t (&li)[TC_LIST], uint32_t kc, int32_t ic) {
+  bool gt[TC_LIST];
+#pragma unroll
+  for (int i = 0; i < TC_LIST; ++i) gt[i] = kc > lk[i];
 #pragma unroll
   for (int i = TC_LIST - 1; i > 0; --i) {
-    const uint64_t x = l[i - 1], y = l[i];
-    const bool sw = y > x;
-    l[i - 1] = sw ? y : x;
-    l[i] = sw ? x : y;
+    lk[i] = gt[i - 1] ? lk[i - 1] : (gt[i] ? kc : lk[i]);
+    li[i] = gt[i - 1] ? li[i - 1] : (gt[i] ? ic : li[i]);
   }
+  lk[0] = gt[0] ? kc : lk[0];
+  li[0] = gt[0] ? ic : li[0];
 }
 
 template <bool STACKED>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
-                     const TcArgs a) {
+                     const __grid_constant__ CUtensorMap mapL, const TcArgs a) {
   using G = TcGeom<STACKED>;
   constexpr int NST = G::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -99,8 +111,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint8_t* sm = smem_raw + (base_u - raw_u);
   const uint32_t ring_u = base_u;
   float* xbuf = reinterpret_cast<float*>(sm + NST * G::STAGE);
-  uint8_t* ctl = sm + NST * G::STAGE + G::XBUF_BYTES;
-  const uint32_t ctl_u = base_u + NST * G::STAGE + G::XBUF_BYTES;
+  float* tbuf = reinterpret_cast<float*>(sm + NST * G::STAGE + G::XBUF_BYTES);
+  uint8_t* ctl = sm + NST * G::STAGE + G::XBUF_BYTES + G::TBUF_BYTES;
+  const uint32_t ctl_u = base_u + NST * G::STAGE + G::XBUF_BYTES + G::TBUF_BYTES;
   auto full_bar = [&](int s) { return ctl_u + 8u * s; };
   auto empty_bar = [&](int s) { return ctl_u + 8u * (NST + s); };
   auto tfull_bar = [&](int acc) { return ctl_u + 8u * (2 * NST + acc); };
@@ -166,7 +179,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int x0 = n * TC_N;
         int nbox = 0;
 #pragma unroll
-        for (int j = 0; j < 3; ++j) nbox += (x0 + 64 * j < a.V) ? 1 : 0;
+        for (int j = 0; j < TC_WBOX; ++j) nbox += (x0 + 64 * j < a.V) ? 1 : 0;
         mbar_arrive_expect_tx(full_bar(s), G::A_BYTES + static_cast<uint32_t>(nbox) * W_BOX_BYTES);
         for (int j = 0; j < nbox; ++j)
           tma_load_2d(st + G::A_BYTES + j * W_BOX_BYTES, &mapW, x0 + 64 * j, kb * TC_KB, full_bar(s), pol_w);
@@ -249,6 +262,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     pdl_wait();  // row_scale comes from the split kernel
     const int et = tid - 64;
     const int wq = warp & 3;  // tensor-memory lane quarter this warp may read
+    const uint32_t tbuf_u = smem_u32(tbuf);
+    const uint64_t pol_l = policy_evict_first();
+    int store_n = 0;  // boxes this warp has stored (selects the double buffer)
+    if (lane == 0) tma_prefetch_map(&mapL);
     for (int tile_i = 0; tile_i < my_tiles; ++tile_i) {
       const int acc = tile_i & 1, use = tile_i >> 1;
       if (et == 0) {
@@ -266,10 +283,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int row = STACKED ? 32 * wq + lane : m * TC_M + 32 * wq + lane;
       const bool valid = owner && row < a.B;
       const float rs = valid ? a.row_scale[row] : 0.f;
-      uint64_t lst[TC_LIST];
+      uint32_t lk[TC_LIST];
+      int32_t li[TC_LIST];
 #pragma unroll
-      for (int i = 0; i < TC_LIST; ++i) lst[i] = 0ull;
-      float* lrow = a.logits + static_cast<int64_t>(valid ? row : 0) * a.ld;
+      for (int i = 0; i < TC_LIST; ++i) {
+        lk[i] = 0u;  // below every key of a finite value
+        li[i] = 0;
+      }
+      const int rbase = row - lane;  // first row of this warp's 32
 #pragma unroll 1
       for (int c = 0; c < TC_CHUNKS; ++c) {
         float v[32];
@@ -289,31 +310,51 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           named_sync(2, 128);
         }
         const int col0 = n * TC_N + 32 * c;
-        if (valid && col0 < a.V) {
+        if (owner && col0 < a.V) {  // warp-uniform
           const int nv = min(32, a.V - col0);  // 16 or 32: V is a multiple of 16
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] *= rs;
+          // the logits: this warp's 32 rows x 32 columns as one 128-byte-swizzled box, stored by TMA
+          // (rows past B and columns past V are clipped by the tensor map)
+          const uint32_t box = tbuf_u + static_cast<uint32_t>(wq * 2 + (store_n & 1)) * 4096u;
+          if (lane == 0) tma_store_wait_read<1>();  // the box written two chunks ago has been read
+          __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            if (j < nv) *reinterpret_cast<float4*>(lrow + col0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t dst = box + static_cast<uint32_t>(lane * 128 + ((q ^ (lane & 7)) << 4));
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(v[4 * q]), "f"(v[4 * q + 1]),
+                         "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
+                         : "memory");
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&mapL, col0, rbase, box, pol_l);
+            tma_store_commit();
+          }
+          ++store_n;
+          // this tile's top TC_LIST candidates of the row
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (j < nv) list_insert(lst, composite(float_key(v[j]), col0 + j));
+            const uint32_t kc = (valid && j < nv) ? float_key(v[j]) : 0u;
+            if (__any_sync(0xffffffffu, kc > lk[TC_LIST - 1])) list_push(lk, li, kc, col0 + j);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
-      if (valid) {
+      if (valid) {  // composites: key in the high word, ~column in the low word (0 for an empty slot)
         uint4* dst = reinterpret_cast<uint4*>(a.lists + (static_cast<int64_t>(row) * a.ntn + n) * TC_LIST);
 #pragma unroll
-        for (int i = 0; i < TC_LIST / 2; ++i)
-          dst[i] = make_uint4(static_cast<uint32_t>(lst[2 * i]), static_cast<uint32_t>(lst[2 * i] >> 32),
-                              static_cast<uint32_t>(lst[2 * i + 1]), static_cast<uint32_t>(lst[2 * i + 1] >> 32));
+        for (int i = 0; i < TC_LIST / 2; ++i) {
+          const uint32_t lo0 = lk[2 * i] ? 0xFFFFFFFFu - static_cast<uint32_t>(li[2 * i]) : 0u;
+          const uint32_t lo1 = lk[2 * i + 1] ? 0xFFFFFFFFu - static_cast<uint32_t>(li[2 * i + 1]) : 0u;
+          dst[i] = make_uint4(lo0, lk[2 * i], lo1, lk[2 * i + 1]);
+        }
       }
     }
+    if (lane == 0) tma_store_wait_all();  // the logits are in global memory before the CTA leaves
   }
 
   // ================================================================ wind down
@@ -338,8 +379,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 }
 
 template <bool STACKED>
-cudaError_t launch_tc_t(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, int grid,
-                        cudaStream_t stream, bool pdl) {
+cudaError_t launch_tc_t(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, const CUtensorMap& mapL,
+                        int grid, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(TC_THREADS);
@@ -350,15 +391,15 @@ cudaError_t launch_tc_t(const TcArgs& a, const CUtensorMap& mapA, const CUtensor
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<STACKED>, mapA, mapW, a);
+  return cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<STACKED>, mapA, mapW, mapL, a);
 }
 
 }  // namespace
 
-cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, int stacked, int grid,
-                      cudaStream_t stream, bool pdl) {
-  return stacked ? launch_tc_t<true>(a, mapA, mapW, grid, stream, pdl)
-                 : launch_tc_t<false>(a, mapA, mapW, grid, stream, pdl);
+cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, const CUtensorMap& mapL,
+                      int stacked, int grid, cudaStream_t stream, bool pdl) {
+  return stacked ? launch_tc_t<true>(a, mapA, mapW, mapL, grid, stream, pdl)
+                 : launch_tc_t<false>(a, mapA, mapW, mapL, grid, stream, pdl);
 }
 
 cudaError_t prepare_tc_gemm(int max_smem_optin) {

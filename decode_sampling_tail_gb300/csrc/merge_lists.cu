@@ -147,25 +147,28 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
       if (start < ntn && ncand > K) ncand = fold(ncand);
     }
 
-    // ---- 2c. saturated lists: scan their tiles' logits
+    // ---- 2c. saturated lists: scan their tiles' logits, as many tiles per pass as the buffer takes
     const int nsat = s_nsat;
-    for (int si = 0; si < nsat; ++si) {
+    for (int s0 = 0; s0 < nsat;) {
       if (ncand + TC_N > a.capc) ncand = fold(ncand);
-      const int j = sat[si];
-      const int c0 = j * TC_N, c1 = min(a.V, c0 + TC_N);
+      const int ng = min(nsat - s0, (a.capc - ncand) / TC_N);  // >= 1 after the fold
       if (tid == 0) s_misc[3] = 0u;
       __syncthreads();
-      for (int cidx = c0 + tid; cidx < c1; cidx += nt) {
-        const uint32_t kv = float_key(__ldcg(lg + cidx));
-        if (kv >= x) {
-          const int p = ncand + static_cast<int>(atomicAdd(&s_misc[3], 1u));
-          keys[p] = kv;
-          idx[p] = cidx;
+      for (int i = tid; i < ng * TC_N; i += nt) {
+        const int cidx = sat[s0 + i / TC_N] * TC_N + i % TC_N;
+        if (cidx < a.V) {
+          const uint32_t kv = float_key(__ldcg(lg + cidx));
+          if (kv >= x) {
+            const int p = ncand + static_cast<int>(atomicAdd(&s_misc[3], 1u));
+            keys[p] = kv;
+            idx[p] = cidx;
+          }
         }
       }
       __syncthreads();
       ncand += static_cast<int>(s_misc[3]);
       __syncthreads();
+      s0 += ng;
     }
 
     // ---- 3. exact top K, sorted; tokens

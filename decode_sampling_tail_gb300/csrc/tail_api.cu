@@ -50,10 +50,12 @@ struct tail_s {
   int tc_ntn;
   int merge_dyn;
   int merge_capc, merge_sortP, merge_smem;
-  const void* tc_map_w_ptr;  // tensor maps cached for (w_t pointer, batch rows)
+  const void* tc_map_w_ptr;  // tensor maps cached for (w_t pointer, logits pointer, batch rows)
+  const void* tc_map_l_ptr;
   int tc_map_rows;
   CUtensorMap tc_map_w;
   CUtensorMap tc_map_a;
+  CUtensorMap tc_map_l;
   // staging of tail_run_host
   void* st_hidden;
   float* st_params;
@@ -148,17 +150,19 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// 2-D bf16 tensor [rows][cols] (cols contiguous), box box_cols x box_rows, 128-byte swizzle, zero fill outside.
-bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                    uint32_t box_rows) {
+// 2-D tensor [rows][cols] (cols contiguous) of bf16 or fp32, box box_cols x box_rows, 128-byte swizzle,
+// zero fill outside on loads, clipped stores.
+bool encode_2d(CUtensorMap* map, const void* base, bool fp32, uint64_t cols, uint64_t rows, uint32_t box_cols,
+               uint32_t box_rows) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t strides[1] = {cols * (fp32 ? 4 : 2)};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -301,15 +305,18 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   const tail_config& c = h->cfg;
   const int stacked = tc_stacked(gbs);
   const int n_mb = tc_mblocks(gbs);
-  if (h->tc_map_w_ptr != w_t || h->tc_map_rows != gbs) {
-    if (!encode_bf16_2d(&h->tc_map_w, w_t, static_cast<uint64_t>(c.V), static_cast<uint64_t>(c.H), 64, 64) ||
-        !encode_bf16_2d(&h->tc_map_a, h->tc_act, static_cast<uint64_t>(c.H),
-                        static_cast<uint64_t>(tc_act_rows(gbs)), 64, TC_M)) {
+  float* logits = out_logits ? out_logits : h->tc_logits;
+  if (h->tc_map_w_ptr != w_t || h->tc_map_l_ptr != logits || h->tc_map_rows != gbs) {
+    if (!encode_2d(&h->tc_map_w, w_t, false, static_cast<uint64_t>(c.V), static_cast<uint64_t>(c.H), 64, 64) ||
+        !encode_2d(&h->tc_map_a, h->tc_act, false, static_cast<uint64_t>(c.H),
+                   static_cast<uint64_t>(tc_act_rows(gbs)), 64, TC_M) ||
+        !encode_2d(&h->tc_map_l, logits, true, static_cast<uint64_t>(c.V), static_cast<uint64_t>(gbs), 32, 32)) {
       h->tc_map_w_ptr = nullptr;
       set_last_error("cuTensorMapEncodeTiled rejected a tensor map of the tensor-core lm_head");
       return TAIL_ERR_CUDA;
     }
     h->tc_map_w_ptr = w_t;
+    h->tc_map_l_ptr = logits;
     h->tc_map_rows = gbs;
   }
   cudaEvent_t* ev = (h->prof_on && h->prof_n < PROF_MAX) ? h->prof_ev + h->prof_n * PROF_EV : nullptr;
@@ -336,7 +343,7 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
 
   TcArgs ta;
   ta.row_scale = h->tc_rs;
-  ta.logits = out_logits ? out_logits : h->tc_logits;
+  ta.logits = logits;
   ta.ld = c.V;
   ta.lists = h->tc_lists;
   ta.err = h->err;
@@ -347,7 +354,8 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   ta.kblocks = (c.H + TC_KB - 1) / TC_KB;
   ta.timeout_ns = h->wait_limit_ns;
   const int ntiles = h->tc_ntn * n_mb;
-  e = launch_tc(ta, h->tc_map_a, h->tc_map_w, stacked, ntiles < h->num_sms ? ntiles : h->num_sms, stream, true);
+  e = launch_tc(ta, h->tc_map_a, h->tc_map_w, h->tc_map_l, stacked, ntiles < h->num_sms ? ntiles : h->num_sms,
+                stream, true);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch (tensor-core lm_head)");
   if (ev) cudaEventRecord(ev[2], stream);
 

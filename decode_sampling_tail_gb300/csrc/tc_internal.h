@@ -64,9 +64,10 @@ struct MergeArgs {
 
 cudaError_t launch_split(const SplitArgs& a, cudaStream_t stream);
 // mapA: activation buffer [rows][H] bf16, box 64 x 128, 128-byte swizzle;
-// mapW: w_t [H][V] bf16, box 64 x 64, 128-byte swizzle.
-cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, int stacked, int grid,
-                      cudaStream_t stream, bool pdl);
+// mapW: w_t [H][V] bf16, box 64 x 64, 128-byte swizzle;
+// mapL: logits [B][V] fp32, box 32 x 32, 128-byte swizzle.
+cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, const CUtensorMap& mapL,
+                      int stacked, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_merge(const MergeArgs& a, int grid, cudaStream_t stream, bool pdl);
 cudaError_t prepare_tc_gemm(int max_smem_optin);
 // per device: shared-memory opt-in of the tensor-core kernels; returns the
