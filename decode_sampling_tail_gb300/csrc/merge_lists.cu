@@ -6,17 +6,18 @@
 // One CTA per batch row.  Input: for every column tile the row's top TC_LIST
 // composites (value desc, index asc), written by the tensor-core lm_head, and
 // the row's fp32 logits.
-//   1. x = the K-th largest key among the first q = ceil(K / ntn) entries of
-//      every list.  These are K distinct elements, so the row's K-th largest
-//      element has key >= x.  (If q exceeds the list length, x = 0.)
+//   1. x = the K-th largest key among all list entries.  These are distinct
+//      elements of the row, so the row's K-th largest element has key >= x.
+//      (With fewer than K entries in all, x = 0.)
 //   2. Every element with key >= x is gathered: from a list whose last entry
 //      is below x, the list holds all of its tile's elements >= x; a list whose
-//      last entry is >= x (a tile with more than TC_LIST elements at or above
-//      x) is replaced by a scan of that tile's logits row.
+//      last entry is >= x (a tile with TC_LIST or more elements at or above x)
+//      is replaced by a scan of that tile's logits row.
 //   3. The exact top K of the gathered set, sorted by (value desc, index asc),
 //      is written out and the row's token is drawn from it.
 #include "common.cuh"
 #include "internal.h"
+#include "radix_select.cuh"
 #include "sampler.cuh"
 #include "select.cuh"
 #include "tc_internal.h"
@@ -36,12 +37,15 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
   __shared__ uint32_t s_red[64];
   __shared__ uint32_t s_list[SEL_BLOCK_BUCKET_MAX];
   __shared__ uint32_t s_misc[4];
+  __shared__ uint32_t s_hist[256];
   __shared__ int s_nsat;
   pdl_wait();  // lists and logits come from the lm_head kernel
 
   const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
   const int K = a.K, ntn = a.ntn;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+  const int nl = ntn * TC_LIST;                           // list entries of a row
+  uint32_t* lk = reinterpret_cast<uint32_t*>(smem);       // [nl]: the keys of every list entry
+  uint32_t* keys = lk + nl;                               // [capc]: gathered candidates
   int32_t* idx = reinterpret_cast<int32_t*>(keys + a.capc);
   uint64_t* comp = reinterpret_cast<uint64_t*>(idx + a.capc);
   uint64_t* sorted = comp + a.sortP;
@@ -67,32 +71,29 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
     const uint64_t* L = a.lists + static_cast<int64_t>(row) * ntn * TC_LIST;
     const float* lg = a.logits + static_cast<int64_t>(row) * a.ld;
 
-    // ---- 1. the bound x from the first q entries of every list (when the lists
-    // hold fewer than K entries, x = 0 makes every list saturated: all logits are scanned)
-    const int q = (K + ntn - 1) / ntn;
-    uint32_t x = 0u;
-    if (tid == 0) s_nsat = 0;
-    if (q <= TC_LIST) {
-      const int nh = q * ntn;
-      for (int j = tid; j < nh; j += nt) keys[j] = composite_key(__ldcg(L + (j / q) * TC_LIST + (j % q)));
-      __syncthreads();
-      x = block_kth_key(keys, nh, K, s_red, s_list, s_misc).key;
+    // ---- 1. the bound x: K-th largest key of all list entries (x = 0 when there are fewer than K:
+    // every list is then saturated and all logits are scanned)
+    for (int j = tid; j < ntn; j += nt) {
+      const uint4* src = reinterpret_cast<const uint4*>(L + static_cast<int64_t>(j) * TC_LIST);
+      uint4 w[TC_LIST / 2];
+#pragma unroll
+      for (int i = 0; i < TC_LIST / 2; ++i) w[i] = __ldcg(src + i);
+#pragma unroll
+      for (int i = 0; i < TC_LIST / 2; ++i) {
+        lk[j * TC_LIST + 2 * i] = w[i].y;  // composite key = high word
+        lk[j * TC_LIST + 2 * i + 1] = w[i].w;
+      }
     }
+    if (tid == 0) s_nsat = 0;
     __syncthreads();
+    const uint32_t x = nl >= K ? block_kth_radix(lk, nl, K, s_hist, s_red, s_misc) : 0u;
 
     // ---- 2a. per list: how many entries reach x, or saturated
     for (int j = tid; j < ntn; j += nt) {
-      const uint4* src = reinterpret_cast<const uint4*>(L + static_cast<int64_t>(j) * TC_LIST);
       int c = 0;
-      uint32_t last = 0;
 #pragma unroll
-      for (int i = 0; i < TC_LIST / 2; ++i) {
-        const uint4 w = __ldcg(src + i);
-        c += w.y >= x ? 1 : 0;  // composite key = high word
-        c += w.w >= x ? 1 : 0;
-        last = w.w;
-      }
-      if (last >= x) {
+      for (int i = 0; i < TC_LIST; ++i) c += lk[j * TC_LIST + i] >= x ? 1 : 0;
+      if (lk[j * TC_LIST + TC_LIST - 1] >= x) {
         cnt[j] = 0;
         sat[atomicAdd(&s_nsat, 1)] = j;
       } else {
@@ -216,18 +217,16 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
 
 bool plan_merge(int K, int ntn, int dyn_max, int* capc, int* sortP, int* smem_bytes) {
   const int sp = next_pow2_host(K) > RANK_SORT_MAX ? next_pow2_host(K) : RANK_SORT_MAX;
-  const int fixed = sp * 8 + K * 8 + K * 4 + (3 * ntn + 1) * 4;
-  const int q = (K + ntn - 1) / ntn;
-  const int heads = q <= TC_LIST ? q * ntn : 0;
-  // the candidate buffer also holds the heads, and must take K plus one saturated tile
+  const int fixed = ntn * TC_LIST * 4 + sp * 8 + K * 8 + K * 4 + (3 * ntn + 1) * 4;
+  // the candidate buffer takes every non-saturated list entry, or folds to K when it cannot;
+  // it must hold K plus one saturated tile
   int want = (TC_LIST - 1) * ntn + TC_N + K;
-  if (want < heads) want = heads;
   if (want < 2 * K) want = 2 * K;
   want = (want + 3) & ~3;
   int cap = (dyn_max - fixed) / 8;
   cap &= ~3;
   if (cap > want) cap = want;
-  if (cap < heads || cap < K + TC_N || cap < 2 * K) return false;
+  if (cap < K + TC_N || cap < 2 * K) return false;
   *capc = cap;
   *sortP = sp;
   *smem_bytes = fixed + cap * 8;
