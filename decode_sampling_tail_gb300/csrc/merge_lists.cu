@@ -6,9 +6,11 @@
 // One CTA per batch row.  Input: for every column tile the row's top TC_LIST
 // composites (value desc, index asc), written by the tensor-core lm_head, and
 // the row's fp32 logits.
-//   1. x = the K-th largest key among all list entries.  These are distinct
+//   1. x = a lower bound (exact in its top 16 bits) of the K-th largest key
+//      among the list heads, each tile's largest element.  These are distinct
 //      elements of the row, so the row's K-th largest element has key >= x.
-//      (With fewer than K entries in all, x = 0.)
+//      (With fewer tiles than K, the K-th largest key of all list entries;
+//      with fewer entries than K, x = 0.)
 //   2. Every element with key >= x is gathered: from a list whose last entry
 //      is below x, the list holds all of its tile's elements >= x; a list whose
 //      last entry is >= x (a tile with TC_LIST or more elements at or above x)
@@ -17,7 +19,6 @@
 //      is written out and the row's token is drawn from it.
 #include "common.cuh"
 #include "internal.h"
-#include "radix_select.cuh"
 #include "sampler.cuh"
 #include "select.cuh"
 #include "tc_internal.h"
@@ -25,6 +26,8 @@
 namespace tail {
 
 namespace {
+
+constexpr int MERGE_HEADS_PER_LANE = 48;  // list heads one warp holds in registers: up to 1536 tiles
 
 int next_pow2_host(int x) {
   int p = 1;
@@ -37,7 +40,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
   __shared__ uint32_t s_red[64];
   __shared__ uint32_t s_list[SEL_BLOCK_BUCKET_MAX];
   __shared__ uint32_t s_misc[4];
-  __shared__ uint32_t s_hist[256];
+  __shared__ uint32_t s_x;
   __shared__ int s_nsat;
   pdl_wait();  // lists and logits come from the lm_head kernel
 
@@ -73,20 +76,50 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
 
     // ---- 1. the bound x: K-th largest key of all list entries (x = 0 when there are fewer than K:
     // every list is then saturated and all logits are scanned)
-    for (int j = tid; j < ntn; j += nt) {
-      const uint4* src = reinterpret_cast<const uint4*>(L + static_cast<int64_t>(j) * TC_LIST);
-      uint4 w[TC_LIST / 2];
+    constexpr int LPT = 4;  // lists per thread whose loads are in flight together
+    for (int j0 = 0; j0 < ntn; j0 += LPT * nt) {
+      uint4 w[LPT][TC_LIST / 2];
 #pragma unroll
-      for (int i = 0; i < TC_LIST / 2; ++i) w[i] = __ldcg(src + i);
+      for (int q = 0; q < LPT; ++q) {
+        const int j = j0 + q * nt + tid;
+        const uint4* src = reinterpret_cast<const uint4*>(L + static_cast<int64_t>(j < ntn ? j : 0) * TC_LIST);
 #pragma unroll
-      for (int i = 0; i < TC_LIST / 2; ++i) {
-        lk[j * TC_LIST + 2 * i] = w[i].y;  // composite key = high word
-        lk[j * TC_LIST + 2 * i + 1] = w[i].w;
+        for (int i = 0; i < TC_LIST / 2; ++i) w[q][i] = j < ntn ? __ldcg(src + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int q = 0; q < LPT; ++q) {
+        const int j = j0 + q * nt + tid;
+        if (j < ntn) {
+#pragma unroll
+          for (int i = 0; i < TC_LIST / 2; ++i) {
+            lk[j * TC_LIST + 2 * i] = w[q][i].y;  // composite key = high word
+            lk[j * TC_LIST + 2 * i + 1] = w[q][i].w;
+          }
+        }
       }
     }
     if (tid == 0) s_nsat = 0;
     __syncthreads();
-    const uint32_t x = nl >= K ? block_kth_radix(lk, nl, K, s_hist, s_red, s_misc) : 0u;
+    uint32_t x;
+    if (ntn >= K && ntn <= 32 * MERGE_HEADS_PER_LANE) {
+      // the list heads (each tile's largest element) are K or more distinct elements: one warp finds
+      // a lower bound of their K-th largest key, exact in its top 16 bits
+      if (warp == 0) {
+        uint32_t hk[MERGE_HEADS_PER_LANE];
+#pragma unroll
+        for (int i = 0; i < MERGE_HEADS_PER_LANE; ++i) {
+          const int j = i * 32 + lane;
+          hk[i] = j < ntn ? lk[j * TC_LIST] : 0u;
+        }
+        const uint32_t b = warp_bound16_regs(hk, K);
+        if (lane == 0) s_x = b;
+      }
+      __syncthreads();
+      x = s_x;
+    } else {
+      // few tiles (or very many): the K-th largest key over every list entry, or 0 when they are fewer than K
+      x = nl >= K ? block_kth_key(lk, nl, K, s_red, s_list, s_misc).key : 0u;
+    }
 
     // ---- 2a. per list: how many entries reach x, or saturated
     for (int j = tid; j < ntn; j += nt) {
@@ -218,10 +251,11 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
 bool plan_merge(int K, int ntn, int dyn_max, int* capc, int* sortP, int* smem_bytes) {
   const int sp = next_pow2_host(K) > RANK_SORT_MAX ? next_pow2_host(K) : RANK_SORT_MAX;
   const int fixed = ntn * TC_LIST * 4 + sp * 8 + K * 8 + K * 4 + (3 * ntn + 1) * 4;
-  // the candidate buffer takes every non-saturated list entry, or folds to K when it cannot;
-  // it must hold K plus one saturated tile
-  int want = (TC_LIST - 1) * ntn + TC_N + K;
-  if (want < 2 * K) want = 2 * K;
+  // the candidate buffer holds the gathered elements and folds to the top K when full: sized for the
+  // usual few hundred (ties in groups of a few) with room for K plus one saturated tile, small enough
+  // for several rows' merges to share an SM
+  int want = 4 * K + TC_N;
+  if (want < 2048) want = 2048;
   want = (want + 3) & ~3;
   int cap = (dyn_max - fixed) / 8;
   cap &= ~3;
