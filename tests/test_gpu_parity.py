@@ -239,3 +239,53 @@ def test_large_g1024_sampled_rows():
     assert np.all((res.tokens >= 0) & (res.tokens < w.V))
     top1 = np.argmax(res.logits, axis=1)
     assert np.array_equal(res.topk_idx[:, 0], top1)
+
+
+# ------------------------------------------------------------------ tensor-core path (9 rows and more)
+
+TC_SHAPES = [
+    # B, H, V, k, dtype: hi/lo sharing one 128-row tile up to 64 rows, separate tiles above
+    (9, 256, 8192, 64, "bf16"),
+    (64, 192, 12288, 256, "f16"),       # the last stacked size
+    (65, 192, 12288, 256, "bf16"),      # the first with hi and lo in separate tiles
+    (128, 128, 6144, 100, "f32"),       # one full m-block
+    (129, 128, 6144, 100, "bf16"),      # a second m-block with one row
+    (200, 160, 4144, 33, "bf16"),       # partial last tile and weight box; H not a multiple of 64
+    (72, 128, 24576, 64, "bf16"),       # more tiles than k: the merge bound comes from the tile maxima
+]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: f"B{s[0]}_H{s[1]}_V{s[2]}_k{s[3]}_{s[4]}")
+def test_tensor_core_batches_match_oracle(shape):
+    B, H, V, k, dt = shape
+    w = gen.custom(B, H, V, k, hidden_dtype=dt, seed=3000 + B)
+    with make_tail(w) as t:
+        assert t.info.tc_min_rows and B >= t.info.tc_min_rows
+        res = tc.run_gpu(t, w, torch)
+    rows = np.arange(B) if B <= 64 else np.unique(np.concatenate([np.arange(0, B, 7), [B - 1]]))
+    exact, exempt = full_check(w, res, rows=rows)
+    assert exact + exempt == len(rows) and exact >= len(rows) - max(1, len(rows) // 8)
+
+
+@pytest.mark.parametrize("V", [6144, 24576], ids=["bound_all_entries", "bound_tile_maxima"])
+def test_tensor_core_saturated_tiles_scan_the_logits(V):
+    # columns repeated in groups of 16: every tile holding a top value holds at least 16 elements at or
+    # above the merge bound, more than its 8-entry candidate list, so the merge must rescan those tiles
+    w = gen.custom(24, 128, V, 64, hidden_dtype="bf16", seed=91, dup_cols=16)
+    with make_tail(w) as t:
+        res = tc.run_gpu(t, w, torch)
+    groups = res.logits.view(np.uint32).reshape(w.B, -1, 16)
+    assert np.all(groups == groups[:, :, :1])
+    exact, exempt = full_check(w, res)
+    assert exact + exempt == w.B
+
+
+def test_tensor_core_emit_off_matches_emit_on():
+    w = gen.custom(40, 128, 8192, 128, hidden_dtype="bf16", seed=92)
+    with make_tail(w) as t:
+        on = tc.run_gpu(t, w, torch, emit=True)
+        off = tc.run_gpu(t, w, torch, emit=False)
+        again = tc.run_gpu(t, w, torch, emit=True)
+    assert np.array_equal(on.topk_idx, off.topk_idx) and np.array_equal(on.tokens, off.tokens)
+    assert np.array_equal(on.logits.view(np.uint32), again.logits.view(np.uint32))
+    full_check(w, on)
