@@ -7,11 +7,13 @@
 // hi + lo the two-bf16 split of the RMSNorm output, on tcgen05 tensor cores
 // with fp32 accumulation in tensor memory.
 //
-// Persistent kernel, one CTA per SM, 6 warps:
-//   warp 0     TMA producer: per ring stage one 64-wide k slice of the
+// Persistent kernel, one CTA per SM, 7 warps:
+//   warp 0     weight producer: per ring stage the 64 x TC_N weight slice
+//              (TC_N / 64 TMA boxes of 64 x 64, 128-byte swizzle), requested
+//              up to NW stages ahead.
+//   warp 6     activation producer: the matching 64-wide k slice of the
 //              activation tile (hi and lo: two 128 x 64 boxes, or one box
-//              holding both when the batch fits in 64 rows) and of the weight
-//              tile (TC_N / 64 boxes of 64 x 64), 128-byte swizzle.
+//              holding both when the batch fits in 64 rows), NA stages ahead.
 //   warp 1     tensor-memory owner and MMA issuer: M = 128, N = TC_N, K = 16
 //              per instruction, A K-major, B (the weight, V contiguous)
 //              MN-major; two accumulators of 256 columns so the epilogue of
@@ -37,7 +39,7 @@ namespace tail {
 
 namespace {
 
-constexpr int TC_THREADS = 192;
+constexpr int TC_THREADS = 224;  // warp 0 weight producer, 1 MMA, 2-5 epilogue, 6 activation producer
 constexpr uint32_t TC_ACC_COLS = 256;               // tensor-memory columns per accumulator
 constexpr uint32_t TC_TMEM_COLS = 2 * TC_ACC_COLS;  // two accumulators
 constexpr uint32_t W_BOX_BYTES = 64 * 64 * 2;
@@ -47,17 +49,24 @@ constexpr int TC_CHUNKS = TC_N / 32;
 constexpr int TC_WBOX = TC_N / 64;                  // 64-column weight boxes per stage
 static_assert(TC_N % 64 == 0 && TC_N <= 256, "tile width: whole 64-column boxes, one accumulator");
 
+// Shared memory: the activation ring (NA stages), the weight ring (NW stages), the
+// stacked hi/lo exchange, the logits store boxes and the barriers.  The two
+// rings are separate so that the weight, streamed from HBM, can be requested
+// further ahead than the L2-resident activations.
 template <bool STACKED>
 struct TcGeom {
-  static constexpr uint32_t A_BYTES = STACKED ? A_BOX_BYTES : 2 * A_BOX_BYTES;
-  static constexpr uint32_t STAGE = A_BYTES + TC_WBOX * W_BOX_BYTES;
-  static constexpr uint32_t TBUF_BYTES = 4 * 2 * 4096;  // per epilogue warp: two 32 x 32 fp32 store boxes
-  static constexpr int NST_FIT =
-      (227 * 1024 - 1024 - (STACKED ? (64 * XBUF_PITCH * 4 + 1023) / 1024 * 1024 : 0) - TBUF_BYTES - 256) / STAGE;
-  static constexpr int NST = NST_FIT < 5 ? NST_FIT : 5;
+  static constexpr uint32_t A_BYTES = STACKED ? A_BOX_BYTES : 2 * A_BOX_BYTES;  // one activation stage
+  static constexpr uint32_t W_BYTES = TC_WBOX * W_BOX_BYTES;                     // one weight stage
+  static constexpr int TBUF_N = STACKED ? 1 : 2;  // 32 x 32 fp32 store boxes per epilogue warp
+  static constexpr uint32_t TBUF_BYTES = 4 * TBUF_N * 4096;
   static constexpr uint32_t XBUF_BYTES = STACKED ? (64 * XBUF_PITCH * 4 + 1023) / 1024 * 1024 : 0;
   static constexpr uint32_t CTL_BYTES = 256;
-  static constexpr uint32_t SMEM = 1024 /* alignment slack */ + NST * STAGE + XBUF_BYTES + TBUF_BYTES + CTL_BYTES;
+  static constexpr int NA = 3;
+  static constexpr int NW_FIT =
+      static_cast<int>((227 * 1024 - 1024 - XBUF_BYTES - TBUF_BYTES - CTL_BYTES - NA * A_BYTES) / W_BYTES);
+  static constexpr int NW = NW_FIT < 8 ? NW_FIT : 8;
+  static constexpr uint32_t SMEM = 1024 /* alignment slack */ + NA * A_BYTES + NW * W_BYTES + XBUF_BYTES +
+                                   TBUF_BYTES + CTL_BYTES;
 };
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
@@ -104,27 +113,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
                      const __grid_constant__ CUtensorMap mapL, const TcArgs a) {
   using G = TcGeom<STACKED>;
-  constexpr int NST = G::NST;
+  constexpr int NA = G::NA, NW = G::NW;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (base_u - raw_u);
-  const uint32_t ring_u = base_u;
-  float* xbuf = reinterpret_cast<float*>(sm + NST * G::STAGE);
-  float* tbuf = reinterpret_cast<float*>(sm + NST * G::STAGE + G::XBUF_BYTES);
-  uint8_t* ctl = sm + NST * G::STAGE + G::XBUF_BYTES + G::TBUF_BYTES;
-  const uint32_t ctl_u = base_u + NST * G::STAGE + G::XBUF_BYTES + G::TBUF_BYTES;
-  auto full_bar = [&](int s) { return ctl_u + 8u * s; };
-  auto empty_bar = [&](int s) { return ctl_u + 8u * (NST + s); };
-  auto tfull_bar = [&](int acc) { return ctl_u + 8u * (2 * NST + acc); };
-  auto tempty_bar = [&](int acc) { return ctl_u + 8u * (2 * NST + 2 + acc); };
-  const uint32_t done_bar = ctl_u + 8u * (2 * NST + 4);
-  int* cw = reinterpret_cast<int*>(ctl + 8 * (2 * NST + 5));
+  const uint32_t ringA_u = base_u;
+  const uint32_t ringW_u = base_u + NA * G::A_BYTES;
+  const uint32_t rings = NA * G::A_BYTES + NW * G::W_BYTES;
+  float* xbuf = reinterpret_cast<float*>(sm + rings);
+  float* tbuf = reinterpret_cast<float*>(sm + rings + G::XBUF_BYTES);
+  uint8_t* ctl = sm + rings + G::XBUF_BYTES + G::TBUF_BYTES;
+  const uint32_t ctl_u = base_u + rings + G::XBUF_BYTES + G::TBUF_BYTES;
+  auto fullA_bar = [&](int s) { return ctl_u + 8u * s; };
+  auto emptyA_bar = [&](int s) { return ctl_u + 8u * (NA + s); };
+  auto fullW_bar = [&](int s) { return ctl_u + 8u * (2 * NA + s); };
+  auto emptyW_bar = [&](int s) { return ctl_u + 8u * (2 * NA + NW + s); };
+  auto tfull_bar = [&](int acc) { return ctl_u + 8u * (2 * NA + 2 * NW + acc); };
+  auto tempty_bar = [&](int acc) { return ctl_u + 8u * (2 * NA + 2 * NW + 2 + acc); };
+  const uint32_t done_bar = ctl_u + 8u * (2 * NA + 2 * NW + 4);
+  int* cw = reinterpret_cast<int*>(ctl + 8 * (2 * NA + 2 * NW + 5));
   volatile int* s_abort = cw;
   volatile int* s_go = cw + 1;  // [2]: epilogue go flags, by tile parity
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(cw + 3);
-  int* s_issued = cw + 4;
-  int* s_consumed = cw + 5;
+  int* s_issued_w = cw + 4;
+  int* s_issued_a = cw + 5;
+  int* s_consumed = cw + 6;
+  static_assert(8 * (2 * G::NA + 2 * G::NW + 5) + 7 * 4 <= G::CTL_BYTES, "barrier region");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntiles = a.ntn * a.n_mb;
@@ -132,9 +147,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int total_it = my_tiles * a.kblocks;
 
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(fullA_bar(s), 1);
+      mbar_init(emptyA_bar(s), 1);
+    }
+    for (int s = 0; s < NW; ++s) {
+      mbar_init(fullW_bar(s), 1);
+      mbar_init(emptyW_bar(s), 1);
     }
     for (int acc = 0; acc < 2; ++acc) {
       mbar_init(tfull_bar(acc), 1);
@@ -144,7 +163,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     *s_abort = 0;
     s_go[0] = 0;
     s_go[1] = 0;
-    *s_issued = 0;
+    *s_issued_w = 0;
+    *s_issued_a = 0;
     *s_consumed = 0;
     fence_mbar_init();
   }
@@ -164,56 +184,68 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   };
 
   if (warp == 0) {
-    // ================================================================ TMA producer
+    // ================================================================ weight producer
     if (lane == 0) {
-      tma_prefetch_map(&mapA);
       tma_prefetch_map(&mapW);
       const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_a = policy_evict_last();
       auto issue_w = [&](int it) {
         int n, m;
         tile_coords(it / a.kblocks, n, m);
         const int kb = it % a.kblocks;
-        const int s = it % NST;
-        const uint32_t st = ring_u + static_cast<uint32_t>(s) * G::STAGE;
+        const int s = it % NW;
+        const uint32_t st = ringW_u + static_cast<uint32_t>(s) * G::W_BYTES;
         const int x0 = n * TC_N;
         int nbox = 0;
 #pragma unroll
-        for (int j = 0; j < TC_WBOX; ++j) nbox += (x0 + 64 * j < a.V) ? 1 : 0;
-        mbar_arrive_expect_tx(full_bar(s), G::A_BYTES + static_cast<uint32_t>(nbox) * W_BOX_BYTES);
+        for (int j = 0; j < TC_WBOX; ++j) nbox += (x0 + 64 * j < a.V) ? 1 : 0;  // >= 1: x0 < V
+        mbar_arrive_expect_tx(fullW_bar(s), static_cast<uint32_t>(nbox) * W_BOX_BYTES);
         for (int j = 0; j < nbox; ++j)
-          tma_load_2d(st + G::A_BYTES + j * W_BOX_BYTES, &mapW, x0 + 64 * j, kb * TC_KB, full_bar(s), pol_w);
+          tma_load_2d(st + j * W_BOX_BYTES, &mapW, x0 + 64 * j, kb * TC_KB, fullW_bar(s), pol_w);
       };
-      auto issue_a = [&](int it) {
-        int n, m;
-        tile_coords(it / a.kblocks, n, m);
-        const int kb = it % a.kblocks;
-        const int s = it % NST;
-        const uint32_t st = ring_u + static_cast<uint32_t>(s) * G::STAGE;
-        if (STACKED) {
-          tma_load_2d(st, &mapA, kb * TC_KB, 0, full_bar(s), pol_a);
-        } else {
-          tma_load_2d(st, &mapA, kb * TC_KB, m * 2 * TC_M, full_bar(s), pol_a);
-          tma_load_2d(st + A_BOX_BYTES, &mapA, kb * TC_KB, m * 2 * TC_M + TC_M, full_bar(s), pol_a);
-        }
-      };
-      const int npre = min(NST, total_it);
+      // the weight does not depend on the split kernel: the first stages go out before its wait
+      const int npre = min(NW, total_it);
       for (int it = 0; it < npre; ++it) issue_w(it);
-      pdl_wait();  // the activations come from the split kernel
-      for (int it = 0; it < npre; ++it) issue_a(it);
       int issued = npre;
       for (int it = npre; it < total_it; ++it) {
         if (*s_abort) break;
-        const uint32_t par = static_cast<uint32_t>((it / NST) - 1) & 1u;
-        if (!wait_or_abort(empty_bar(it % NST), par, a.timeout_ns, s_abort)) {
+        if (!wait_or_abort(emptyW_bar(it % NW), static_cast<uint32_t>((it / NW) - 1) & 1u, a.timeout_ns, s_abort)) {
           fail(a.err, DEV_TIMEOUT_EMPTY, s_abort);
           break;
         }
         issue_w(it);
-        issue_a(it);
         issued = it + 1;
       }
-      *s_issued = issued;
+      *s_issued_w = issued;
+    }
+  } else if (warp == 6) {
+    // ================================================================ activation producer
+    if (lane == 0) {
+      tma_prefetch_map(&mapA);
+      const uint64_t pol_a = policy_evict_last();
+      pdl_wait();  // the activations come from the split kernel
+      int issued = 0;
+      for (int it = 0; it < total_it; ++it) {
+        if (*s_abort) break;
+        const int s = it % NA;
+        if (it >= NA &&
+            !wait_or_abort(emptyA_bar(s), static_cast<uint32_t>((it / NA) - 1) & 1u, a.timeout_ns, s_abort)) {
+          fail(a.err, DEV_TIMEOUT_EMPTY, s_abort);
+          break;
+        }
+        int n, m;
+        tile_coords(it / a.kblocks, n, m);
+        const int kb = it % a.kblocks;
+        const uint32_t st = ringA_u + static_cast<uint32_t>(s) * G::A_BYTES;
+        mbar_arrive_expect_tx(fullA_bar(s), G::A_BYTES);
+        if (STACKED) {
+          tma_load_2d(st, &mapA, kb * TC_KB, 0, fullA_bar(s), pol_a);
+        } else {
+          tma_load_2d(st, &mapA, kb * TC_KB, m * 2 * TC_M, fullA_bar(s), pol_a);
+          tma_load_2d(st + A_BOX_BYTES, &mapA, kb * TC_KB, m * 2 * TC_M + TC_M, fullA_bar(s), pol_a);
+        }
+        issued = it + 1;
+      }
+      *s_issued_a = issued;
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
@@ -230,25 +262,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * TC_ACC_COLS;
         for (int kb = 0; kb < a.kblocks; ++kb, ++it) {
-          const int s = it % NST;
-          if (!wait_or_abort(full_bar(s), static_cast<uint32_t>(it / NST) & 1u, a.timeout_ns, s_abort)) {
+          const int sa = it % NA, sw = it % NW;
+          if (!wait_or_abort(fullA_bar(sa), static_cast<uint32_t>(it / NA) & 1u, a.timeout_ns, s_abort) ||
+              !wait_or_abort(fullW_bar(sw), static_cast<uint32_t>(it / NW) & 1u, a.timeout_ns, s_abort)) {
             fail(a.err, DEV_TIMEOUT_FULL, s_abort);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = ring_u + static_cast<uint32_t>(s) * G::STAGE;
+          const uint32_t sta = ringA_u + static_cast<uint32_t>(sa) * G::A_BYTES;
+          const uint32_t stw = ringW_u + static_cast<uint32_t>(sw) * G::W_BYTES;
 #pragma unroll
           for (int ks = 0; ks < TC_KB / 16; ++ks) {
-            const uint64_t bd = sdesc_sw128(st + G::A_BYTES + ks * 2048u, W_BOX_BYTES, 1024u);
-            const uint64_t ah = sdesc_sw128(st + ks * 32u, 16u, 1024u);
+            const uint64_t bd = sdesc_sw128(stw + ks * 2048u, W_BOX_BYTES, 1024u);
+            const uint64_t ah = sdesc_sw128(sta + ks * 32u, 16u, 1024u);
             tc_mma(d, ah, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
             if (!STACKED) {
-              const uint64_t al = sdesc_sw128(st + A_BOX_BYTES + ks * 32u, 16u, 1024u);
+              const uint64_t al = sdesc_sw128(sta + A_BOX_BYTES + ks * 32u, 16u, 1024u);
               tc_mma(d, al, bd, idesc, 1u);
             }
           }
-          tc_commit(empty_bar(s));  // the stage is free once these MMAs have read it
+          tc_commit(emptyA_bar(sa));  // the stages are free once these MMAs have read them
+          tc_commit(emptyW_bar(sw));
         }
         if (ok) tc_commit(tfull_bar(acc));
       }
@@ -316,8 +351,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int j = 0; j < 32; ++j) v[j] *= rs;
           // the logits: this warp's 32 rows x 32 columns as one 128-byte-swizzled box, stored by TMA
           // (rows past B and columns past V are clipped by the tensor map)
-          const uint32_t box = tbuf_u + static_cast<uint32_t>(wq * 2 + (store_n & 1)) * 4096u;
-          if (lane == 0) tma_store_wait_read<1>();  // the box written two chunks ago has been read
+          const uint32_t box = tbuf_u + static_cast<uint32_t>(wq * G::TBUF_N + store_n % G::TBUF_N) * 4096u;
+          if (lane == 0) {  // the box this store reuses has been read by its previous store
+            if (G::TBUF_N == 2) tma_store_wait_read<1>(); else tma_store_wait_read<0>();
+          }
           __syncwarp();
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -359,10 +396,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   // ================================================================ wind down
   __syncthreads();
-  if (warp == 0 && lane == 0) {
+  if ((warp == 0 || warp == 6) && lane == 0) {
     // copies issued for stages the MMA warp never consumed must land before the CTA leaves
-    for (int it = *s_consumed; it < *s_issued; ++it) {
-      if (!mbar_wait_bounded(full_bar(it % NST), static_cast<uint32_t>(it / NST) & 1u, DEFAULT_TIMEOUT_NS)) {
+    const bool w = warp == 0;
+    const int nst = w ? NW : NA;
+    const int issued = w ? *s_issued_w : *s_issued_a;
+    for (int it = *s_consumed; it < issued; ++it) {
+      const uint32_t bar = w ? fullW_bar(it % nst) : fullA_bar(it % nst);
+      if (!mbar_wait_bounded(bar, static_cast<uint32_t>(it / nst) & 1u, DEFAULT_TIMEOUT_NS)) {
         raise_error(a.err, DEV_TIMEOUT_DRAIN);
         break;
       }
