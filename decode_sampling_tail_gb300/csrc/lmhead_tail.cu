@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
           const int pos = i * 32 + lane;
           pk[i] = pos < npub ? __ldcg(srcp + pos) : 0u;
         }
-        x = warp_bound16_regs(pk, a.K);
+        x = warp_bound16_span_regs(pk, a.K);
       }
       uint32_t k[SEL_NPL];
       load_row_keys(r, k);
@@ -502,11 +502,13 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
         const uint64_t ci = comp[i];
         int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
         int j = 0;
+        const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(comp);  // comp is 16-byte aligned
         for (; j + 4 <= nr; j += 4) {
-          r0 += comp[j] > ci;
-          r1 += comp[j + 1] > ci;
-          r2 += comp[j + 2] > ci;
-          r3 += comp[j + 3] > ci;
+          const ulonglong2 p = c2[j >> 1], q = c2[(j >> 1) + 1];
+          r0 += p.x > ci;
+          r1 += p.y > ci;
+          r2 += q.x > ci;
+          r3 += q.y > ci;
         }
         for (; j < nr; ++j) r0 += comp[j] > ci;
         const int rank = (r0 + r1) + (r2 + r3);

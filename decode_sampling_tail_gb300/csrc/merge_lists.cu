@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
           const int j = i * 32 + lane;
           hk[i] = j < ntn ? lk[j * TC_LIST] : 0u;
         }
-        const uint32_t b = warp_bound16_regs(hk, K);
+        const uint32_t b = warp_bound16_span_regs(hk, K);
         if (lane == 0) s_x = b;
       }
       __syncthreads();
