@@ -406,6 +406,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
     int* s_cnt = reinterpret_cast<int*>(ebuf + a.K);
     int* s_off = s_cnt + a.nslab;
     for (int row = c; row < a.B; row += a.nslab) {
+      SampleParams prm = {};
+      if (a.params != nullptr) prm = load_sample_params(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols);
       for (int s = tid; s < a.nslab; s += nt) s_cnt[s] = __ldcg(a.cand_cnt + static_cast<int64_t>(row) * a.nslab + s);
       __syncthreads();
       if (warp == 0) {  // exclusive scan of the per-slab counts
@@ -519,9 +521,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
         a.topk_val[static_cast<int64_t>(row) * a.topk_ld + j] = key_float(composite_key(sorted[j]));
         a.topk_idx[static_cast<int64_t>(row) * a.topk_ld + j] = composite_idx(sorted[j]);
       }
-      if (a.params != nullptr && a.tokens != nullptr && warp == 0) {
-        const int32_t tok = sample_sorted_row(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols, sorted, want, ebuf);
-        if (lane == 0) a.tokens[row] = tok;
+      if (a.params != nullptr && a.tokens != nullptr) {  // every thread takes part in the draw
+        const int32_t tok = sample_sorted_row(prm, sorted, want, ebuf,
+                                              reinterpret_cast<float*>(s_red));
+        if (tid == 0) a.tokens[row] = tok;
       }
       __syncthreads();
     }

@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
   };
 
   for (int row = blockIdx.x; row < a.B; row += gridDim.x) {
+    SampleParams prm = {};
+    if (a.params != nullptr) prm = load_sample_params(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols);
     const uint64_t* L = a.lists + static_cast<int64_t>(row) * ntn * TC_LIST;
     const float* lg = a.logits + static_cast<int64_t>(row) * a.ld;
 
@@ -237,9 +239,10 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
       a.topk_val[static_cast<int64_t>(row) * a.topk_ld + j] = key_float(composite_key(sorted[j]));
       a.topk_idx[static_cast<int64_t>(row) * a.topk_ld + j] = composite_idx(sorted[j]);
     }
-    if (a.params != nullptr && a.tokens != nullptr && warp == 0) {
-      const int32_t tok = sample_sorted_row(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols, sorted, want, ebuf);
-      if (lane == 0) a.tokens[row] = tok;
+    if (a.params != nullptr && a.tokens != nullptr) {  // every thread takes part in the draw
+      const int32_t tok = sample_sorted_row(prm, sorted, want, ebuf,
+                                            reinterpret_cast<float*>(s_red));
+      if (tid == 0) a.tokens[row] = tok;
     }
     __syncthreads();
   }
