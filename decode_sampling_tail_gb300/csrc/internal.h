@@ -47,9 +47,9 @@ struct GemvArgs {
   int64_t logits_out_ld;    // row stride of logits_out in floats
   float* logits_scratch;    // [B, V] staging when the slab logits do not fit in shared memory
   uint32_t* pub;            // [B][nslab][TAIL_PUB_PER_SLAB] published lane maxima
-  uint32_t* cand_key;       // [B][nslab][K] order keys of the emitted candidates
-  int32_t* cand_idx;        // [B][nslab][K] their vocabulary ids
-  int32_t* cand_cnt;        // [B][nslab] candidates emitted per (row, slab)
+  uint32_t* cand_key;       // [B][nslab * K] order keys of each row's emitted candidates, packed
+  int32_t* cand_idx;        // [B][nslab * K] their vocabulary ids
+  unsigned long long* row_sync;  // [B]: (slabs emitted << 32) | candidates reserved; 0 between runs
   unsigned long long* bar;  // grid barrier arrival counter (grows monotonically)
   float* topk_val;          // [B][topk_ld] sorted top-k logits
   int32_t* topk_idx;        // [B][topk_ld] their vocabulary ids

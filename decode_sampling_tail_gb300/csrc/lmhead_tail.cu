@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
   __shared__ uint32_t s_red[64];
   __shared__ uint32_t s_list[SEL_BLOCK_BUCKET_MAX];
   __shared__ uint32_t s_misc[4];
+  __shared__ int s_rows[1];
   __shared__ int s_flag;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   const uint32_t full0 = smem_u32(bars);
@@ -362,7 +363,12 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
 #pragma unroll
       for (int i = 0; i < SEL_NPL; ++i) mine += (i * 32 + lane < n && k[i] >= x) ? 1u : 0u;
       const uint32_t tot = __reduce_add_sync(0xffffffffu, mine);
-      const int64_t obase = (static_cast<int64_t>(r) * a.nslab + c) * a.K;
+      // reserve room in the row's packed candidate array, emit, then count this slab as arrived
+      const uint32_t take = tot <= static_cast<uint32_t>(a.K) ? tot : static_cast<uint32_t>(a.K);
+      uint32_t off = 0;
+      if (lane == 0) off = static_cast<uint32_t>(atomicAdd(a.row_sync + r, static_cast<unsigned long long>(take)));
+      off = __shfl_sync(0xffffffffu, off, 0);
+      const int64_t obase = static_cast<int64_t>(r) * a.nslab * a.K + off;
       if (tot <= static_cast<uint32_t>(a.K)) {
         uint32_t incl = mine;
 #pragma unroll
@@ -380,7 +386,6 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
             ++o;
           }
         }
-        if (lane == 0) a.cand_cnt[static_cast<int64_t>(r) * a.nslab + c] = static_cast<int32_t>(tot);
       } else {
         // more than K pass: the slab's exact top-K (ties by index) covers its share of the global top-K
         const Threshold th = warp_select_regs(k, a.K, wlist);
@@ -388,106 +393,83 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
           a.cand_key[obase + pos] = kv;
           a.cand_idx[obase + pos] = static_cast<int32_t>(vbase + i);
         });
-        if (lane == 0) a.cand_cnt[static_cast<int64_t>(r) * a.nslab + c] = a.K;
       }
+      __threadfence();
       __syncwarp();
+      if (lane == 0) atomicAdd(a.row_sync + r, 1ull << 32);
     }
   }
-  const bool ok2 = grid_barrier(a.bar, a.timeout_ns, a.err, &s_flag);
 
   // ================================================================ phase C: final top-K, sort, sampler
-  if (!aborted && ok1 && ok2) {
+  if (!aborted && ok1) {
     const int nt = blockDim.x, nw = nt >> 5;
     uint32_t* keys = reinterpret_cast<uint32_t*>(ring);
     int32_t* idx = reinterpret_cast<int32_t*>(keys + a.capc);
     uint64_t* comp = reinterpret_cast<uint64_t*>(idx + a.capc);
     uint64_t* sorted = comp + a.sortP;
     float* ebuf = reinterpret_cast<float*>(sorted + a.K);
-    int* s_cnt = reinterpret_cast<int*>(ebuf + a.K);
-    int* s_off = s_cnt + a.nslab;
+    // keeps the top K of the m > K candidates, in place
+    auto fold = [&](int m) {
+      for (int j = tid; j < a.sortP; j += nt) comp[j] = 0ull;
+      __syncthreads();
+      block_top_composites(keys, idx, m, a.K, comp, s_red, s_list, s_misc);
+      for (int j = tid; j < a.K; j += nt) {
+        keys[j] = composite_key(comp[j]);
+        idx[j] = composite_idx(comp[j]);
+      }
+      __syncthreads();
+      return a.K;
+    };
     for (int row = c; row < a.B; row += a.nslab) {
       SampleParams prm = {};
       if (a.params != nullptr) prm = load_sample_params(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols);
-      for (int s = tid; s < a.nslab; s += nt) s_cnt[s] = __ldcg(a.cand_cnt + static_cast<int64_t>(row) * a.nslab + s);
-      __syncthreads();
-      if (warp == 0) {  // exclusive scan of the per-slab counts
-        const int per = (a.nslab + 31) / 32;
-        const int s0 = min(a.nslab, lane * per), s1 = min(a.nslab, s0 + per);
-        int loc = 0;
-        for (int s = s0; s < s1; ++s) loc += s_cnt[s];
-        int incl = loc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
+      // wait (bounded) until every slab has emitted its candidates of this row
+      if (tid == 0) {
+        unsigned long long v = 0;
+        const uint64_t t0 = global_timer_ns();
+        while (true) {
+          asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.row_sync + row) : "memory");
+          if ((v >> 32) >= static_cast<unsigned long long>(a.nslab)) break;
+          if (global_timer_ns() - t0 > a.timeout_ns) {
+            raise_error(a.err, DEV_TIMEOUT_BARRIER);
+            v = ~0ull;
+            break;
+          }
         }
-        int run = incl - loc;
-        for (int s = s0; s < s1; ++s) {
-          s_off[s] = run;
-          run += s_cnt[s];
-        }
-        if (lane == 31) s_off[a.nslab] = incl;
+        s_rows[0] = v == ~0ull ? -1 : static_cast<int>(v & 0xFFFFFFFFull);
       }
       __syncthreads();
+      const int total_c = s_rows[0];
+      if (total_c < 0) break;  // uniform: a slab never arrived (the error flag is raised)
       const int64_t cbase = static_cast<int64_t>(row) * a.nslab * a.K;
-      const int total_c = s_off[a.nslab];
-      int ncand;
-      if (total_c <= a.capc) {
-        // every thread issues its loads first (no store in between), then stores them
-        for (int base = 0; base < total_c; base += GATHER_PT * nt) {
+      // gather the packed candidates; when they exceed the buffer, fold it to its top K between runs
+      int ncand = 0;
+      for (int base = 0; base < total_c;) {
+        const int take = min(total_c - base, a.capc - ncand);
+        for (int i0 = 0; i0 < take; i0 += GATHER_PT * nt) {  // loads first, then stores
           uint32_t kr[GATHER_PT];
           int32_t ir[GATHER_PT];
 #pragma unroll
           for (int q = 0; q < GATHER_PT; ++q) {
-            const int i = base + q * nt + tid;
-            kr[q] = 0u;
-            ir[q] = 0;
-            if (i < total_c) {
-              int lo = 0, hi = a.nslab;  // slab s with s_off[s] <= i < s_off[s + 1]
-              while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (s_off[mid] <= i) lo = mid; else hi = mid;
-              }
-              const int64_t src = cbase + static_cast<int64_t>(lo) * a.K + (i - s_off[lo]);
-              kr[q] = __ldcg(a.cand_key + src);
-              ir[q] = __ldcg(a.cand_idx + src);
-            }
+            const int i = i0 + q * nt + tid;
+            kr[q] = i < take ? __ldcg(a.cand_key + cbase + base + i) : 0u;
+            ir[q] = i < take ? __ldcg(a.cand_idx + cbase + base + i) : 0;
           }
 #pragma unroll
           for (int q = 0; q < GATHER_PT; ++q) {
-            const int i = base + q * nt + tid;
-            if (i < total_c) {
-              keys[i] = kr[q];
-              idx[i] = ir[q];
+            const int i = i0 + q * nt + tid;
+            if (i < take) {
+              keys[ncand + i] = kr[q];
+              idx[ncand + i] = ir[q];
             }
           }
         }
-        ncand = total_c;
+        ncand += take;
+        base += take;
         __syncthreads();
-      } else {
-        // more candidates than fit: gather slab by slab, folding the buffer to its top K when full
-        ncand = 0;
-        for (int s = 0; s < a.nslab; ++s) {
-          const int cs = s_cnt[s];
-          if (ncand + cs > a.capc) {
-            for (int j = tid; j < a.sortP; j += nt) comp[j] = 0ull;
-            __syncthreads();
-            block_top_composites(keys, idx, ncand, a.K, comp, s_red, s_list, s_misc);
-            for (int j = tid; j < a.K; j += nt) {
-              keys[j] = composite_key(comp[j]);
-              idx[j] = composite_idx(comp[j]);
-            }
-            ncand = a.K;
-            __syncthreads();
-          }
-          for (int j = tid; j < cs; j += nt) {
-            keys[ncand + j] = __ldcg(a.cand_key + cbase + static_cast<int64_t>(s) * a.K + j);
-            idx[ncand + j] = __ldcg(a.cand_idx + cbase + static_cast<int64_t>(s) * a.K + j);
-          }
-          ncand += cs;
-          __syncthreads();
-        }
+        if (base < total_c) ncand = fold(ncand);
       }
+      if (tid == 0) a.row_sync[row] = 0ull;  // ready for the next run
       const int want = min(a.K, ncand);
       // candidates to rank: all of them when few, else the top `want` found by a selection
       int nr = ncand;

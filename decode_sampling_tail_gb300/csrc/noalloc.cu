@@ -8,8 +8,8 @@
 // module, zero-filled, and its address is looked up once per device (with that
 // device current) by the first call that runs there.  That first call also
 // opts the lm_head kernels into their shared-memory size.  Every later call
-// only computes a layout on the host, clears the barrier counter and error
-// word with one cudaMemsetAsync and launches kernels: no cudaMalloc, cudaFree
+// only computes a layout on the host, clears the barrier counter, the error
+// word and the per-row arrival words with one cudaMemsetAsync and launches kernels: no cudaMalloc, cudaFree
 // or other allocating routine on any call.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -90,25 +90,26 @@ size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Byte offsets of one pass's scratch inside the static array.
 struct Layout {
-  size_t bar, err, apack, row_scale, pub, cnt, ckey, cidx, lscr, tkv, tki, total;
+  size_t bar, err, rsync, apack, row_scale, pub, ckey, cidx, lscr, tkv, tki, total;
 };
 
 // Scratch of a pass of B rows under `plan`; the first 256 bytes hold the
-// grid-barrier counter (offset 0) and the error word (offset 8).
+// grid-barrier counter (offset 0) and the error word (offset 8), the per-row
+// arrival words follow; everything before `apack` starts each call at zero.
 Layout layout_for(const GemvPlan& plan, int B, int H, int V, int K, int nslab) {
   Layout L = {};
   size_t o = 0;
   L.bar = 0;
   L.err = 8;
   o = 256;
+  L.rsync = o;
+  o += up256(static_cast<size_t>(B) * 8);
   L.apack = o;
   o += up256(static_cast<size_t>(H / KSTEP) * plan.mt * APACK_TILE_BYTES);
   L.row_scale = o;
   o += up256(static_cast<size_t>(plan.mt) * MTILE_ROWS * 4);
   L.pub = o;
   o += up256(static_cast<size_t>(B) * nslab * TAIL_PUB_PER_SLAB * 4);
-  L.cnt = o;
-  o += up256(static_cast<size_t>(B) * nslab * 4);
   L.ckey = o;
   o += up256(static_cast<size_t>(B) * nslab * K * 4);
   L.cidx = o;
@@ -193,10 +194,12 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* base = d->base;
-  // The grid barrier counter and the error word must start at zero: the
-  // counter's generations are multiples of the grid size, which differs
-  // between configs sharing this array.
-  e = cudaMemsetAsync(base, 0, 16, s);
+  // The grid barrier counter, the error word and the per-row arrival words must
+  // start at zero: the counter's generations are multiples of the grid size,
+  // which differs between configs sharing this array, and a call interrupted by
+  // a device error may leave the others nonzero.
+  const size_t zero_bytes = layout_for(plan_gemv(R, H, V, K, nslab, d->max_dyn), R, H, V, K, nslab).apack;
+  e = cudaMemsetAsync(base, 0, zero_bytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "tail_run_noalloc: cudaMemsetAsync");
 
   const int sz = elem_bytes(cfg->hidden_dtype);
@@ -232,7 +235,7 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
     ga.pub = reinterpret_cast<uint32_t*>(base + L.pub);
     ga.cand_key = reinterpret_cast<uint32_t*>(base + L.ckey);
     ga.cand_idx = reinterpret_cast<int32_t*>(base + L.cidx);
-    ga.cand_cnt = reinterpret_cast<int32_t*>(base + L.cnt);
+    ga.row_sync = reinterpret_cast<unsigned long long*>(base + L.rsync);
     ga.bar = reinterpret_cast<unsigned long long*>(base + L.bar);
     ga.topk_val = reinterpret_cast<float*>(base + L.tkv);
     ga.topk_idx = reinterpret_cast<int32_t*>(base + L.tki);

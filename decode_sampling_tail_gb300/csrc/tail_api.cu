@@ -37,7 +37,7 @@ struct tail_s {
   int32_t* cand_idx;
   float* logit_scratch;
   uint32_t* pub;
-  int32_t* cand_cnt;
+  unsigned long long* row_sync;
   unsigned long long* bar;
   float* topk_val;
   int32_t* topk_idx;
@@ -124,7 +124,7 @@ cudaError_t dalloc(T** p, size_t n, int64_t* total) {
 
 void free_all(tail_t* h) {
   void* ptrs[] = {h->apack,    h->row_scale, h->cand_key,  h->cand_idx,  h->logit_scratch, h->pub,
-                  h->cand_cnt, h->bar,       h->topk_val,  h->topk_idx,  h->err,           h->st_hidden,
+                  h->row_sync, h->bar,       h->topk_val,  h->topk_idx,  h->err,           h->st_hidden,
                   h->st_params, h->st_tokens, h->st_logits, h->tc_act,   h->tc_rs,         h->tc_lists,
                   h->tc_logits};
   for (void* p : ptrs)
@@ -263,7 +263,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   e = e ? e : dalloc(&h->cand_idx, static_cast<size_t>(R) * h->nslab * K, &tot);
   e = e ? e : dalloc(&h->logit_scratch, static_cast<size_t>(R) * cfg->V, &tot);
   e = e ? e : dalloc(&h->pub, static_cast<size_t>(R) * h->nslab * TAIL_PUB_PER_SLAB, &tot);
-  e = e ? e : dalloc(&h->cand_cnt, static_cast<size_t>(R) * h->nslab, &tot);
+  e = e ? e : dalloc(&h->row_sync, static_cast<size_t>(R), &tot);
   e = e ? e : dalloc(&h->bar, 1, &tot);
   e = e ? e : dalloc(&h->topk_val, static_cast<size_t>(cfg->gbs_max) * K, &tot);
   e = e ? e : dalloc(&h->topk_idx, static_cast<size_t>(cfg->gbs_max) * K, &tot);
@@ -284,6 +284,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   }
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->bar, 0, sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(h->row_sync, 0, static_cast<size_t>(R) * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(h->apack, 0, ksteps * mt_max * APACK_TILE_BYTES);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -446,7 +447,7 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     ga.max_slab_cols = plan.max_slab_cols;
     ga.smem_bytes = plan.smem_bytes;
     ga.pub = h->pub;
-    ga.cand_cnt = h->cand_cnt;
+    ga.row_sync = h->row_sync;
     ga.bar = h->bar;
     ga.topk_val = (out_topk_vals ? out_topk_vals : h->topk_val) + static_cast<int64_t>(r0) * K;
     ga.topk_idx = (out_topk_idx ? out_topk_idx : h->topk_idx) + static_cast<int64_t>(r0) * K;
@@ -572,6 +573,8 @@ int tail_check(tail_t* h) {
     // a wait that ran out may leave the grid barrier counter off its generation boundary
     cudaMemset(h->err, 0, sizeof(int));
     cudaMemset(h->bar, 0, sizeof(unsigned long long));
+    // so may the per-row arrival words of an interrupted run
+    cudaMemset(h->row_sync, 0, static_cast<size_t>(h->rows_pass) * sizeof(unsigned long long));
     cudaDeviceSynchronize();
     return TAIL_ERR_DEVICE;
   }

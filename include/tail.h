@@ -155,9 +155,10 @@ int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const 
  *                  bounded device wait that ran out, in which case the
  *                  outputs are undefined.
  * Size limit: one pass of B rows needs, each part rounded up to 256 bytes,
- * 256 (barrier counter and error word) + 32 * H * mt (activation pack; mt = 1,
+ * 256 (barrier counter and error word) + 8 * B (per-row arrival words)
+ * + 32 * H * mt (activation pack; mt = 1,
  * 2, 4 or 8 for B up to 8, 16, 32, 64) + 32 * mt (row scales)
- * + 20 * B * nslab (published maxima, counts) + 8 * B * nslab * k (per-slab
+ * + 16 * B * nslab (published maxima) + 8 * B * nslab * k (per-slab
  * candidates) + 8 * B * k (top-k staging) + 4 * B * V (logits staging, only
  * when a slab's logits do not fit in shared memory) bytes, nslab being the
  * vocabulary slab count (min(SMs, V / 128), at least 1).  Batches run in
@@ -165,9 +166,9 @@ int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const 
  * that is 8 rows per pass.  When not even one row fits, the call returns
  * TAIL_ERR_UNSUPPORTED before launching anything, and tail_last_error()
  * states the bytes needed and the 4 MiB limit.
- * Zeroing: every call clears the grid-barrier counter and the error word with
- * one cudaMemsetAsync on `stream`; the rest of the scratch is fully written
- * by the kernels before it is read.
+ * Zeroing: every call clears the grid-barrier counter, the error word and the
+ * per-row arrival words with one cudaMemsetAsync on `stream`; the rest of the
+ * scratch is fully written by the kernels before it is read.
  * First call on a device: sets up that device (looks up the static array's
  * address with cudaGetSymbolAddress, which loads the library's device image
  * if it is not loaded yet, and opts the lm_head kernels into their shared
