@@ -394,9 +394,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
           a.cand_idx[obase + pos] = static_cast<int32_t>(vbase + i);
         });
       }
-      __threadfence();
+      // the warp barrier orders every lane's candidate stores before lane 0's release of the arrival
       __syncwarp();
-      if (lane == 0) atomicAdd(a.row_sync + r, 1ull << 32);
+      if (lane == 0)
+        asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(a.row_sync + r), "l"(1ull << 32) : "memory");
     }
   }
 
