@@ -150,6 +150,21 @@ class ClockSampler:
 CPU_SAMPLE_ROWS = 64  # larger batches are timed on their first 64 rows (the metric is per row)
 
 
+def max_over_ranks(value_ms: float, dist, device) -> float:
+    """The job's time for N replicas: the slowest rank's (one all-reduce MAX; identity on one rank)."""
+    if dist is None:
+        return value_ms
+    import torch
+    t = torch.tensor([value_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_rank_step: int, steps: int, world: int, job_ms: float) -> float:
+    """Whole-job throughput: every rank's rows over the slowest rank's time."""
+    return rows_per_rank_step * steps * world / (job_ms / 1e3)
+
+
 def cpu_oracle_step(w, nthreads):
     """One oracle pass over the workload's first min(B, CPU_SAMPLE_ROWS) rows; returns the rows done."""
     import oracle
@@ -276,12 +291,9 @@ def main():
         dist.barrier()
     total_ms = ev0.elapsed_time(ev1)
     t.check()
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_step = total_ms / args.steps
-    rows_s = w.B * args.steps * world / (total_ms / 1e3)
+    rows_s = job_rows_per_s(w.B, args.steps, world, total_ms)
 
     # ---------------- spread of single steps (own loop, events around each step; not the headline)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * min(args.steps, 50))]
@@ -324,12 +336,9 @@ def main():
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
         e2e_ms = max(e0.elapsed_time(e1), wall * 1e3)
-        if dist:
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
         s_in = 4 if w.hidden_dtype == "f32" else 2
-        e2e = {"value": w.B * args.steps * world / (e2e_ms / 1e3), "unit": "rows/s",
+        e2e = {"value": job_rows_per_s(w.B, args.steps, world, e2e_ms), "unit": "rows/s",
                "h2d_bytes_per_step": w.B * w.H * s_in + w.B * 4 * 4, "d2h_bytes_per_step": w.B * 4,
                "us_per_step": 1e3 * e2e_ms / args.steps, "api": "tail_run_host"}
 
