@@ -210,9 +210,39 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
     // ---- 3. exact top K, sorted; tokens
     const int want = min(K, ncand);
     int nr = ncand;
-    if (ncand <= RANK_SORT_MAX) {
-      for (int j = tid; j < ncand; j += nt) comp[j] = composite(keys[j], idx[j]);
+    if (ncand > RANK_SORT_MAX && ncand <= 32 * MERGE_HEADS_PER_LANE) {
+      // many candidates (ties in groups): keep those at or above a 16-bit-exact lower bound of the
+      // K-th largest candidate key, found by one warp in registers; all K winners stay
+      if (warp == 0) {
+        uint32_t ck[MERGE_HEADS_PER_LANE];
+#pragma unroll
+        for (int i = 0; i < MERGE_HEADS_PER_LANE; ++i) {
+          const int j = i * 32 + lane;
+          ck[i] = j < ncand ? keys[j] : 0u;
+        }
+        const uint32_t b = warp_bound16_span_regs(ck, want);
+        if (lane == 0) {
+          s_x = b;
+          s_misc[3] = 0u;
+        }
+      }
       __syncthreads();
+      const uint32_t xc = s_x;
+      for (int j = tid; j < ncand; j += nt) {
+        if (keys[j] >= xc) {
+          const unsigned pos = atomicAdd(&s_misc[3], 1u);
+          if (pos < static_cast<unsigned>(RANK_SORT_MAX)) comp[pos] = composite(keys[j], idx[j]);
+        }
+      }
+      __syncthreads();
+      nr = static_cast<int>(s_misc[3]);
+      __syncthreads();
+    }
+    if (nr <= RANK_SORT_MAX) {
+      if (nr == ncand) {
+        for (int j = tid; j < ncand; j += nt) comp[j] = composite(keys[j], idx[j]);
+        __syncthreads();
+      }
     } else {
       for (int j = tid; j < a.sortP; j += nt) comp[j] = 0ull;
       __syncthreads();
@@ -258,7 +288,7 @@ bool plan_merge(int K, int ntn, int dyn_max, int* capc, int* sortP, int* smem_by
   // usual few hundred (ties in groups of a few) with room for K plus one saturated tile, small enough
   // for several rows' merges to share an SM
   int want = 4 * K + TC_N;
-  if (want < 2048) want = 2048;
+  if (want < 4096) want = 4096;  // room for ~20 rescanned tiles per pass
   want = (want + 3) & ~3;
   int cap = (dyn_max - fixed) / 8;
   cap &= ~3;
