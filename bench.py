@@ -40,6 +40,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gptoss_g8")
     ap.add_argument("--emit", action="store_true", help="also write the fp32 logits (emit_logits on)")
+    ap.add_argument("--legacy-rms", action="store_true",
+                    help="deferred_rms off: (x * rstd) * gamma feeds the GEMM instead of a per-row scale after it")
+    ap.add_argument("--params", default="4", choices=["4", "3", "none"],
+                    help="sampling_params columns: 4 (explicit u), 3 (u = 0.5), none (no sampler)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -251,7 +255,11 @@ def main():
     tokens = torch.empty(w.B, dtype=torch.int32, device=dev)
     logits = torch.empty((w.B, w.V), dtype=torch.float32, device=dev) if emit else None
     t = dst.Tail(w.H, w.V, w.k, w.B, hidden_actual=w.Hu, eps=w.eps, hidden_dtype=w.hidden_dtype,
-                 zero_interleaved_pad=bool(w.zero_pad), device=local_rank)
+                 zero_interleaved_pad=bool(w.zero_pad), deferred_rms=not args.legacy_rms, device=local_rank)
+    if args.params == "3":
+        params = params[:, :3].contiguous()
+    elif args.params == "none":
+        params = None
     stream = torch.cuda.Stream(dev)
     tc_path = t.info.tc_min_rows > 0 and w.B >= t.info.tc_min_rows
     if tc_path:  # split -> tensor-core lm_head -> merge + sampler, one pass
@@ -317,10 +325,11 @@ def main():
 
     # ---------------- end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and params is not None:  # without the sampler a step returns no tokens to read back
         hid_h = torch.from_numpy(np.ascontiguousarray(w.hidden.view(np.int16) if w.hidden_dtype != "f32"
                                                       else w.hidden)).pin_memory()
-        par_h = torch.from_numpy(np.ascontiguousarray(w.params)).pin_memory()
+        ncols = int(params.shape[1])
+        par_h = torch.from_numpy(np.ascontiguousarray(w.params[:, :ncols])).pin_memory()
         tok_h = torch.empty(w.B, dtype=torch.int32).pin_memory()
         for _ in range(3):
             t.run_host(hid_h, gamma, w_t, par_h, tok_h, stream=stream)
@@ -339,7 +348,7 @@ def main():
         e2e_ms = max_over_ranks(e2e_ms, dist, dev)
         s_in = 4 if w.hidden_dtype == "f32" else 2
         e2e = {"value": job_rows_per_s(w.B, args.steps, world, e2e_ms), "unit": "rows/s",
-               "h2d_bytes_per_step": w.B * w.H * s_in + w.B * 4 * 4, "d2h_bytes_per_step": w.B * 4,
+               "h2d_bytes_per_step": w.B * w.H * s_in + w.B * ncols * 4, "d2h_bytes_per_step": w.B * 4,
                "us_per_step": 1e3 * e2e_ms / args.steps, "api": "tail_run_host"}
 
     if rank != 0:
@@ -382,6 +391,7 @@ def main():
         "data": "synthetic (seeded generators, distributions of the named workload)",
         "config": {"workload": w.name, "gbs": w.B, "H": w.H, "hidden_actual": w.Hu, "V": w.V, "k": w.k,
                    "hidden_dtype": w.hidden_dtype, "emit_logits": emit,
+                   "deferred_rms": not args.legacy_rms, "sampling_params_cols": args.params,
                    "arithmetic": "bf16 W x bf16 hi+lo activations, fp32 accumulate",
                    "l2": "no flush: the 1.16 GB weight is larger than L2 and streams from HBM every step",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
