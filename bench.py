@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--emit", action="store_true", help="also write the fp32 logits (emit_logits on)")
     ap.add_argument("--legacy-rms", action="store_true",
                     help="deferred_rms off: (x * rstd) * gamma feeds the GEMM instead of a per-row scale after it")
+    ap.add_argument("--vocab-shards", type=int, default=0,
+                    help="vocabulary-parallel variant: time one rank's step (its 1/S slice + the merge of all "
+                         "S slices' candidates; the all-gather between GPUs is not part of one GPU's timing)")
     ap.add_argument("--params", default="4", choices=["4", "3", "none"],
                     help="sampling_params columns: 4 (explicit u), 3 (u = 0.5), none (no sampler)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -223,6 +226,69 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def run_vocab_shards(args, w, dev, dst, torch):
+    """One rank's step of the vocabulary-parallel tail on this GPU: the tail on slice 0 (no sampler),
+    then the merge of all slices' top-k lists (the other slices' lists computed once beforehand)."""
+    from decode_sampling_tail_gb300.vocab_parallel import ShardedTail
+    from gen.torch_io import to_device
+    S = args.vocab_shards
+    hidden, gamma, w_t, params = to_device(w, torch, str(dev))
+    kw = dict(hidden_actual=w.Hu, eps=w.eps, hidden_dtype=w.hidden_dtype, zero_interleaved_pad=bool(w.zero_pad))
+    vals = torch.empty((S, w.B, w.k), dtype=torch.float32, device=dev)
+    idx = torch.empty((S, w.B, w.k), dtype=torch.int32, device=dev)
+    tokens = torch.empty(w.B, dtype=torch.int32, device=dev)
+    ranks = [ShardedTail(w.H, w.V, w.k, w.B, r, S, **kw) for r in range(S)]
+    slices = [w_t[:, rk.lo:rk.hi].contiguous() for rk in ranks]
+    for r, rk in enumerate(ranks):  # every slice's candidates, as the all-gather would deliver them
+        rk.local_topk(hidden, gamma, slices[r], vals[r], idx[r])
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.Stream(dev)
+    r0 = ranks[0]
+
+    def step():
+        r0.local_topk(hidden, gamma, slices[0], vals[0], idx[0], stream=stream)
+        r0.merge(vals, idx, params, tokens, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize(dev)
+    # device time of each kernel (events between them; host launch costs are not device time)
+    dst.tail_profile_enable(r0.tail.h, True)
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            r0.local_topk(hidden, gamma, slices[0], vals[0], idx[0], stream=stream)
+            e[2 * i].record(stream)
+            r0.merge(vals, idx, params, tokens, stream=stream)
+            e[2 * i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    kms, npass = dst.tail_profile_read(r0.tail.h)
+    dst.tail_profile_enable(r0.tail.h, False)
+    for rk in ranks:
+        rk.tail.check()
+    tail_ms = sum(kms.values()) / max(1, npass)
+    merge_ms = sum(e[2 * i].elapsed_time(e[2 * i + 1]) for i in range(args.steps)) / args.steps
+    ms = tail_ms + merge_ms
+    line = {
+        "metric": METRIC, "value": w.B / (ms / 1e3), "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generators, distributions of the named workload)",
+        "config": {"workload": w.name, "gbs": w.B, "H": w.H, "V": w.V, "k": w.k, "vocab_shards": S,
+                   "slice_columns": r0.hi - r0.lo,
+                   "measures": "one rank's step: its slice's tail + the merge; the all-gather of "
+                               f"{w.B * w.k * 8} bytes per rank between GPUs is not included"},
+        "slice_tail_kernel_us": {k: 1e3 * v / max(1, npass) for k, v in kms.items()},
+        "merge_us": merge_ms * 1e3,
+        "timing": "device time of the kernels of one rank's step (per-kernel events)",
+        "slice_lm_head_hbm_gbs": 2 * w.H * (r0.hi - r0.lo) / (kms["lm_head"] / max(1, npass) / 1e3) / 1e9,
+    }
+    print(json.dumps(line), flush=True)
+    for rk in ranks:
+        rk.close()
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -249,6 +315,9 @@ def main():
     torch.cuda.set_device(dev)
 
     w = gen.make(args.workload)
+    if args.vocab_shards:
+        run_vocab_shards(args, w, dev, dst, torch)
+        return
     emit = bool(args.emit)
     from gen.torch_io import to_device
     hidden, gamma, w_t, params = to_device(w, torch, str(dev))

@@ -29,7 +29,8 @@ TAIL_ERR_DEVICE = -5
 
 EXPORTS = ("tail_create", "tail_run", "tail_run_ex", "tail_run_host", "tail_check", "tail_get_info",
            "tail_destroy", "tail_status_string", "tail_profile_enable", "tail_profile_read",
-           "tail_set_wait_limit", "tail_debug_drop_stage", "tail_last_error", "tail_run_noalloc")
+           "tail_set_wait_limit", "tail_debug_drop_stage", "tail_last_error", "tail_run_noalloc",
+           "tail_merge_shards")
 KERNELS = ("rms_rows", "lm_head", "merge")
 
 
@@ -88,6 +89,8 @@ def lib(path: str | None = None):
         L.tail_run_host.restype = ctypes.c_int
         L.tail_run_noalloc.argtypes = [ctypes.POINTER(tail_config), P, P, P, P, i32, i32, P, P, P, P]
         L.tail_run_noalloc.restype = ctypes.c_int
+        L.tail_merge_shards.argtypes = [i32, i32, i32, i32, P, P, ctypes.POINTER(i32), P, i32, P, P, P, P]
+        L.tail_merge_shards.restype = ctypes.c_int
         L.tail_check.argtypes = [P]
         L.tail_check.restype = ctypes.c_int
         L.tail_get_info.argtypes = [P, ctypes.POINTER(tail_info)]
@@ -147,6 +150,13 @@ def tail_run_noalloc(cfg: tail_config, hidden, gamma, w_t, params, n_param_cols,
                      out_logits_opt, out_status_opt, stream) -> int:
     return lib().tail_run_noalloc(ctypes.byref(cfg), hidden, gamma, w_t, params, n_param_cols, gbs,
                                   out_tokens, out_logits_opt, out_status_opt, stream)
+
+
+def tail_merge_shards(nshard, k_in, k, gbs, cand_vals, cand_idx, shard_offsets, params, n_param_cols, out_tokens,
+                      out_topk_vals_opt, out_topk_idx_opt, stream) -> int:
+    offs = (ctypes.c_int32 * len(shard_offsets))(*[int(o) for o in shard_offsets])
+    return lib().tail_merge_shards(nshard, k_in, k, gbs, cand_vals, cand_idx, offs, params, n_param_cols,
+                                   out_tokens, out_topk_vals_opt, out_topk_idx_opt, stream)
 
 
 def tail_check(h) -> int:
@@ -301,3 +311,19 @@ class Tail:
         rc = tail_check(self.h)
         if rc != TAIL_OK:
             raise TailError(rc, "tail_check")
+
+
+def merge_shards(cand_vals, cand_idx, shard_offsets, k, params=None, out_tokens=None, out_topk_vals=None,
+                 out_topk_idx=None, stream=None):
+    """tail_merge_shards with torch CUDA tensors: cand_vals [nshard, gbs, k_in] float32, cand_idx the same
+    shape int32 (ids within each shard), shard_offsets a sequence of each shard's first global id."""
+    nshard, gbs, k_in = (int(d) for d in cand_vals.shape)
+    ncols = int(params.shape[1]) if params is not None else 4
+    rc = tail_merge_shards(nshard, k_in, k, gbs, _ptr(cand_vals), _ptr(cand_idx), list(shard_offsets),
+                           _ptr(params), ncols, _ptr(out_tokens), _ptr(out_topk_vals), _ptr(out_topk_idx),
+                           _stream_ptr(stream, cand_vals.device))
+    if rc == TAIL_ERR_UNSUPPORTED:
+        raise TailError(rc, "tail_merge_shards [" + lib().tail_last_error().decode() + "]")
+    if rc != TAIL_OK:
+        raise TailError(rc, "tail_merge_shards")
+    return out_tokens

@@ -184,6 +184,32 @@ int tail_run_noalloc(const tail_config* cfg, const void* hidden, const float* ga
                      float* out_logits_opt, int32_t* out_status_opt, void* stream);
 
 /*
+ * Vocabulary-parallel tail: the merge step.  With the vocabulary split into
+ * nshard contiguous slices (one per rank, as in the page's deployment; section
+ * "Background": each rank's chunked top-k, then one top-k over the union), a
+ * rank runs tail_run_ex on its own slice (a handle created with V = the slice
+ * width, `w_t` its [H, V_s] columns, params NULL) to get its sorted top-k; the
+ * ranks exchange those (k candidates per row each: values and slice-local
+ * ids); this call then merges them on the current device and stream:
+ *   cand_vals      [nshard][gbs][k_in] fp32, each shard's top-k values (device).
+ *   cand_idx       [nshard][gbs][k_in] int32, their ids within the shard (device).
+ *   shard_offsets  [nshard] int32 (host): the first global vocabulary id of each shard.
+ *   k              the global top-k size, 1 <= k <= min(nshard * k_in, 1024);
+ *                  exact when every shard passed its top k (k_in >= k).
+ *   params, n_param_cols, out_tokens: as in tail_run (params NULL: no draw).
+ *   out_topk_vals_opt / out_topk_idx_opt: [gbs][k] the merged top-k in
+ *                  (value desc, global id asc) order, or NULL.
+ * The result equals the unsharded tail's bitwise when the shards computed the
+ * same fp32 logits (the lm_head's per-column arithmetic does not depend on how
+ * the vocabulary is split).  nshard <= 64 and nshard * k_in <= 16384;
+ * TAIL_ERR_UNSUPPORTED beyond.  No handle and no allocation.
+ */
+int tail_merge_shards(int32_t nshard, int32_t k_in, int32_t k, int32_t gbs, const float* cand_vals,
+                      const int32_t* cand_idx, const int32_t* shard_offsets, const float* params,
+                      int32_t n_param_cols, int32_t* out_tokens, float* out_topk_vals_opt,
+                      int32_t* out_topk_idx_opt, void* stream);
+
+/*
  * Synchronises the handle's device work and reads the device error flag that
  * kernels raise when a bounded wait runs out.  Returns TAIL_ERR_DEVICE (and
  * clears the flag) if it was set, TAIL_ERR_CUDA on a sticky CUDA error, else
