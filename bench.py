@@ -4,7 +4,9 @@ One step = one whole tail (RMSNorm -> lm_head -> global top-k -> sampler) over
 one batch of the synthetic workload, inputs resident in HBM.  Default
 workload: the GPT-OSS-shaped decode tail (gbs=8, H=2880, V=201088, k=256,
 emit_logits off).  The bf16 weight (1.16 GB) is far larger than the 129 MB L2,
-so every step streams it from HBM; no L2 flush is needed between steps.
+so every step streams it from HBM; no L2 flush is needed between steps.  A
+workload whose weight is below twice the L2 is timed with a 512 MiB write
+between steps, outside each step's event pair.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--emit]
     python bench.py --impl reference ...   # the fp64 CPU oracle as the reference arm
@@ -30,6 +32,8 @@ if ROOT not in sys.path:
 METRIC = "tail µs/step & rows/s at H=2880,V=201088; achieved HBM GB/s vs peak"
 SPEC_HBM_GBS = 8000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 << 20      # GB300 L2
+FLUSH_BYTES = 512 << 20   # written between timed steps when a step's weight would stay in L2
 
 
 def parse():
@@ -47,6 +51,8 @@ def parse():
                          "S slices' candidates; the all-gather between GPUs is not part of one GPU's timing)")
     ap.add_argument("--params", default="4", choices=["4", "3", "none"],
                     help="sampling_params columns: 4 (explicit u), 3 (u = 0.5), none (no sampler)")
+    ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tensor"],
+                    help="lm_head realisation: auto (by vocabulary width), mma.sync up to 8 rows, or tensor cores")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -233,7 +239,8 @@ def run_vocab_shards(args, w, dev, dst, torch):
     from gen.torch_io import to_device
     S = args.vocab_shards
     hidden, gamma, w_t, params = to_device(w, torch, str(dev))
-    kw = dict(hidden_actual=w.Hu, eps=w.eps, hidden_dtype=w.hidden_dtype, zero_interleaved_pad=bool(w.zero_pad))
+    kw = dict(hidden_actual=w.Hu, eps=w.eps, hidden_dtype=w.hidden_dtype, zero_interleaved_pad=bool(w.zero_pad),
+              path=args.path)
     vals = torch.empty((S, w.B, w.k), dtype=torch.float32, device=dev)
     idx = torch.empty((S, w.B, w.k), dtype=torch.int32, device=dev)
     tokens = torch.empty(w.B, dtype=torch.int32, device=dev)
@@ -277,6 +284,7 @@ def run_vocab_shards(args, w, dev, dst, torch):
         "data": "synthetic (seeded generators, distributions of the named workload)",
         "config": {"workload": w.name, "gbs": w.B, "H": w.H, "V": w.V, "k": w.k, "vocab_shards": S,
                    "slice_columns": r0.hi - r0.lo,
+                   "lm_head_path": ("tensor" if 0 < r0.tail.info.tc_min_rows <= w.B else "mma.sync"),
                    "measures": "one rank's step: its slice's tail + the merge; the all-gather of "
                                f"{w.B * w.k * 8} bytes per rank between GPUs is not included"},
         "slice_tail_kernel_us": {k: 1e3 * v / max(1, npass) for k, v in kms.items()},
@@ -324,7 +332,8 @@ def main():
     tokens = torch.empty(w.B, dtype=torch.int32, device=dev)
     logits = torch.empty((w.B, w.V), dtype=torch.float32, device=dev) if emit else None
     t = dst.Tail(w.H, w.V, w.k, w.B, hidden_actual=w.Hu, eps=w.eps, hidden_dtype=w.hidden_dtype,
-                 zero_interleaved_pad=bool(w.zero_pad), deferred_rms=not args.legacy_rms, device=local_rank)
+                 zero_interleaved_pad=bool(w.zero_pad), deferred_rms=not args.legacy_rms, path=args.path,
+                 device=local_rank)
     if args.params == "3":
         params = params[:, :3].contiguous()
     elif args.params == "none":
@@ -340,6 +349,12 @@ def main():
     def step():
         t.run(hidden, gamma, w_t, params, out_tokens=tokens, out_logits=logits, stream=stream)
 
+    # a weight at least twice the L2 streams from HBM every step by itself; a smaller one is flushed
+    # from L2 between timed steps
+    flush_buf = None
+    if 2 * w.H * w.V < 2 * L2_BYTES:
+        flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             step()
@@ -353,20 +368,32 @@ def main():
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)  # let the sampler come up before the timed region
-    # one event pair around the K steps: an event between steps would stand between the kernels of
-    # consecutive steps and cost them their programmatic-launch overlap
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    if flush_buf is None:
+        # one event pair around the K steps: an event between steps would stand between the kernels of
+        # consecutive steps and cost them their programmatic-launch overlap
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                step()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = ev0.elapsed_time(ev1)
+    else:
+        # the step's inputs fit in L2: overwrite L2 before every step, outside the step's event pair
+        evf = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush_buf.fill_(i)
+                evf[2 * i].record(stream)
+                step()
+                evf[2 * i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = sum(evf[2 * i].elapsed_time(evf[2 * i + 1]) for i in range(args.steps))
     clock_rec = clocks.stop()
     if dist:
         dist.barrier()
-    total_ms = ev0.elapsed_time(ev1)
     t.check()
     total_ms = max_over_ranks(total_ms, dist, dev)
     ms_step = total_ms / args.steps
@@ -376,6 +403,8 @@ def main():
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * min(args.steps, 50))]
     with torch.cuda.stream(stream):
         for i in range(0, len(evs), 2):
+            if flush_buf is not None:
+                flush_buf.fill_(i)
             evs[i].record(stream)
             step()
             evs[i + 1].record(stream)
@@ -385,7 +414,9 @@ def main():
     # ---------------- per-kernel device times (own loop: events between the kernels)
     dst.tail_profile_enable(t.h, True)
     with torch.cuda.stream(stream):
-        for _ in range(min(args.steps, 200 // max(1, passes))):
+        for i in range(min(args.steps, 200 // max(1, passes))):
+            if flush_buf is not None:
+                flush_buf.fill_(i)
             step()
     kms, npass = dst.tail_profile_read(t.h)
     dst.tail_profile_enable(t.h, False)
@@ -462,7 +493,11 @@ def main():
                    "hidden_dtype": w.hidden_dtype, "emit_logits": emit,
                    "deferred_rms": not args.legacy_rms, "sampling_params_cols": args.params,
                    "arithmetic": "bf16 W x bf16 hi+lo activations, fp32 accumulate",
-                   "l2": "no flush: the 1.16 GB weight is larger than L2 and streams from HBM every step",
+                   "l2": (f"flushed: a {FLUSH_BYTES >> 20} MiB buffer is written before every timed step, "
+                          "outside its event pair" if flush_buf is not None else
+                          f"no flush: the {2 * w.H * w.V / 1e9:.2f} GB weight is larger than L2 and streams "
+                          "from HBM every step"),
+                   "lm_head_path": "tensor" if tc_path else "mma.sync",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "step_hbm_gbs": step_gbs,
         "step_frac_of_spec_8tbs": step_gbs / SPEC_HBM_GBS,

@@ -26,6 +26,10 @@ TAIL_ERR_UNSUPPORTED = -2
 TAIL_ERR_CUDA = -3
 TAIL_ERR_OOM = -4
 TAIL_ERR_DEVICE = -5
+# tail_path: which lm_head serves which batch sizes ("gemv": mma.sync kernel up to 8 rows,
+# "tensor": tensor-core path for every batch, "auto": "tensor" for narrow vocabularies)
+PATHS = {"auto": 0, "gemv": 1, "tensor": 2}
+TC_ALL_ROWS_MAX_V = 131072
 
 EXPORTS = ("tail_create", "tail_run", "tail_run_ex", "tail_run_host", "tail_check", "tail_get_info",
            "tail_destroy", "tail_status_string", "tail_profile_enable", "tail_profile_read",
@@ -54,7 +58,7 @@ class tail_config(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("hidden_actual", ctypes.c_int32), ("V", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("gbs_max", ctypes.c_int32), ("eps", ctypes.c_float),
                 ("hidden_dtype", ctypes.c_int32), ("zero_interleaved_pad", ctypes.c_int32),
-                ("deferred_rms", ctypes.c_int32)]
+                ("deferred_rms", ctypes.c_int32), ("path", ctypes.c_int32)]
 
 
 class tail_info(ctypes.Structure):
@@ -244,14 +248,14 @@ class Tail:
     ``hidden`` is [gbs, H] (float32, float16 or bfloat16 matching ``hidden_dtype``;
     uint16/int16 bit patterns are accepted for the 16-bit types), ``gamma`` [H]
     float32, ``w_t`` [H, V] bfloat16 (or its int16 bits), ``params`` [gbs, 3|4]
-    float32 or None.
+    float32 or None.  ``path`` is a key of ``PATHS``.
     """
 
     def __init__(self, H: int, V: int, k: int = 256, gbs_max: int = 64, *, hidden_actual: int = 0,
                  eps: float = 1e-5, hidden_dtype: str = "bf16", zero_interleaved_pad: bool = True,
-                 deferred_rms: bool = True, device: int = 0):
+                 deferred_rms: bool = True, path: str = "auto", device: int = 0):
         self.cfg = tail_config(H, hidden_actual, V, k, gbs_max, eps, _DTYPES[hidden_dtype],
-                               int(zero_interleaved_pad), int(deferred_rms))
+                               int(zero_interleaved_pad), int(deferred_rms), PATHS[path])
         self.device = device
         self.h = tail_create(self.cfg, device)
         self.info = tail_get_info(self.h)

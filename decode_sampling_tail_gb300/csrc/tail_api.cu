@@ -28,6 +28,7 @@ struct tail_s {
   int max_smem;
   int nslab;
   int rows_pass;  // rows per lm_head pass
+  int tc_min;     // batches of at least this many rows take the tensor-core path; 0: none do
   int pdl_ok;     // 0 once a cooperative launch with programmatic serialization was refused
   int64_t scratch_bytes;
   // device scratch
@@ -42,7 +43,7 @@ struct tail_s {
   float* topk_val;
   int32_t* topk_idx;
   int* err;
-  // tensor-core path (gbs >= TC_MIN_ROWS)
+  // tensor-core path (gbs >= tc_min)
   uint16_t* tc_act;     // [tc_act_rows(gbs_max)][H] bf16 hi/lo rows
   float* tc_rs;         // [gbs_max] row scales
   uint64_t* tc_lists;   // [gbs_max][ntn][TC_LIST]
@@ -189,6 +190,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   *out = nullptr;
   int rc = validate_config(cfg);
   if (rc) return rc;
+  if (cfg->path < TAIL_PATH_AUTO || cfg->path > TAIL_PATH_TENSOR) return TAIL_ERR_INVALID_ARG;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return TAIL_ERR_INVALID_ARG;
   DeviceGuard guard(device);
@@ -208,14 +210,35 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   h->max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
   const int64_t npairs = cfg->V / 16;
   h->nslab = slab_count(npairs, h->num_sms, MAX_SLABS);
-  // batches of TC_MIN_ROWS rows or more run on the tensor-core path in one pass;
-  // smaller ones on the mma.sync lm_head
-  h->rows_pass = cfg->gbs_max < TC_MIN_ROWS - 1 ? cfg->gbs_max : TC_MIN_ROWS - 1;
-  const bool use_tc = cfg->gbs_max >= TC_MIN_ROWS;
   if (!prop.cooperativeLaunch) {
     delete h;
     return TAIL_ERR_UNSUPPORTED;
   }
+  // the tensor-core path, when the merge can be planned for k and V: batches of
+  // TC_MIN_ROWS rows or more always take it; narrow vocabularies take it for
+  // every batch (the mma.sync kernel's per-row bulk copies make it no faster there)
+  h->tc_ntn = tc_col_tiles(cfg->V);
+  cudaError_t te = prepare_tc(static_cast<int>(prop.sharedMemPerBlockOptin), &h->merge_dyn);
+  if (te != cudaSuccess) {
+    delete h;
+    return cuda_fail(te, "cudaFuncSetAttribute (tensor-core kernels)");
+  }
+  const bool tc_ok =
+      encode_tiled() && plan_merge(cfg->k, h->tc_ntn, h->merge_dyn, &h->merge_capc, &h->merge_sortP, &h->merge_smem);
+  if (cfg->path == TAIL_PATH_TENSOR)
+    h->tc_min = 1;
+  else if (cfg->path == TAIL_PATH_AUTO && cfg->V <= TAIL_TC_ALL_ROWS_MAX_V && tc_ok)
+    h->tc_min = 1;
+  else
+    h->tc_min = TC_MIN_ROWS;
+  const bool use_tc = cfg->gbs_max >= h->tc_min;
+  if (use_tc && !tc_ok) {
+    delete h;
+    return TAIL_ERR_UNSUPPORTED;
+  }
+  if (!use_tc) h->tc_min = 0;
+  // smaller batches run on the mma.sync lm_head, up to TC_MIN_ROWS - 1 rows a pass
+  h->rows_pass = h->tc_min == 1 ? 0 : cfg->gbs_max < TC_MIN_ROWS - 1 ? cfg->gbs_max : TC_MIN_ROWS - 1;
   int max_dyn = 0;
   cudaError_t pe2 = prepare_gemv(h->max_smem, &max_dyn);
   if (pe2 != cudaSuccess) {
@@ -231,24 +254,11 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
     }
   }
   // the slab selects hold a slab row in registers: at most SEL_NPL keys per lane
-  if ((npairs + h->nslab - 1) / h->nslab * 16 > 32 * SEL_NPL) {
+  if (h->rows_pass > 0 && (npairs + h->nslab - 1) / h->nslab * 16 > 32 * SEL_NPL) {
     delete h;
     return TAIL_ERR_UNSUPPORTED;
   }
   h->pdl_ok = 1;
-  if (use_tc) {
-    cudaError_t te = prepare_tc(static_cast<int>(prop.sharedMemPerBlockOptin), &h->merge_dyn);
-    if (te != cudaSuccess) {
-      delete h;
-      return cuda_fail(te, "cudaFuncSetAttribute (tensor-core kernels)");
-    }
-    h->tc_ntn = tc_col_tiles(cfg->V);
-    if (!encode_tiled() ||
-        !plan_merge(cfg->k, h->tc_ntn, h->merge_dyn, &h->merge_capc, &h->merge_sortP, &h->merge_smem)) {
-      delete h;
-      return TAIL_ERR_UNSUPPORTED;
-    }
-  }
 
   const int R = h->rows_pass;
   const int Rpad = ((R + 7) / 8) * 8 < 8 ? 8 : ((R + 7) / 8) * 8;
@@ -284,7 +294,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   }
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(h->bar, 0, sizeof(unsigned long long));
-  if (e == cudaSuccess) e = cudaMemset(h->row_sync, 0, static_cast<size_t>(R) * sizeof(unsigned long long));
+  if (e == cudaSuccess && R > 0) e = cudaMemset(h->row_sync, 0, static_cast<size_t>(R) * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(h->apack, 0, ksteps * mt_max * APACK_TILE_BYTES);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -299,7 +309,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   return TAIL_OK;
 }
 
-// Batches of TC_MIN_ROWS rows or more: split -> tensor-core lm_head -> merge + sampler, one pass.
+// Batches of tc_min rows or more: split -> tensor-core lm_head -> merge + sampler, one pass.
 static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
                   int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits, float* out_topk_vals,
                   int32_t* out_topk_idx, cudaStream_t stream) {
@@ -387,9 +397,10 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
                     const float* params, int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits,
                     float* out_topk_vals, int32_t* out_topk_idx, cudaStream_t stream) {
   const tail_config& c = h->cfg;
-  if (gbs >= TC_MIN_ROWS)
+  if (h->tc_min > 0 && gbs >= h->tc_min)
     return run_tc(h, hidden, gamma, w_t, params, ncols, gbs, out_tokens, out_logits, out_topk_vals, out_topk_idx,
                   stream);
+  if (h->rows_pass <= 0) return TAIL_ERR_UNSUPPORTED;  // no mma.sync scratch (not reached: tc_min is 1)
   const int K = c.k;
   const int64_t npairs = c.V / 16;
   cudaError_t e = cudaSuccess;
@@ -574,7 +585,7 @@ int tail_check(tail_t* h) {
     cudaMemset(h->err, 0, sizeof(int));
     cudaMemset(h->bar, 0, sizeof(unsigned long long));
     // so may the per-row arrival words of an interrupted run
-    cudaMemset(h->row_sync, 0, static_cast<size_t>(h->rows_pass) * sizeof(unsigned long long));
+    if (h->rows_pass > 0) cudaMemset(h->row_sync, 0, static_cast<size_t>(h->rows_pass) * sizeof(unsigned long long));
     cudaDeviceSynchronize();
     return TAIL_ERR_DEVICE;
   }
@@ -645,7 +656,7 @@ int tail_get_info(const tail_t* h, tail_info* out) {
   out->rows_per_pass = h->rows_pass;
   out->kernels_per_run = 2;
   out->scratch_bytes = h->scratch_bytes;
-  out->tc_min_rows = h->tc_lists ? TC_MIN_ROWS : 0;
+  out->tc_min_rows = h->tc_min;
   return TAIL_OK;
 }
 

@@ -60,7 +60,27 @@ typedef struct {
                                       so all H lanes are summed; 0: lanes [H_u, H) are ignored */
   int32_t deferred_rms;         /* 1 (default): rstd scales the GEMM output per row;
                                    0: legacy form, (x * rstd) * gamma feeds the GEMM */
+  int32_t path;                 /* tail_path: which lm_head serves which batch sizes (no page
+                                   counterpart: both compute the same logits, within the
+                                   logit tolerance).  Ignored by tail_run_noalloc. */
 } tail_config;
+
+/*
+ * lm_head realisations.  The cooperative mma.sync kernel streams W once for up
+ * to 8 rows and fuses the top-k and the sampler; it issues one bulk copy per
+ * W row per stage, so its time hardly falls below ~150 us however narrow the
+ * vocabulary.  The tensor-core path (split, tcgen05 lm_head with per-tile
+ * candidate lists, merge + sampler) serves any batch in one pass.
+ */
+typedef enum {
+  TAIL_PATH_AUTO = 0,   /* tensor cores for every batch when V <= TAIL_TC_ALL_ROWS_MAX_V,
+                           else as TAIL_PATH_GEMV */
+  TAIL_PATH_GEMV = 1,   /* mma.sync kernel for gbs <= 8, tensor cores for gbs >= 9 */
+  TAIL_PATH_TENSOR = 2  /* tensor cores for every batch (TAIL_ERR_UNSUPPORTED at create
+                           when the merge cannot be planned for k and V) */
+} tail_path;
+
+#define TAIL_TC_ALL_ROWS_MAX_V 131072
 
 /* Static facts about a handle, for benchmarks and tests. */
 typedef struct {
@@ -74,7 +94,7 @@ typedef struct {
   int64_t scratch_bytes;    /* device scratch owned by the handle */
   int32_t tc_min_rows;      /* runs with gbs >= this take the tensor-core path (split, tcgen05
                                lm_head with per-tile candidate lists, merge + sampler: 3 kernels,
-                               one pass); 0 when gbs_max is below it */
+                               one pass): 1 or 9 by cfg.path; 0 when gbs_max is below it */
 } tail_info;
 
 /*

@@ -43,7 +43,7 @@ def test_config_validation_without_gpu(L):
     h = ctypes.c_void_p()
     def create(**kw):
         base = dict(H=256, hidden_actual=0, V=4096, k=16, gbs_max=4, eps=1e-5, hidden_dtype=0,
-                    zero_interleaved_pad=1, deferred_rms=1)
+                    zero_interleaved_pad=1, deferred_rms=1, path=0)
         base.update(kw)
         cfg = dst.tail_config(*[base[f[0]] for f in dst.tail_config._fields_])
         return L.tail_create(ctypes.byref(cfg), 0, ctypes.byref(h))
@@ -57,6 +57,8 @@ def test_config_validation_without_gpu(L):
     assert create(eps=-1.0) == dst.TAIL_ERR_INVALID_ARG
     assert create(H=100) == dst.TAIL_ERR_UNSUPPORTED               # H % 16
     assert create(V=4100) == dst.TAIL_ERR_UNSUPPORTED              # V % 16
+    assert create(path=3) == dst.TAIL_ERR_INVALID_ARG
+    assert create(path=-1) == dst.TAIL_ERR_INVALID_ARG
     assert L.tail_create(None, 0, ctypes.byref(h)) == dst.TAIL_ERR_INVALID_ARG
     assert h.value is None
 
@@ -75,3 +77,25 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(dst, "_lib", None)
     with pytest.raises(dst.TailLibraryMissing):
         dst.lib(str(tmp_path / "absent.so"))
+
+
+def header_struct_fields(name):
+    """Field names of `typedef struct { ... } name;` in include/tail.h, in order."""
+    import re
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct \{([^{}]*)\}\s*" + name + ";", text).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    return re.findall(r"\b(\w+);", body)
+
+
+def test_python_structs_mirror_the_header():
+    assert [f[0] for f in dst.tail_config._fields_] == header_struct_fields("tail_config")
+    assert [f[0] for f in dst.tail_info._fields_] == header_struct_fields("tail_info")
+
+
+def test_path_constants_mirror_the_header():
+    import re
+    text = open(HEADER).read()
+    for key, name in (("auto", "AUTO"), ("gemv", "GEMV"), ("tensor", "TENSOR")):
+        assert int(re.search(r"TAIL_PATH_" + name + r"\s*=\s*(\d+)", text).group(1)) == dst.PATHS[key]
+    assert int(re.search(r"#define TAIL_TC_ALL_ROWS_MAX_V (\d+)", text).group(1)) == dst.TC_ALL_ROWS_MAX_V

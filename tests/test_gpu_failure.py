@@ -24,7 +24,7 @@ def test_wait_that_runs_out_is_reported_and_recoverable():
     w = gen.custom(8, 512, 65536, 64, hidden_dtype="bf16", seed=61)
     hidden, gamma, w_t, p = tc.to_device(w, torch)
     tok = torch.zeros(w.B, dtype=torch.int32, device=hidden.device)
-    with dst.Tail(w.H, w.V, w.k, w.B) as t:
+    with dst.Tail(w.H, w.V, w.k, w.B, path="gemv") as t:  # the hook drops a stage of the mma.sync ring
         assert dst.tail_set_wait_limit(t.h, 2_000_000) == dst.TAIL_OK
         assert dst.tail_debug_drop_stage(t.h, 3) == dst.TAIL_OK
         t.run(hidden, gamma, w_t, p, out_tokens=tok)

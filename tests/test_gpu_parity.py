@@ -25,6 +25,13 @@ def make_tail(w, gbs_max=None, **kw):
                     hidden_dtype=w.hidden_dtype, zero_interleaved_pad=bool(w.zero_pad), **kw)
 
 
+@pytest.fixture(params=["gemv", "tensor"])
+def path(request):
+    """The lm_head realisation a small-batch test runs on: the cooperative mma.sync kernel, or the
+    tensor-core path that narrow vocabularies take for every batch size."""
+    return request.param
+
+
 def full_check(w, res, rows=None, params=None):
     rows = np.arange(w.B) if rows is None else np.asarray(rows)
     L, ov, oi = tc.oracle_rows(w, rows)
@@ -54,7 +61,7 @@ SMALL = [
 
 
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: f"B{s[0]}_H{s[1]}_V{s[2]}_k{s[3]}_{s[4]}")
-def test_small_shapes_match_oracle(shape):
+def test_small_shapes_match_oracle(shape, path):
     B, H, V, k, dt, Hu, zp = shape
     w = gen.custom(B, H, V, k, hidden_dtype=dt, Hu=Hu, zero_pad=zp, seed=1000 + B)
     if Hu is not None and not zp:
@@ -63,16 +70,16 @@ def test_small_shapes_match_oracle(shape):
             w.hidden[:, Hu:] = 3.0
         else:
             w.hidden[:, Hu:] = 0x4040
-    with make_tail(w) as t:
+    with make_tail(w, path=path) as t:
         res = tc.run_gpu(t, w, torch)
     exact, exempt = full_check(w, res)
     assert exact + exempt == B and exact >= B - max(1, B // 8)
 
 
 @pytest.mark.parametrize("ncols", ["3col", "none"])
-def test_param_column_forms(ncols):
+def test_param_column_forms(ncols, path):
     w = gen.custom(6, 64, 2048, 32, hidden_dtype="bf16", seed=77)
-    with make_tail(w) as t:
+    with make_tail(w, path=path) as t:
         res = tc.run_gpu(t, w, torch, params=ncols)
     if ncols == "none":
         assert np.all(res.tokens == -7), "tokens written although params is NULL"
@@ -83,32 +90,32 @@ def test_param_column_forms(ncols):
         assert exact >= 5
 
 
-def test_legacy_rms_realization_matches_oracle():
+def test_legacy_rms_realization_matches_oracle(path):
     w = gen.custom(8, 256, 8192, 64, hidden_dtype="bf16", seed=55)
-    with make_tail(w, deferred_rms=False) as t:
+    with make_tail(w, deferred_rms=False, path=path) as t:
         legacy = tc.run_gpu(t, w, torch)
-    with make_tail(w) as t:
+    with make_tail(w, path=path) as t:
         deferred = tc.run_gpu(t, w, torch)
     full_check(w, legacy)
     assert np.max(np.abs(legacy.logits - deferred.logits)) < 1e-5
 
 
-def test_sixteen_bit_input_equals_prewidened_fp32():
+def test_sixteen_bit_input_equals_prewidened_fp32(path):
     w16 = gen.custom(8, 128, 4096, 64, hidden_dtype="bf16", seed=56)
     w32 = gen.custom(8, 128, 4096, 64, hidden_dtype="bf16", seed=56)
     w32.hidden = gen.bf16_bits_to_f32(w16.hidden)
     w32.hidden_dtype = "f32"
-    with make_tail(w16) as t:
+    with make_tail(w16, path=path) as t:
         a = tc.run_gpu(t, w16, torch)
-    with make_tail(w32) as t:
+    with make_tail(w32, path=path) as t:
         b = tc.run_gpu(t, w32, torch)
     assert np.array_equal(a.logits.view(np.uint32), b.logits.view(np.uint32))
     assert np.array_equal(a.topk_idx, b.topk_idx) and np.array_equal(a.tokens, b.tokens)
 
 
-def test_repeat_runs_bitwise_identical_and_rows_independent_of_batch():
+def test_repeat_runs_bitwise_identical_and_rows_independent_of_batch(path):
     w = gen.custom(8, 128, 4096, 64, hidden_dtype="bf16", seed=57)
-    with make_tail(w) as t:
+    with make_tail(w, path=path) as t:
         r1 = tc.run_gpu(t, w, torch)
         r2 = tc.run_gpu(t, w, torch)
     assert np.array_equal(r1.logits.view(np.uint32), r2.logits.view(np.uint32))
@@ -118,20 +125,20 @@ def test_repeat_runs_bitwise_identical_and_rows_independent_of_batch():
         sub.hidden = np.ascontiguousarray(w.hidden[:nb])
         sub.params = np.ascontiguousarray(w.params[:nb])
         sub.B = nb
-        with make_tail(sub) as t:
+        with make_tail(sub, path=path) as t:
             rs = tc.run_gpu(t, sub, torch)
         assert np.array_equal(rs.logits.view(np.uint32), r1.logits[:nb].view(np.uint32))
         assert np.array_equal(rs.tokens, r1.tokens[:nb])
 
 
-def test_outputs_untouched_outside_their_rows():
+def test_outputs_untouched_outside_their_rows(path):
     w = gen.custom(5, 64, 2048, 32, hidden_dtype="bf16", seed=58)
     hidden, gamma, w_t, p = tc.to_device(w, torch)
     dev = hidden.device
     guard = 4096
     tok = torch.full((w.B + 2 * guard,), 12345, dtype=torch.int32, device=dev)
     lg = torch.full((w.B * w.V + 2 * guard,), 7.5, dtype=torch.float32, device=dev)
-    with make_tail(w) as t:
+    with make_tail(w, path=path) as t:
         t.run(hidden, gamma, w_t, p, out_tokens=tok[guard:guard + w.B],
               out_logits=lg[guard:guard + w.B * w.V].view(w.B, w.V))
         torch.cuda.synchronize()
@@ -140,10 +147,10 @@ def test_outputs_untouched_outside_their_rows():
     assert np.all(lg_h[:guard] == 7.5) and np.all(lg_h[guard + w.B * w.V:] == 7.5)
 
 
-def test_host_entry_point_matches_device_entry_point():
+def test_host_entry_point_matches_device_entry_point(path):
     w = gen.custom(4, 64, 2048, 32, hidden_dtype="bf16", seed=59)
     hidden, gamma, w_t, p = tc.to_device(w, torch)
-    with make_tail(w) as t:
+    with make_tail(w, path=path) as t:
         dev = tc.run_gpu(t, w, torch, dev_tensors=(hidden, gamma, w_t, p))
         toks = np.zeros(w.B, np.int32)
         logits = np.zeros((w.B, w.V), np.float32)
@@ -152,11 +159,11 @@ def test_host_entry_point_matches_device_entry_point():
     assert np.array_equal(logits.view(np.uint32), dev.logits.view(np.uint32))
 
 
-def test_invalid_arguments_return_status_codes():
+def test_invalid_arguments_return_status_codes(path):
     w = gen.custom(4, 64, 2048, 32, hidden_dtype="bf16", seed=60)
     hidden, gamma, w_t, p = tc.to_device(w, torch)
     tok = torch.zeros(8, dtype=torch.int32, device=hidden.device)
-    with make_tail(w) as t:
+    with make_tail(w, path=path) as t:
         s = t._stream(None)
         P = dst._ptr
         # gbs beyond gbs_max
@@ -171,7 +178,7 @@ def test_invalid_arguments_return_status_codes():
         # gbs == 0 is a no-op
         assert dst.tail_run(t.h, None, None, None, None, 4, 0, None, None, s) == dst.TAIL_OK
         assert dst.tail_check(t.h) == dst.TAIL_OK
-    bad_cfg = dst.tail_config(100, 0, 2048, 32, 4, 1e-5, 2, 1, 1)  # H % 16 != 0
+    bad_cfg = dst.tail_config(100, 0, 2048, 32, 4, 1e-5, 2, 1, 1, dst.PATHS[path])  # H % 16 != 0
     with pytest.raises(dst.TailError) as ei:
         dst.tail_create(bad_cfg, 0)
     assert ei.value.status == dst.TAIL_ERR_UNSUPPORTED
@@ -195,12 +202,28 @@ def test_gptoss_g8_full(g8, emit):
     assert exact >= 7
 
 
-def test_tiny_full():
+def test_tiny_full(path):
     w = gen.make("tiny")
-    with make_tail(w) as t:
+    with make_tail(w, path=path) as t:
         res = tc.run_gpu(t, w, torch)
     exact, exempt = full_check(w, res)
     assert exact == 1
+
+
+def test_auto_path_choice_follows_vocabulary_width():
+    # narrow vocabularies: tensor cores for every batch; wider ones: mma.sync up to 8 rows
+    # (tc_min_rows 0: no batch a handle of gbs_max 8 accepts reaches the tensor-core path)
+    for V, gbs_max, want in ((dst.TC_ALL_ROWS_MAX_V, 8, 1), (dst.TC_ALL_ROWS_MAX_V + 16, 8, 0),
+                             (dst.TC_ALL_ROWS_MAX_V + 16, 9, 9)):
+        with dst.Tail(64, V, 16, gbs_max) as t:
+            assert t.info.tc_min_rows == want
+            assert (t.info.rows_per_pass == 0) == (want == 1)
+    with dst.Tail(64, 4096, 16, 8, path="gemv") as t:
+        assert t.info.tc_min_rows == 0 and t.info.rows_per_pass == 8
+    with dst.Tail(64, 4096, 16, 16, path="gemv") as t:
+        assert t.info.tc_min_rows == 9
+    with dst.Tail(64, 1 << 18, 16, 2, path="tensor") as t:
+        assert t.info.tc_min_rows == 1
 
 
 def test_padded_g64_full():

@@ -1,8 +1,9 @@
 """The vocabulary-parallel tail on one GPU ("simulated shards"): every slice
 runs the tail with its own weight columns and no sampler, the slices' top-k
 lists are merged by tail_merge_shards, and the result must equal the
-unsharded tail bit for bit (the lm_head's arithmetic for a column does not
-depend on how the vocabulary is split) -- tokens, top-k ids and values."""
+unsharded tail bit for bit when both run the same lm_head realisation (the
+arithmetic for a column does not depend on how the vocabulary is split) --
+tokens, top-k ids and values."""
 import numpy as np
 import pytest
 
@@ -19,19 +20,25 @@ import decode_sampling_tail_gb300 as dst  # noqa: E402
 from decode_sampling_tail_gb300.vocab_parallel import ShardedTail  # noqa: E402
 
 
-def unsharded(w, dev):
+@pytest.fixture(params=["gemv", "tensor"])
+def path(request):
+    return request.param
+
+
+def unsharded(w, dev, path="auto"):
     hidden, gamma, w_t, params = dev
     with dst.Tail(w.H, w.V, w.k, w.B, hidden_actual=w.Hu, eps=w.eps, hidden_dtype=w.hidden_dtype,
-                  zero_interleaved_pad=bool(w.zero_pad)) as t:
+                  zero_interleaved_pad=bool(w.zero_pad), path=path) as t:
         return tc.run_gpu(t, w, torch, dev_tensors=dev)
 
 
-def sharded(w, dev, nshard, params_form="all"):
+def sharded(w, dev, nshard, params_form="all", path="auto"):
     hidden, gamma, w_t, params = dev
     vals = torch.empty((nshard, w.B, w.k), dtype=torch.float32, device="cuda")
     idx = torch.empty((nshard, w.B, w.k), dtype=torch.int32, device="cuda")
     ranks = [ShardedTail(w.H, w.V, w.k, w.B, s, nshard, hidden_actual=w.Hu, eps=w.eps,
-                         hidden_dtype=w.hidden_dtype, zero_interleaved_pad=bool(w.zero_pad)) for s in range(nshard)]
+                         hidden_dtype=w.hidden_dtype, zero_interleaved_pad=bool(w.zero_pad), path=path)
+             for s in range(nshard)]
     try:
         for s, rk in enumerate(ranks):
             w_slice = w_t[:, rk.lo:rk.hi].contiguous()
@@ -51,11 +58,11 @@ def sharded(w, dev, nshard, params_form="all"):
 
 
 @pytest.mark.parametrize("nshard", [2, 8])
-def test_gptoss_g8_vocab_shards_equal_the_unsharded_tail(nshard):
+def test_gptoss_g8_vocab_shards_equal_the_unsharded_tail(nshard, path):
     w = gen.make("gptoss_g8")
     dev = tc.to_device(w, torch)
-    ref = unsharded(w, dev)
-    tok, tv, ti = sharded(w, dev, nshard)
+    ref = unsharded(w, dev, path)
+    tok, tv, ti = sharded(w, dev, nshard, path=path)
     assert np.array_equal(ti, ref.topk_idx)
     assert np.array_equal(tv.view(np.uint32), ref.topk_vals.view(np.uint32))
     assert np.array_equal(tok, ref.tokens)
@@ -63,12 +70,12 @@ def test_gptoss_g8_vocab_shards_equal_the_unsharded_tail(nshard):
 
 @pytest.mark.parametrize("shape", [(5, 128, 4096, 64, "f16"), (20, 160, 8192, 100, "bf16"), (70, 64, 6144, 33, "f32")],
                          ids=lambda s: f"B{s[0]}_V{s[2]}_k{s[3]}")
-def test_small_vocab_shards_equal_the_unsharded_tail_and_the_oracle(shape):
+def test_small_vocab_shards_equal_the_unsharded_tail_and_the_oracle(shape, path):
     B, H, V, k, dt = shape
     w = gen.custom(B, H, V, k, hidden_dtype=dt, seed=4000 + B, dup_cols=2)  # ties that straddle slice edges
     dev = tc.to_device(w, torch)
-    ref = unsharded(w, dev)
-    tok, tv, ti = sharded(w, dev, 3)
+    ref = unsharded(w, dev, path)
+    tok, tv, ti = sharded(w, dev, 3, path=path)
     assert np.array_equal(ti, ref.topk_idx) and np.array_equal(tok, ref.tokens)
     L, ov, oi = tc.oracle_rows(w, np.arange(B))
     tc.check_topk(tv, ti, L, ov, oi, w.k, ref.logits)

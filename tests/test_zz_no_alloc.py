@@ -45,7 +45,7 @@ def run_handle(w, hidden, gamma, w_t, params):
     tok = torch.full((B,), -7, dtype=torch.int32, device="cuda")
     lg = torch.empty((B, V), dtype=torch.float32, device="cuda")
     with dst.Tail(hidden.shape[1], V, w.k, B, hidden_actual=w.Hu, eps=w.eps, hidden_dtype=w.hidden_dtype,
-                  zero_interleaved_pad=bool(w.zero_pad)) as t:
+                  zero_interleaved_pad=bool(w.zero_pad), path="gemv") as t:
         t.run(hidden, gamma, w_t, params, out_tokens=tok, out_logits=lg)
         torch.cuda.synchronize()
         t.check()
@@ -158,7 +158,7 @@ def test_noalloc_invalid_arguments():
     gamma = torch.ones((H,), dtype=torch.float32, device="cuda")
     w_t = torch.zeros((H, V), dtype=torch.bfloat16, device="cuda")
     params = torch.zeros((2, 4), dtype=torch.float32, device="cuda")
-    cfg = dst.tail_config(H, 0, V, 8, 1, 1e-5, dst.TAIL_BF16, 1, 1)   # gbs_max 1 < gbs 2
+    cfg = dst.tail_config(H, 0, V, 8, 1, 1e-5, dst.TAIL_BF16, 1, 1, 0)   # gbs_max 1 < gbs 2
     ptr = lambda t: t.data_ptr()  # noqa: E731
     s = torch.cuda.current_stream().cuda_stream
     assert dst.tail_run_noalloc(cfg, ptr(hidden), ptr(gamma), ptr(w_t), ptr(params), 4, 2, None, None, None,
