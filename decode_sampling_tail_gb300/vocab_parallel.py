@@ -13,6 +13,12 @@ Per step, every rank
      id) and draws the token -- every rank the same token, so the sampler is
      replicated rather than owned.
 
+Row ownership (the page's `owned_row_block`, single hop): instead of the
+all-gather, an all-to-all sends every rank only the candidates of the rows it
+owns, a contiguous block of gbs / N rows; each rank merges and samples those
+rows alone, with `sampling_params` holding only its own rows.  The exchange
+then moves gbs * k * 8 bytes per rank in total rather than N times that.
+
 On one GPU the same functions run the slices one after another ("simulated
 shards"); the result equals the unsharded tail bit for bit, because the
 lm_head's arithmetic for a column does not depend on how the vocabulary is
@@ -32,6 +38,31 @@ def shard_bounds(V: int, nshard: int) -> list[int]:
         raise ValueError(f"cannot split V={V} into {nshard} slices of whole 16-column pairs")
     pairs = V // COL_ALIGN
     return [COL_ALIGN * (pairs * s // nshard) for s in range(nshard + 1)]
+
+
+def owned_row_block(rank: int, vtp: int, gbs: int) -> tuple[int, int]:
+    """(row_start, n_rows): the contiguous block of batch rows `rank` owns after the exchange
+    (page function `owned_row_block`, one hop).  gbs must split evenly over the vtp ranks."""
+    if vtp < 1 or not 0 <= rank < vtp or gbs % vtp:
+        raise ValueError(f"gbs={gbs} rows do not split into {vtp} equal blocks (rank {rank})")
+    n = gbs // vtp
+    return rank * n, n
+
+
+def exchange_candidates(vals, idx, group=None):
+    """All-to-all of this rank's [gbs, k] candidates: rank q receives, from every rank in rank
+    order, the rows of q's block.  Returns [nshard, gbs / nshard, k] tensors for this rank's rows."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    gbs, k = int(vals.shape[0]), int(vals.shape[1])
+    owned_row_block(0, world, gbs)  # validates the split
+    out_v = torch.empty_like(vals)
+    out_i = torch.empty_like(idx)
+    # row blocks are contiguous in [gbs, k]: block q goes to rank q; the receive is source-rank major
+    dist.all_to_all_single(out_v, vals.contiguous(), group=group)
+    dist.all_to_all_single(out_i, idx.contiguous(), group=group)
+    return out_v.view(world, gbs // world, k), out_i.view(world, gbs // world, k)
 
 
 def gather_candidates(vals, idx, group=None):
@@ -70,12 +101,24 @@ class ShardedTail:
         return merge_shards(all_vals, all_idx, self.bounds[:-1], self.k, params=params, out_tokens=out_tokens,
                             out_topk_vals=out_topk_vals, out_topk_idx=out_topk_idx, stream=stream)
 
-    def step(self, hidden, gamma, w_slice, params, out_tokens, group=None, stream=None):
-        """One vocabulary-parallel step on this rank: local top-k, all-gather, merge and draw."""
+    def step(self, hidden, gamma, w_slice, params, out_tokens, group=None, stream=None, owned_rows=False):
+        """One vocabulary-parallel step on this rank: local top-k, exchange, merge and draw.
+
+        owned_rows=False: all-gather, every rank draws every row (params and out_tokens [gbs]).
+        owned_rows=True: all-to-all, this rank draws only its `owned_row_block` (params and
+        out_tokens hold those gbs / N rows)."""
+        import contextlib
+
         import torch
         gbs = int(hidden.shape[0])
-        vals = torch.empty((gbs, self.k), dtype=torch.float32, device=hidden.device)
-        idx = torch.empty((gbs, self.k), dtype=torch.int32, device=hidden.device)
-        self.local_topk(hidden, gamma, w_slice, vals, idx, stream=stream)
-        all_v, all_i = gather_candidates(vals, idx, group)
-        return self.merge(all_v, all_i, params, out_tokens, stream=stream)
+        # the collective orders itself after the current stream: make that the kernels' stream
+        ctx = torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+        with ctx:
+            vals = torch.empty((gbs, self.k), dtype=torch.float32, device=hidden.device)
+            idx = torch.empty((gbs, self.k), dtype=torch.int32, device=hidden.device)
+            self.local_topk(hidden, gamma, w_slice, vals, idx, stream=stream)
+            if owned_rows:
+                all_v, all_i = exchange_candidates(vals, idx, group)
+            else:
+                all_v, all_i = gather_candidates(vals, idx, group)
+            return self.merge(all_v, all_i, params, out_tokens, stream=stream)

@@ -97,3 +97,32 @@ def test_merge_without_sampler_leaves_tokens_and_rejects_bad_arguments():
                                  s) == dst.TAIL_ERR_INVALID_ARG  # k above nshard * k_in
     assert dst.tail_merge_shards(0, 16, 8, 4, v.data_ptr(), i.data_ptr(), [], None, 4, None, None, None,
                                  s) == dst.TAIL_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("nshard", [2, 4])
+def test_owned_row_blocks_draw_the_unsharded_tokens(nshard, path):
+    # the all-to-all of owned rows, simulated: rank q merges [nshard, gbs / nshard, k] candidates of
+    # its row block with only its rows' sampling parameters
+    from decode_sampling_tail_gb300.vocab_parallel import owned_row_block
+    w = gen.custom(8, 256, 16384, 64, hidden_dtype="bf16", seed=4200, dup_cols=2)
+    dev = tc.to_device(w, torch)
+    hidden, gamma, w_t, params = dev
+    ref = unsharded(w, dev, path)
+    vals = torch.empty((nshard, w.B, w.k), dtype=torch.float32, device="cuda")
+    idx = torch.empty((nshard, w.B, w.k), dtype=torch.int32, device="cuda")
+    ranks = [ShardedTail(w.H, w.V, w.k, w.B, s, nshard, path=path) for s in range(nshard)]
+    try:
+        for s, rk in enumerate(ranks):
+            rk.local_topk(hidden, gamma, w_t[:, rk.lo:rk.hi].contiguous(), vals[s], idx[s])
+        for q, rk in enumerate(ranks):
+            r0, n = owned_row_block(q, nshard, w.B)
+            tok = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+            ti = torch.empty((n, w.k), dtype=torch.int32, device="cuda")
+            rk.merge(vals[:, r0:r0 + n].contiguous(), idx[:, r0:r0 + n].contiguous(),
+                     params[r0:r0 + n].contiguous(), tok, out_topk_idx=ti)
+            torch.cuda.synchronize()
+            assert np.array_equal(tok.cpu().numpy(), ref.tokens[r0:r0 + n])
+            assert np.array_equal(ti.cpu().numpy(), ref.topk_idx[r0:r0 + n])
+    finally:
+        for rk in ranks:
+            rk.close()
