@@ -16,13 +16,20 @@ constexpr int GEMV_KPB = 2;          // ring stage = 32 rows of W
 constexpr int GEMV_MAX_STAGES = 8;
 constexpr int MAX_K = 1024;
 constexpr int MAX_SLABS = 160;       // vocabulary slabs (lm_head CTAs) at most
-constexpr int TAIL_PUB_PER_SLAB = 4; // lane maxima each (row, slab) publishes for the global bound
-constexpr int PHASE_C_CAP = 16384;   // candidates of one row held in shared memory at once
-constexpr int RANK_SORT_MAX = 640;   // up to this many candidates phase C ranks them all directly
+constexpr int SLAB_LEADERS = 8;      // lane maxima behind each (row, slab)'s publication bound b
+constexpr int SLAB_BOUND_KEYS = 4;   // of them, published for the owner's global bound
+constexpr int SLAB_META_WORDS = 8;   // per (row, slab): 4 leader keys, candidate count, b, 2 spare
+constexpr int SLAB_CAND = 32;        // candidate slots per (row, slab); more elements >= b: none published
+constexpr int RANK_SORT_MAX = 640;   // up to this many candidates the row owner ranks them all directly
 constexpr uint64_t DEFAULT_TIMEOUT_NS = 1000000000ull;  // 1 s bound on every device wait
 
-// Slab c of nslab covers column pairs [pair_lo(c), pair_lo(c+1)) of V/16 pairs.
-__host__ __device__ inline int64_t slab_pair_lo(int64_t npairs, int nslab, int c) { return npairs * c / nslab; }
+// Slab c of nslab covers column pairs [pair_lo(c), pair_lo(c+1)) of V/16 pairs:
+// floor(npairs * c / nslab), written as q * c + floor(r * c / nslab) with
+// npairs = q * nslab + r so that only 32-bit divisions occur (npairs < 2^27).
+__host__ __device__ inline int64_t slab_pair_lo(int64_t npairs, int nslab, int c) {
+  const int np = static_cast<int>(npairs);
+  return static_cast<int64_t>(np / nslab) * c + (np % nslab) * c / nslab;
+}
 
 struct RmsArgs {
   const void* hidden;
@@ -45,12 +52,10 @@ struct GemvArgs {
   const float* row_scale;   // [B_pad]
   float* logits_out;        // [B, V] caller logits for this pass, or null
   int64_t logits_out_ld;    // row stride of logits_out in floats
-  float* logits_scratch;    // [B, V] staging when the slab logits do not fit in shared memory
-  uint32_t* pub;            // [B][nslab][TAIL_PUB_PER_SLAB] published lane maxima
-  uint32_t* cand_key;       // [B][nslab * K] order keys of each row's emitted candidates, packed
-  int32_t* cand_idx;        // [B][nslab * K] their vocabulary ids
-  unsigned long long* row_sync;  // [B]: (slabs emitted << 32) | candidates reserved; 0 between runs
-  unsigned long long* bar;  // grid barrier arrival counter (grows monotonically)
+  float* logits_scratch;    // [B, V] the logits when the caller takes none (the row owner rescans it)
+  uint32_t* meta;           // [B][nslab][SLAB_META_WORDS] each slab's publication per row
+  uint64_t* cand;           // [B][nslab][SLAB_CAND] published candidates as (key, id) composites
+  unsigned long long* row_sync;  // [B]: slabs that have published the row; 0 between runs
   float* topk_val;          // [B][topk_ld] sorted top-k logits
   int32_t* topk_idx;        // [B][topk_ld] their vocabulary ids
   int64_t topk_ld;
@@ -67,7 +72,7 @@ struct GemvArgs {
   int logits_in_smem;
   int max_slab_cols;
   int smem_bytes;
-  int capc;                 // phase C candidate capacity (shared memory)
+  int capc;                 // row owner candidate capacity (shared memory)
   int sortP;                // composite buffer entries: max(next power of two >= K, RANK_SORT_MAX)
   uint64_t timeout_ns;
   int drop_iter;            // test hook: ring iteration the producer never issues (-1: none)

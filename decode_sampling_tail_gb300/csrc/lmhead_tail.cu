@@ -26,18 +26,19 @@
 //   * Every column's k-reduction runs through the same mma sequence wherever
 //     the column sits, so duplicated W columns give bitwise-equal logits.
 //
-// Top-k and sampler, in three phases separated by a grid barrier (the launch
-// is cooperative, so every CTA is resident; each wait is bounded):
-//   A  per (row, slab): publish the 4 largest of the 32 lane maxima of the
-//      slab's logits.  They are 4 distinct elements of the row.
-//   B  per row: x = the K-th largest of the nslab * 4 published keys.  At
-//      least K elements of the row are >= x, so the row's K-th largest key is
-//      >= x and every global top-K element is >= x.  Each CTA emits its slab
-//      elements >= x (its exact slab top-K if more than K pass) -- a handful
-//      per slab instead of K.
-//   C  CTA r gathers row r's candidates, keeps the top K (ties at the
-//      boundary settled by index), sorts them, writes the top-k outputs and
-//      runs the sampler on warp 0.
+// Top-k and sampler, in two phases with one exchange between them (the launch
+// is cooperative, so every CTA is resident and the owners' waits end; each
+// wait is bounded):
+//   P  per (row, slab), no waiting: b = the 8th largest of the 32 lane maxima
+//      of the slab's logits (8 distinct elements are >= b).  The slab
+//      publishes every element >= b (typically ~10), b, and its 4 largest lane
+//      maxima, then releases the row's arrival word.
+//   O  CTA r, once all slabs have published row r: x = a lower bound of the
+//      K-th largest of the nslab * 4 lane maxima (K distinct elements are
+//      >= x); ranks the published candidates >= x; v = the K-th of them.  Only
+//      a slab with b > v can hide a top-K element (in [v, b)); its row of the
+//      global logits copy is rescanned.  Then the sorted top-k outputs and the
+//      draw, with every thread of the CTA.
 #include "common.cuh"
 #include "internal.h"
 #include "sampler.cuh"
@@ -49,52 +50,333 @@ namespace {
 
 constexpr int MAX_STAGES = 8;
 constexpr int BAR_REGION = 256;  // ring barriers and control words at the start of shared memory
-constexpr int PUB = TAIL_PUB_PER_SLAB;
-constexpr int NPUB_L = (PUB * MAX_SLABS + 31) / 32;  // published keys per lane in phase B
-constexpr int GATHER_PT = 4;                           // candidate loads in flight per thread in phase C
+constexpr int NLEAD_L = SLAB_BOUND_KEYS * ((MAX_SLABS + 31) / 32);  // leader keys per lane of the owner's bound
+constexpr int NGATHER = (MAX_SLABS * SLAB_CAND + GEMV_THREADS - 33) / (GEMV_THREADS - 32);  // slots per gatherer
+static_assert(SLAB_BOUND_KEYS == 4 && SLAB_META_WORDS == 8, "a slab's publication is two 16-byte stores");
+static_assert(SLAB_LEADERS >= SLAB_BOUND_KEYS && SLAB_LEADERS <= 32, "leaders are distinct lane maxima");
+static_assert(SLAB_CAND == 32 && (GEMV_THREADS - 32) % 32 == 0, "the owner's gather reads one slab per warp step");
 
 __device__ __forceinline__ void consumer_barrier() {
   asm volatile("bar.sync 1, %0;" ::"r"(GEMV_CONSUMER_WARPS * 32) : "memory");
 }
 
-// Grid-wide barrier over the co-resident CTAs of a cooperative launch.  The
-// counter only grows (each barrier adds gridDim.x), so generations never
-// collide.  Returns false, after raising the error flag, if the wait ran out.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* counter, uint64_t limit_ns, int* err,
-                                             volatile int* s_flag) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned long long nb = gridDim.x;
-    const unsigned long long old = atomicAdd(counter, 1ull);
-    const unsigned long long target = (old / nb + 1) * nb;
-    int ok = 1;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-      unsigned long long cur;
-      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(cur) : "l"(counter) : "memory");
-      if (cur >= target) break;
-      if (global_timer_ns() - t0 > limit_ns) {
-        raise_error(err, DEV_TIMEOUT_BARRIER);
-        ok = 0;
-        break;
+// The post-stream phases.  They are inlined: a kernel that holds a real call
+// (even one never taken) streams the weight markedly slower.
+
+// ================================================================ phase P: publish the slab's leaders
+// Per row: the SLAB_LEADERS largest lane maxima are distinct elements of the
+// slab, so at least that many slab elements are >= b, the smallest of them.
+// The slab publishes every element >= b (up to SLAB_CAND of them, else none,
+// with b raised above every key), b, and its SLAB_BOUND_KEYS largest lane
+// maxima -- distinct elements of the row, for the owner's global bound.  An
+// unpublished element of the slab is below b.  Nothing waits here: a release
+// on the row's arrival word hands the publication to the row's owner.
+__device__ __forceinline__ void publish_rows(const GemvArgs& a, const float* slab_logits, int max_cols, int n,
+                                         int64_t vbase, int c) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto load_row_keys = [&](int r, uint32_t (&k)[SEL_NPL]) {
+    const float* src = a.logits_in_smem ? slab_logits + r * max_cols
+                                        : a.logits_scratch + static_cast<int64_t>(r) * a.V + vbase;
+#pragma unroll
+    for (int i = 0; i < SEL_NPL; ++i) {
+      const int pos = i * 32 + lane;
+      k[i] = pos < n ? float_key(src[pos]) : 0u;
+    }
+  };  for (int r = warp; r < a.B; r += GEMV_CONSUMER_WARPS) {
+    uint32_t k[SEL_NPL];
+    load_row_keys(r, k);
+    uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+#pragma unroll
+    for (int i = 0; i < SEL_NPL; i += 4) {
+      m0 = max(m0, k[i]);
+      m1 = max(m1, k[i + 1]);
+      m2 = max(m2, k[i + 2]);
+      m3 = max(m3, k[i + 3]);
+    }
+    uint32_t lm = max(max(m0, m1), max(m2, m3));
+    uint32_t lead[SLAB_BOUND_KEYS];
+    uint32_t b = 0u;
+#pragma unroll
+    for (int j = 0; j < SLAB_LEADERS; ++j) {
+      const uint32_t best = __reduce_max_sync(0xffffffffu, lm);
+      const uint32_t who = __ballot_sync(0xffffffffu, lm == best);
+      if (j < SLAB_BOUND_KEYS) lead[j] = best;
+      b = best;
+      if (lane == __ffs(who) - 1) lm = 0u;  // each lane maximum counts once
+    }
+    uint32_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < SEL_NPL; ++i) mine += (i * 32 + lane < n && k[i] >= b) ? 1u : 0u;
+    const uint32_t tot = __reduce_add_sync(0xffffffffu, mine);
+    const bool fits = tot <= static_cast<uint32_t>(SLAB_CAND);
+    if (fits) {
+      uint32_t incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      uint64_t* dst = a.cand + (static_cast<int64_t>(r) * a.nslab + c) * SLAB_CAND;
+      uint32_t o = incl - mine;
+#pragma unroll
+      for (int i = 0; i < SEL_NPL; ++i) {
+        const int pos = i * 32 + lane;
+        if (pos < n && k[i] >= b) dst[o++] = composite(k[i], static_cast<int32_t>(vbase + pos));
       }
     }
-    __threadfence();
-    *s_flag = ok;
+    if (lane == 0) {
+      uint4* mp = reinterpret_cast<uint4*>(a.meta + (static_cast<int64_t>(r) * a.nslab + c) * SLAB_META_WORDS);
+      mp[0] = make_uint4(lead[0], lead[1], lead[2], lead[3]);
+      mp[1] = make_uint4(fits ? tot : 0u, fits ? b : 0xFFFFFFFFu, 0u, 0u);
+    }
+    // the warp barrier orders every lane's stores (and, through the CTA barriers above, the CTA's
+    // global logits copy) before lane 0's release
+    __syncwarp();
+    if (lane == 0)
+      asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(a.row_sync + r), "l"(1ull) : "memory");
+  }
+}
+
+// sorted[0, want) = the largest `want` of the m distinct composites comp[0, m),
+// in descending order, with every thread of the CTA.  comp must have room for
+// m rounded up to a multiple of 32.  Each warp sorts runs of 32 in registers
+// (bitonic network over the lanes); an element's position is then its place
+// in its own run plus, for every other run, the number of its elements above
+// it (a binary search of that sorted run).
+__device__ __forceinline__ void sort_runs(uint64_t* comp, uint64_t* sorted, int m, int want) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int R = (m + 31) >> 5;
+  for (int r = warp; r < R; r += nw) {
+    const int i = r * 32 + lane;
+    uint64_t v = i < m ? comp[i] : 0ull;  // 0 is below every composite
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+        // blocks with (lane & k) == 0 run descending; the lower lane of a pair keeps the larger
+        const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+        v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+      }
+    }
+    comp[i] = v;
   }
   __syncthreads();
-  return *s_flag != 0;
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    const uint64_t v = comp[i];
+    const int own = i >> 5;
+    int pos = i & 31;
+#pragma unroll 4
+    for (int q = 0; q < R; ++q) {
+      const uint64_t* run = comp + q * 32;
+      int above = 0;  // elements of run q greater than v (the run is descending)
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1)
+        if (run[above + step - 1] > v) above += step;
+      if (run[above] > v) ++above;
+      pos += q == own ? 0 : above;
+    }
+    if (pos < want) sorted[pos] = v;
+  }
+  __syncthreads();
+}
+
+// sorted[0, min(K, m)) = the top of keys/idx[0, m) in (value desc, index asc)
+// order, with every thread of the CTA; returns min(K, m).
+__device__ __forceinline__ int rank_top(const GemvArgs& a, const uint32_t* keys, const int32_t* idx, uint64_t* comp,
+                                        uint64_t* sorted, int m, uint32_t* s_red, uint32_t* s_list, uint32_t* s_misc) {
+  const int want = min(a.K, m);
+  if (m <= RANK_SORT_MAX) {
+    for (int j = threadIdx.x; j < m; j += blockDim.x) comp[j] = composite(keys[j], idx[j]);
+    __syncthreads();
+    sort_runs(comp, sorted, m, want);
+  } else {
+    block_top_composites(keys, idx, m, want, comp, s_red, s_list, s_misc);
+    sort_runs(comp, sorted, want, want);
+  }
+  return want;
+}
+
+// Appends to keys/idx[m, ...) the elements of row `row` in each listed slab
+// s_bad[0, nbad) whose key is in [thr, b_s) -- the ones the slab did not
+// publish that may reach the top K -- read from the global logits copy.  The
+// buffer is folded to its top K whenever a slab might not fit.  Returns the
+// new count.
+__device__ __forceinline__ int rescan_slabs(const GemvArgs& a, int row, uint32_t thr, int nbad, const uint32_t* s_bad,
+                                         const uint32_t* s_b, uint32_t* keys, int32_t* idx, uint64_t* comp, int m,
+                                         uint32_t* s_red, uint32_t* s_list, uint32_t* s_misc, uint32_t* s_own) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const float* lsrc = a.logits_out ? a.logits_out + static_cast<int64_t>(row) * a.logits_out_ld
+                                   : a.logits_scratch + static_cast<int64_t>(row) * a.V;
+  for (int bi = 0; bi < nbad; ++bi) {
+    const int s = static_cast<int>(s_bad[bi]);
+    const int64_t c0 = slab_pair_lo(a.npairs, a.nslab, s) * 16;
+    const int w = static_cast<int>(slab_pair_lo(a.npairs, a.nslab, s + 1) * 16 - c0);
+    if (m + w > a.capc) {  // keep the top K so far
+      for (int j = tid; j < a.sortP; j += nt) comp[j] = 0ull;
+      __syncthreads();
+      block_top_composites(keys, idx, m, a.K, comp, s_red, s_list, s_misc);
+      for (int j = tid; j < a.K; j += nt) {
+        keys[j] = composite_key(comp[j]);
+        idx[j] = composite_idx(comp[j]);
+      }
+      if (tid == 0) s_own[1] = static_cast<uint32_t>(a.K);
+      __syncthreads();
+      m = a.K;
+    }
+    const uint32_t bs = s_b[s];
+    for (int j = tid; j < w; j += nt) {
+      const uint32_t kv = float_key(__ldcg(lsrc + c0 + j));
+      if (kv >= thr && kv < bs) {
+        const uint32_t p = atomicAdd(&s_own[1], 1u);
+        keys[p] = kv;
+        idx[p] = static_cast<int32_t>(c0 + j);
+      }
+    }
+    __syncthreads();
+    m = static_cast<int>(s_own[1]);
+  }
+  return m;
+}
+
+// ================================================================ phase O: the row owner
+// CTA c owns rows c, c + nslab, ...  Once every slab has published row r:
+//   x = a lower bound of the K-th largest published leader key: at least K
+//       distinct elements are >= x, so every top-K element is >= x;
+//   F = the published candidates >= x, ranked by (value desc, index asc);
+//   v = the K-th of them (x when F holds fewer than K).  A slab whose b is
+//       above v may hold unpublished elements in [v, b): its logits row is
+//       rescanned for them.  Any other unpublished element is below its
+//       slab's b <= v, so the top K of F and the rescans is the exact top K.
+__device__ __forceinline__ void own_rows(const GemvArgs& a, uint8_t* ring, int c, uint32_t* s_red, uint32_t* s_list,
+                                     uint32_t* s_misc, uint32_t* s_own) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nt = blockDim.x;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(ring);
+  int32_t* idx = reinterpret_cast<int32_t*>(keys + a.capc);
+  uint64_t* comp = reinterpret_cast<uint64_t*>(idx + a.capc);
+  uint64_t* sorted = comp + a.sortP;
+  float* ebuf = reinterpret_cast<float*>(sorted + a.K);
+  uint32_t* s_cnt = reinterpret_cast<uint32_t*>(ebuf + a.K);  // slab counts, then the rescan list
+  uint32_t* s_b = s_cnt + a.nslab;
+  const int nflat = a.nslab * SLAB_CAND;
+  for (int row = c; row < a.B; row += a.nslab) {
+    SampleParams prm = {};
+    if (a.params != nullptr) prm = load_sample_params(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols);
+    // wait (bounded) until every slab has published this row
+    if (tid == 0) {
+      unsigned long long v = 0;
+      int ok = 1;
+      const uint64_t t0 = global_timer_ns();
+      while (true) {
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.row_sync + row) : "memory");
+        if (v >= static_cast<unsigned long long>(a.nslab)) break;
+        if (global_timer_ns() - t0 > a.timeout_ns) {
+          raise_error(a.err, DEV_TIMEOUT_BARRIER);
+          ok = 0;
+          break;
+        }
+      }
+      if (ok) a.row_sync[row] = 0ull;  // every slab has arrived: ready for the next run
+      s_own[2] = ok ? 0u : 1u;
+      s_own[1] = 0u;  // F's size
+      s_own[3] = 0u;  // slabs to rescan
+    }
+    __syncthreads();
+    if (s_own[2] != 0u) break;  // uniform: a slab never published (the error flag is raised)
+    const uint32_t* meta = a.meta + static_cast<int64_t>(row) * a.nslab * SLAB_META_WORDS;
+    const uint64_t* cand = a.cand + static_cast<int64_t>(row) * nflat;
+    uint64_t cr[NGATHER];
+    const int tg = tid - 32, ntg = nt - 32;
+    if (warp == 0) {
+      // the leaders, for the bound; every slab's count and b
+      uint32_t pk[NLEAD_L];
+#pragma unroll
+      for (int j = 0; j < NLEAD_L / SLAB_BOUND_KEYS; ++j) {
+        const int s = j * 32 + lane;
+        uint4 l = make_uint4(0u, 0u, 0u, 0u);
+        if (s < a.nslab) {
+          l = __ldcg(reinterpret_cast<const uint4*>(meta + s * SLAB_META_WORDS));
+          const uint2 cb = __ldcg(reinterpret_cast<const uint2*>(meta + s * SLAB_META_WORDS + 4));
+          s_cnt[s] = cb.x;
+          s_b[s] = cb.y;
+        }
+        pk[4 * j] = l.x;
+        pk[4 * j + 1] = l.y;
+        pk[4 * j + 2] = l.z;
+        pk[4 * j + 3] = l.w;
+      }
+      const uint32_t x = a.nslab * SLAB_BOUND_KEYS >= a.K ? warp_bound16_span_regs(pk, a.K) : 0u;
+      if (lane == 0) s_own[0] = x;
+    } else {
+      // the candidate slots, loaded blind; the empty ones are dropped below
+#pragma unroll
+      for (int q = 0; q < NGATHER; ++q) {
+        const int f = q * ntg + tg;
+        cr[q] = f < nflat ? __ldcg(cand + f) : 0ull;
+      }
+    }
+    __syncthreads();
+    const uint32_t x = s_own[0];
+    if (warp != 0) {
+      // a warp's 32 slots of one step are one slab's (SLAB_CAND == 32, ntg a multiple of 32); the
+      // warp counts its kept slots by ballots, reserves room once, then writes them
+      uint32_t bm[NGATHER];
+      uint32_t cnt = 0u;
+#pragma unroll
+      for (int q = 0; q < NGATHER; ++q) {
+        const int f = q * ntg + tg;
+        const bool take = f < nflat && static_cast<uint32_t>(lane) < s_cnt[min(f, nflat - 1) / SLAB_CAND] &&
+                          composite_key(cr[q]) >= x;
+        bm[q] = __ballot_sync(0xffffffffu, take);
+        cnt += static_cast<uint32_t>(__popc(bm[q]));
+      }
+      uint32_t base = 0u;
+      if (lane == 0 && cnt != 0u) base = atomicAdd(&s_own[1], cnt);
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const uint32_t below = lanemask_lt();
+#pragma unroll
+      for (int q = 0; q < NGATHER; ++q) {
+        if (bm[q] & (1u << lane)) {
+          const uint32_t p = base + static_cast<uint32_t>(__popc(bm[q] & below));
+          keys[p] = composite_key(cr[q]);
+          idx[p] = composite_idx(cr[q]);
+        }
+        base += static_cast<uint32_t>(__popc(bm[q]));
+      }
+    }
+    __syncthreads();
+    int m = static_cast<int>(s_own[1]);
+    int want = rank_top(a, keys, idx, comp, sorted, m, s_red, s_list, s_misc);
+    // slabs whose unpublished elements may reach the top K
+    const uint32_t thr = want >= a.K ? composite_key(sorted[a.K - 1]) : x;
+    for (int s = tid; s < a.nslab; s += nt)
+      if (s_b[s] > thr) s_cnt[atomicAdd(&s_own[3], 1u)] = static_cast<uint32_t>(s);
+    __syncthreads();
+    const int nbad = static_cast<int>(s_own[3]);
+    if (nbad > 0) {
+      m = rescan_slabs(a, row, thr, nbad, s_cnt, s_b, keys, idx, comp, m, s_red, s_list, s_misc, s_own);
+      want = rank_top(a, keys, idx, comp, sorted, m, s_red, s_list, s_misc);
+    }
+    for (int j = tid; j < want; j += nt) {
+      a.topk_val[static_cast<int64_t>(row) * a.topk_ld + j] = key_float(composite_key(sorted[j]));
+      a.topk_idx[static_cast<int64_t>(row) * a.topk_ld + j] = composite_idx(sorted[j]);
+    }
+    if (a.params != nullptr && a.tokens != nullptr) {  // every thread takes part in the draw
+      const int32_t tok = sample_sorted_row(prm, sorted, want, ebuf, reinterpret_cast<float*>(s_red));
+      if (tid == 0) a.tokens[row] = tok;
+    }
+    __syncthreads();
+  }
 }
 
 template <int MT, int PW>
-__global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_red[64];
   __shared__ uint32_t s_list[SEL_BLOCK_BUCKET_MAX];
   __shared__ uint32_t s_misc[4];
-  __shared__ int s_rows[1];
-  __shared__ int s_flag;
+  __shared__ uint32_t s_own[4];  // owner: x, |F|, wait failed, slabs to rescan
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + MAX_STAGES);
@@ -209,11 +491,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
             v.x = (acc[m][q][n][0] + acc[m][q][n][2]) * sc;
             v.y = (acc[m][q][n][1] + acc[m][q][n][3]) * sc;
             if (a.logits_out) *reinterpret_cast<float2*>(a.logits_out + r * a.logits_out_ld + col) = v;
-            if (a.logits_in_smem) {
+            if (a.logits_in_smem)
               *reinterpret_cast<float2*>(slab_logits + r * max_cols + (col - pair_lo * 16)) = v;
-            } else {
+            // a global copy for the row owner's rescans (and for the slab scan when it is not in smem)
+            if (!a.logits_out || !a.logits_in_smem)
               *reinterpret_cast<float2*>(a.logits_scratch + static_cast<int64_t>(r) * a.V + col) = v;
-            }
           }
         }
       }
@@ -303,215 +585,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const Gemv
   const bool aborted = *s_abort != 0;
   const int n = slab_pairs * 16;
   const int64_t vbase = pair_lo * 16;
-  uint32_t* wlist = reinterpret_cast<uint32_t*>(
-                        ring + (a.logits_in_smem ? ((static_cast<size_t>(a.B) * max_cols * 4 + 127) & ~size_t(127)) : 0)) +
-                    warp * SEL_BUCKET_MAX;
-  auto load_row_keys = [&](int r, uint32_t (&k)[SEL_NPL]) {
-    const float* src = a.logits_in_smem ? slab_logits + r * max_cols
-                                        : a.logits_scratch + static_cast<int64_t>(r) * a.V + vbase;
-#pragma unroll
-    for (int i = 0; i < SEL_NPL; ++i) {
-      const int pos = i * 32 + lane;
-      k[i] = pos < n ? float_key(src[pos]) : 0u;
-    }
-  };
 
-  // ================================================================ phase A: publish lane maxima
-  if (!aborted && warp < GEMV_CONSUMER_WARPS) {
-    for (int r = warp; r < a.B; r += GEMV_CONSUMER_WARPS) {
-      uint32_t k[SEL_NPL];
-      load_row_keys(r, k);
-      uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
-#pragma unroll
-      for (int i = 0; i < SEL_NPL; i += 4) {
-        m0 = max(m0, k[i]);
-        m1 = max(m1, k[i + 1]);
-        m2 = max(m2, k[i + 2]);
-        m3 = max(m3, k[i + 3]);
-      }
-      uint32_t lm = max(max(m0, m1), max(m2, m3));
-      uint32_t* dst = a.pub + (static_cast<int64_t>(r) * a.nslab + c) * PUB;
-#pragma unroll
-      for (int j = 0; j < PUB; ++j) {
-        const uint32_t best = __reduce_max_sync(0xffffffffu, lm);
-        const uint32_t who = __ballot_sync(0xffffffffu, lm == best);
-        if (lane == 0) dst[j] = best;
-        if (lane == __ffs(who) - 1) lm = 0u;  // each lane maximum is published once
-      }
-    }
-  }
-  const bool ok1 = grid_barrier(a.bar, a.timeout_ns, a.err, &s_flag);
 
-  // ================================================================ phase B: emit the slab's elements >= x
-  if (!aborted && ok1 && warp < GEMV_CONSUMER_WARPS) {
-    const int npub = a.nslab * PUB;
-    for (int r = warp; r < a.B; r += GEMV_CONSUMER_WARPS) {
-      uint32_t x = 0u;  // below every key: no bound when too few keys are published
-      if (npub >= a.K) {
-        uint32_t pk[NPUB_L];
-        const uint32_t* srcp = a.pub + static_cast<int64_t>(r) * npub;
-#pragma unroll
-        for (int i = 0; i < NPUB_L; ++i) {
-          const int pos = i * 32 + lane;
-          pk[i] = pos < npub ? __ldcg(srcp + pos) : 0u;
-        }
-        x = warp_bound16_span_regs(pk, a.K);
-      }
-      uint32_t k[SEL_NPL];
-      load_row_keys(r, k);
-      uint32_t mine = 0;
-#pragma unroll
-      for (int i = 0; i < SEL_NPL; ++i) mine += (i * 32 + lane < n && k[i] >= x) ? 1u : 0u;
-      const uint32_t tot = __reduce_add_sync(0xffffffffu, mine);
-      // reserve room in the row's packed candidate array, emit, then count this slab as arrived
-      const uint32_t take = tot <= static_cast<uint32_t>(a.K) ? tot : static_cast<uint32_t>(a.K);
-      uint32_t off = 0;
-      if (lane == 0) off = static_cast<uint32_t>(atomicAdd(a.row_sync + r, static_cast<unsigned long long>(take)));
-      off = __shfl_sync(0xffffffffu, off, 0);
-      const int64_t obase = static_cast<int64_t>(r) * a.nslab * a.K + off;
-      if (tot <= static_cast<uint32_t>(a.K)) {
-        uint32_t incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += t;
-        }
-        uint32_t o = incl - mine;
-#pragma unroll
-        for (int i = 0; i < SEL_NPL; ++i) {
-          const int pos = i * 32 + lane;
-          if (pos < n && k[i] >= x) {
-            a.cand_key[obase + o] = k[i];
-            a.cand_idx[obase + o] = static_cast<int32_t>(vbase + pos);
-            ++o;
-          }
-        }
-      } else {
-        // more than K pass: the slab's exact top-K (ties by index) covers its share of the global top-K
-        const Threshold th = warp_select_regs(k, a.K, wlist);
-        warp_compact_regs(k, n, th, [&](int pos, int i, uint32_t kv) {
-          a.cand_key[obase + pos] = kv;
-          a.cand_idx[obase + pos] = static_cast<int32_t>(vbase + i);
-        });
-      }
-      // the warp barrier orders every lane's candidate stores before lane 0's release of the arrival
-      __syncwarp();
-      if (lane == 0)
-        asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(a.row_sync + r), "l"(1ull << 32) : "memory");
-    }
-  }
-
-  // ================================================================ phase C: final top-K, sort, sampler
-  if (!aborted && ok1) {
-    const int nt = blockDim.x, nw = nt >> 5;
-    uint32_t* keys = reinterpret_cast<uint32_t*>(ring);
-    int32_t* idx = reinterpret_cast<int32_t*>(keys + a.capc);
-    uint64_t* comp = reinterpret_cast<uint64_t*>(idx + a.capc);
-    uint64_t* sorted = comp + a.sortP;
-    float* ebuf = reinterpret_cast<float*>(sorted + a.K);
-    // keeps the top K of the m > K candidates, in place
-    auto fold = [&](int m) {
-      for (int j = tid; j < a.sortP; j += nt) comp[j] = 0ull;
-      __syncthreads();
-      block_top_composites(keys, idx, m, a.K, comp, s_red, s_list, s_misc);
-      for (int j = tid; j < a.K; j += nt) {
-        keys[j] = composite_key(comp[j]);
-        idx[j] = composite_idx(comp[j]);
-      }
-      __syncthreads();
-      return a.K;
-    };
-    for (int row = c; row < a.B; row += a.nslab) {
-      SampleParams prm = {};
-      if (a.params != nullptr) prm = load_sample_params(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols);
-      // wait (bounded) until every slab has emitted its candidates of this row
-      if (tid == 0) {
-        unsigned long long v = 0;
-        const uint64_t t0 = global_timer_ns();
-        while (true) {
-          asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.row_sync + row) : "memory");
-          if ((v >> 32) >= static_cast<unsigned long long>(a.nslab)) break;
-          if (global_timer_ns() - t0 > a.timeout_ns) {
-            raise_error(a.err, DEV_TIMEOUT_BARRIER);
-            v = ~0ull;
-            break;
-          }
-        }
-        s_rows[0] = v == ~0ull ? -1 : static_cast<int>(v & 0xFFFFFFFFull);
-      }
-      __syncthreads();
-      const int total_c = s_rows[0];
-      if (total_c < 0) break;  // uniform: a slab never arrived (the error flag is raised)
-      const int64_t cbase = static_cast<int64_t>(row) * a.nslab * a.K;
-      // gather the packed candidates; when they exceed the buffer, fold it to its top K between runs
-      int ncand = 0;
-      for (int base = 0; base < total_c;) {
-        const int take = min(total_c - base, a.capc - ncand);
-        for (int i0 = 0; i0 < take; i0 += GATHER_PT * nt) {  // loads first, then stores
-          uint32_t kr[GATHER_PT];
-          int32_t ir[GATHER_PT];
-#pragma unroll
-          for (int q = 0; q < GATHER_PT; ++q) {
-            const int i = i0 + q * nt + tid;
-            kr[q] = i < take ? __ldcg(a.cand_key + cbase + base + i) : 0u;
-            ir[q] = i < take ? __ldcg(a.cand_idx + cbase + base + i) : 0;
-          }
-#pragma unroll
-          for (int q = 0; q < GATHER_PT; ++q) {
-            const int i = i0 + q * nt + tid;
-            if (i < take) {
-              keys[ncand + i] = kr[q];
-              idx[ncand + i] = ir[q];
-            }
-          }
-        }
-        ncand += take;
-        base += take;
-        __syncthreads();
-        if (base < total_c) ncand = fold(ncand);
-      }
-      if (tid == 0) a.row_sync[row] = 0ull;  // ready for the next run
-      const int want = min(a.K, ncand);
-      // candidates to rank: all of them when few, else the top `want` found by a selection
-      int nr = ncand;
-      if (ncand <= RANK_SORT_MAX) {
-        for (int j = tid; j < ncand; j += nt) comp[j] = composite(keys[j], idx[j]);
-        __syncthreads();
-      } else {
-        block_top_composites(keys, idx, ncand, want, comp, s_red, s_list, s_misc);
-        nr = want;
-      }
-      // rank sort: the composites are distinct, so rank(i) = #{j : comp[j] > comp[i]} is the
-      // position of candidate i in (value desc, index asc) order
-      for (int i = tid; i < nr; i += nt) {
-        const uint64_t ci = comp[i];
-        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-        int j = 0;
-        const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(comp);  // comp is 16-byte aligned
-        for (; j + 4 <= nr; j += 4) {
-          const ulonglong2 p = c2[j >> 1], q = c2[(j >> 1) + 1];
-          r0 += p.x > ci;
-          r1 += p.y > ci;
-          r2 += q.x > ci;
-          r3 += q.y > ci;
-        }
-        for (; j < nr; ++j) r0 += comp[j] > ci;
-        const int rank = (r0 + r1) + (r2 + r3);
-        if (rank < want) sorted[rank] = ci;
-      }
-      __syncthreads();
-      for (int j = tid; j < want; j += nt) {
-        a.topk_val[static_cast<int64_t>(row) * a.topk_ld + j] = key_float(composite_key(sorted[j]));
-        a.topk_idx[static_cast<int64_t>(row) * a.topk_ld + j] = composite_idx(sorted[j]);
-      }
-      if (a.params != nullptr && a.tokens != nullptr) {  // every thread takes part in the draw
-        const int32_t tok = sample_sorted_row(prm, sorted, want, ebuf,
-                                              reinterpret_cast<float*>(s_red));
-        if (tid == 0) a.tokens[row] = tok;
-      }
-      __syncthreads();
-    }
-  }
+  if (!aborted && warp < GEMV_CONSUMER_WARPS) publish_rows(a, slab_logits, max_cols, n, vbase, c);
+  if (!aborted) own_rows(a, ring, c, s_red, s_list, s_misc, s_own);
   pdl_launch_dependents();
 }
 
@@ -563,23 +640,25 @@ GemvPlan plan_gemv(int B, int H, int V, int K, int nslab, int max_smem, int kpb,
   if (p.nstages > MAX_STAGES) p.nstages = MAX_STAGES;
   p.max_slab_cols = max_slab_pairs * 16;
   const int nblk = (max_slab_pairs + p.cb_pairs - 1) / p.cb_pairs;
-  const int list_bytes = GEMV_CONSUMER_WARPS * SEL_BUCKET_MAX * 4;
-  const int smem_logits = ((B * p.max_slab_cols * 4 + 127) & ~127) + list_bytes;
+  const int smem_logits = (B * p.max_slab_cols * 4 + 127) & ~127;
   const int ring = p.nstages * p.stage_bytes;
   p.logits_in_smem = (nblk == 1 && smem_logits <= budget) ? 1 : 0;
-  // phase C: candidate buffer (capc keys + ids), sort buffer, sampler scratch, slab counts and offsets
+  // owner phase: candidate buffer (capc keys + ids), sort buffer, sampler scratch, slab counts and bounds
   // composite buffer: the top-K selection writes up to K entries, the direct rank sort up to RANK_SORT_MAX
   p.sortP = next_pow2(K) > RANK_SORT_MAX ? next_pow2(K) : RANK_SORT_MAX;
   const int fixed_c = p.sortP * 8 + K * 8 + K * 4 + (2 * nslab + 8) * 4;
-  const int want_capc = nslab * K < PHASE_C_CAP ? ((nslab * K + 3) & ~3) : PHASE_C_CAP;
-  int epi = p.logits_in_smem ? smem_logits : list_bytes;
+  // every published slot of a row, or K kept candidates plus one slab's rescan
+  const int need_capc = nslab * SLAB_CAND > K + p.max_slab_cols ? nslab * SLAB_CAND : K + p.max_slab_cols;
+  const int want_capc = ((need_capc > 2 * K ? need_capc : 2 * K) + 3) & ~3;
+  int epi = p.logits_in_smem ? smem_logits : 0;
   const int phase_c = want_capc * 8 + fixed_c;
   if (phase_c > epi) epi = phase_c;
   p.smem_bytes = BAR_REGION + (ring > epi ? ring : epi);
   if (p.smem_bytes > max_smem) p.smem_bytes = max_smem;
   p.capc = ((p.smem_bytes - BAR_REGION - fixed_c) / 8) & ~3;
-  if (p.capc > PHASE_C_CAP) p.capc = PHASE_C_CAP;
-  p.ok = p.nstages >= 2 && p.capc >= 2 * K && BAR_REGION + ring <= max_smem &&
+  if (p.capc > want_capc) p.capc = want_capc;
+  p.ok = p.nstages >= 2 && p.capc >= 2 * K && p.capc >= need_capc && nslab <= MAX_SLABS &&
+         BAR_REGION + ring <= max_smem &&
          (!p.logits_in_smem || BAR_REGION + smem_logits <= max_smem);
   return p;
 }

@@ -8,9 +8,9 @@
 // module, zero-filled, and its address is looked up once per device (with that
 // device current) by the first call that runs there.  That first call also
 // opts the lm_head kernels into their shared-memory size.  Every later call
-// only computes a layout on the host, clears the barrier counter, the error
-// word and the per-row arrival words with one cudaMemsetAsync and launches kernels: no cudaMalloc, cudaFree
-// or other allocating routine on any call.
+// only computes a layout on the host, clears the error word and the per-row
+// arrival words with one cudaMemsetAsync and launches kernels: no cudaMalloc,
+// cudaFree or other allocating routine on any call.
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -26,7 +26,7 @@ using namespace tail;
 
 namespace {
 
-constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(4) << 20;  // 4 MiB per device
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(8) << 20;  // 8 MiB per device
 constexpr int NOALLOC_MAX_DEVICES = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
@@ -90,16 +90,17 @@ size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Byte offsets of one pass's scratch inside the static array.
 struct Layout {
-  size_t bar, err, rsync, apack, row_scale, pub, ckey, cidx, lscr, tkv, tki, total;
+  size_t err, rsync, apack, row_scale, meta, cand, lscr, tkv, tki, total;
 };
 
-// Scratch of a pass of B rows under `plan`; the first 256 bytes hold the
-// grid-barrier counter (offset 0) and the error word (offset 8), the per-row
-// arrival words follow; everything before `apack` starts each call at zero.
-Layout layout_for(const GemvPlan& plan, int B, int H, int V, int K, int nslab) {
+// Scratch of a pass of B rows under `plan`; the first 256 bytes hold the error
+// word (offset 8), the per-row arrival words follow; everything before `apack`
+// starts each call at zero.  The logits staging is left out when the caller's
+// logits serve the row owners' rescans (has_out) and the slab logits stay in
+// shared memory.
+Layout layout_for(const GemvPlan& plan, int B, int H, int V, int K, int nslab, bool has_out) {
   Layout L = {};
   size_t o = 0;
-  L.bar = 0;
   L.err = 8;
   o = 256;
   L.rsync = o;
@@ -108,14 +109,12 @@ Layout layout_for(const GemvPlan& plan, int B, int H, int V, int K, int nslab) {
   o += up256(static_cast<size_t>(H / KSTEP) * plan.mt * APACK_TILE_BYTES);
   L.row_scale = o;
   o += up256(static_cast<size_t>(plan.mt) * MTILE_ROWS * 4);
-  L.pub = o;
-  o += up256(static_cast<size_t>(B) * nslab * TAIL_PUB_PER_SLAB * 4);
-  L.ckey = o;
-  o += up256(static_cast<size_t>(B) * nslab * K * 4);
-  L.cidx = o;
-  o += up256(static_cast<size_t>(B) * nslab * K * 4);
+  L.meta = o;
+  o += up256(static_cast<size_t>(B) * nslab * SLAB_META_WORDS * 4);
+  L.cand = o;
+  o += up256(static_cast<size_t>(B) * nslab * SLAB_CAND * 8);
   L.lscr = o;
-  if (!plan.logits_in_smem) o += up256(static_cast<size_t>(B) * V * 4);
+  if (!has_out || !plan.logits_in_smem) o += up256(static_cast<size_t>(B) * V * 4);
   L.tkv = o;
   o += up256(static_cast<size_t>(B) * K * 4);
   L.tki = o;
@@ -162,12 +161,13 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
   }
 
   // Rows per pass: the most (up to 64) whose plan is valid and whose scratch fits the static array.
+  const bool has_out = out_logits_opt != nullptr;
   const int rmax = gbs < MAX_ROWS_PER_PASS ? gbs : MAX_ROWS_PER_PASS;
   int R = 0;
   size_t need1 = 0;
   for (int r = rmax; r >= 1; --r) {
     const GemvPlan p = plan_gemv(r, H, V, K, nslab, d->max_dyn);
-    const size_t need = layout_for(p, r, H, V, K, nslab).total;
+    const size_t need = layout_for(p, r, H, V, K, nslab, has_out).total;
     if (r == 1) need1 = need;
     if (p.ok && need <= NOALLOC_SCRATCH_BYTES) {
       R = r;
@@ -186,7 +186,7 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
   const int rem = gbs % R;
   if (rem) {
     const GemvPlan p = plan_gemv(rem, H, V, K, nslab, d->max_dyn);
-    if (!p.ok || layout_for(p, rem, H, V, K, nslab).total > NOALLOC_SCRATCH_BYTES) {
+    if (!p.ok || layout_for(p, rem, H, V, K, nslab, has_out).total > NOALLOC_SCRATCH_BYTES) {
       set_last_error("tail_run_noalloc: the last pass of the batch has no plan that fits the static scratch");
       return TAIL_ERR_UNSUPPORTED;
     }
@@ -194,11 +194,9 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* base = d->base;
-  // The grid barrier counter, the error word and the per-row arrival words must
-  // start at zero: the counter's generations are multiples of the grid size,
-  // which differs between configs sharing this array, and a call interrupted by
-  // a device error may leave the others nonzero.
-  const size_t zero_bytes = layout_for(plan_gemv(R, H, V, K, nslab, d->max_dyn), R, H, V, K, nslab).apack;
+  // The error word and the per-row arrival words must start at zero: a call
+  // interrupted by a device error may leave them nonzero.
+  const size_t zero_bytes = layout_for(plan_gemv(R, H, V, K, nslab, d->max_dyn), R, H, V, K, nslab, has_out).apack;
   e = cudaMemsetAsync(base, 0, zero_bytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "tail_run_noalloc: cudaMemsetAsync");
 
@@ -206,7 +204,7 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
   for (int r0 = 0; r0 < gbs; r0 += R) {
     const int B = gbs - r0 < R ? gbs - r0 : R;
     const GemvPlan plan = plan_gemv(B, H, V, K, nslab, d->max_dyn);
-    const Layout L = layout_for(plan, B, H, V, K, nslab);
+    const Layout L = layout_for(plan, B, H, V, K, nslab, has_out);
 
     RmsArgs ra;
     ra.hidden = static_cast<const uint8_t*>(hidden) + static_cast<int64_t>(r0) * H * sz;
@@ -231,12 +229,10 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
     ga.row_scale = reinterpret_cast<const float*>(base + L.row_scale);
     ga.logits_out = out_logits_opt ? out_logits_opt + static_cast<int64_t>(r0) * V : nullptr;
     ga.logits_out_ld = V;
-    ga.logits_scratch = plan.logits_in_smem ? nullptr : reinterpret_cast<float*>(base + L.lscr);
-    ga.pub = reinterpret_cast<uint32_t*>(base + L.pub);
-    ga.cand_key = reinterpret_cast<uint32_t*>(base + L.ckey);
-    ga.cand_idx = reinterpret_cast<int32_t*>(base + L.cidx);
+    ga.logits_scratch = (has_out && plan.logits_in_smem) ? nullptr : reinterpret_cast<float*>(base + L.lscr);
+    ga.meta = reinterpret_cast<uint32_t*>(base + L.meta);
+    ga.cand = reinterpret_cast<uint64_t*>(base + L.cand);
     ga.row_sync = reinterpret_cast<unsigned long long*>(base + L.rsync);
-    ga.bar = reinterpret_cast<unsigned long long*>(base + L.bar);
     ga.topk_val = reinterpret_cast<float*>(base + L.tkv);
     ga.topk_idx = reinterpret_cast<int32_t*>(base + L.tki);
     ga.topk_ld = K;

@@ -34,12 +34,10 @@ struct tail_s {
   // device scratch
   uint32_t* apack;
   float* row_scale;
-  uint32_t* cand_key;
-  int32_t* cand_idx;
+  uint64_t* cand;
   float* logit_scratch;
-  uint32_t* pub;
+  uint32_t* meta;
   unsigned long long* row_sync;
-  unsigned long long* bar;
   float* topk_val;
   int32_t* topk_idx;
   int* err;
@@ -124,8 +122,8 @@ cudaError_t dalloc(T** p, size_t n, int64_t* total) {
 }
 
 void free_all(tail_t* h) {
-  void* ptrs[] = {h->apack,    h->row_scale, h->cand_key,  h->cand_idx,  h->logit_scratch, h->pub,
-                  h->row_sync, h->bar,       h->topk_val,  h->topk_idx,  h->err,           h->st_hidden,
+  void* ptrs[] = {h->apack,    h->row_scale, h->cand,      h->logit_scratch, h->meta,
+                  h->row_sync, h->topk_val,  h->topk_idx,  h->err,           h->st_hidden,
                   h->st_params, h->st_tokens, h->st_logits, h->tc_act,   h->tc_rs,         h->tc_lists,
                   h->tc_logits};
   for (void* p : ptrs)
@@ -269,12 +267,10 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   cudaError_t e = cudaSuccess;
   e = e ? e : dalloc(&h->apack, ksteps * mt_max * APACK_TILE_BYTES / 4, &tot);
   e = e ? e : dalloc(&h->row_scale, static_cast<size_t>(mt_max) * 8, &tot);
-  e = e ? e : dalloc(&h->cand_key, static_cast<size_t>(R) * h->nslab * K, &tot);
-  e = e ? e : dalloc(&h->cand_idx, static_cast<size_t>(R) * h->nslab * K, &tot);
+  e = e ? e : dalloc(&h->cand, static_cast<size_t>(R) * h->nslab * SLAB_CAND, &tot);
   e = e ? e : dalloc(&h->logit_scratch, static_cast<size_t>(R) * cfg->V, &tot);
-  e = e ? e : dalloc(&h->pub, static_cast<size_t>(R) * h->nslab * TAIL_PUB_PER_SLAB, &tot);
+  e = e ? e : dalloc(&h->meta, static_cast<size_t>(R) * h->nslab * SLAB_META_WORDS, &tot);
   e = e ? e : dalloc(&h->row_sync, static_cast<size_t>(R), &tot);
-  e = e ? e : dalloc(&h->bar, 1, &tot);
   e = e ? e : dalloc(&h->topk_val, static_cast<size_t>(cfg->gbs_max) * K, &tot);
   e = e ? e : dalloc(&h->topk_idx, static_cast<size_t>(cfg->gbs_max) * K, &tot);
   e = e ? e : dalloc(&h->err, 1, &tot);
@@ -293,7 +289,6 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
       e = cudaMemset(h->tc_act, 0, static_cast<size_t>(tc_act_rows(cfg->gbs_max)) * cfg->H * sizeof(uint16_t));
   }
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
-  if (e == cudaSuccess) e = cudaMemset(h->bar, 0, sizeof(unsigned long long));
   if (e == cudaSuccess && R > 0) e = cudaMemset(h->row_sync, 0, static_cast<size_t>(R) * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(h->apack, 0, ksteps * mt_max * APACK_TILE_BYTES);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -438,8 +433,7 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     ga.logits_out = out_logits ? out_logits + static_cast<int64_t>(r0) * c.V : nullptr;
     ga.logits_out_ld = c.V;
     ga.logits_scratch = h->logit_scratch;
-    ga.cand_key = h->cand_key;
-    ga.cand_idx = h->cand_idx;
+    ga.cand = h->cand;
     ga.err = h->err;
     ga.B = B;
     ga.H = c.H;
@@ -457,9 +451,8 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     ga.logits_in_smem = plan.logits_in_smem;
     ga.max_slab_cols = plan.max_slab_cols;
     ga.smem_bytes = plan.smem_bytes;
-    ga.pub = h->pub;
+    ga.meta = h->meta;
     ga.row_sync = h->row_sync;
-    ga.bar = h->bar;
     ga.topk_val = (out_topk_vals ? out_topk_vals : h->topk_val) + static_cast<int64_t>(r0) * K;
     ga.topk_idx = (out_topk_idx ? out_topk_idx : h->topk_idx) + static_cast<int64_t>(r0) * K;
     ga.topk_ld = K;
@@ -581,10 +574,8 @@ int tail_check(tail_t* h) {
   int flag = 0;
   if (cudaMemcpy(&flag, h->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TAIL_ERR_CUDA;
   if (flag != 0) {
-    // a wait that ran out may leave the grid barrier counter off its generation boundary
     cudaMemset(h->err, 0, sizeof(int));
-    cudaMemset(h->bar, 0, sizeof(unsigned long long));
-    // so may the per-row arrival words of an interrupted run
+    // a wait that ran out leaves the per-row arrival words of the interrupted run behind
     if (h->rows_pass > 0) cudaMemset(h->row_sync, 0, static_cast<size_t>(h->rows_pass) * sizeof(unsigned long long));
     cudaDeviceSynchronize();
     return TAIL_ERR_DEVICE;

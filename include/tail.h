@@ -163,7 +163,7 @@ int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const 
  * It runs the same kernels and gives the same results as tail_run with the
  * same config (bitwise equal when gbs <= 8 at GPT-OSS sizes; larger batches
  * run as several passes and agree within the logit tolerance).  Instead of
- * handle scratch it uses one static device array of 4 MiB per device, part of
+ * handle scratch it uses one static device array of 8 MiB per device, part of
  * this library's device image; no call allocates, frees or calls a routine
  * that allocates.
  *   cfg            the config tail_create would take (validated on every call);
@@ -175,19 +175,20 @@ int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const 
  *                  bounded device wait that ran out, in which case the
  *                  outputs are undefined.
  * Size limit: one pass of B rows needs, each part rounded up to 256 bytes,
- * 256 (barrier counter and error word) + 8 * B (per-row arrival words)
+ * 256 (error word) + 8 * B (per-row arrival words)
  * + 32 * H * mt (activation pack; mt = 1,
  * 2, 4 or 8 for B up to 8, 16, 32, 64) + 32 * mt (row scales)
- * + 16 * B * nslab (published maxima) + 8 * B * nslab * k (per-slab
- * candidates) + 8 * B * k (top-k staging) + 4 * B * V (logits staging, only
- * when a slab's logits do not fit in shared memory) bytes, nslab being the
- * vocabulary slab count (min(SMs, V / 128), at least 1).  Batches run in
- * passes of as many rows (at most 64) as fit in 4 MiB.  At H = 2880, V = 201088, k = 256
- * that is 8 rows per pass.  When not even one row fits, the call returns
+ * + 32 * B * nslab (per-slab publications) + 256 * B * nslab (published
+ * candidates) + 8 * B * k (top-k staging) + 4 * B * V (logits staging,
+ * left out when out_logits_opt is given and a slab's logits fit in shared
+ * memory) bytes, nslab being the vocabulary slab count (min(SMs, V / 128),
+ * at least 1).  Batches run in passes of as many rows (at most 64) as fit in
+ * 8 MiB.  At H = 2880, V = 201088, k = 256 that is 9 rows per pass.  When
+ * not even one row fits, the call returns
  * TAIL_ERR_UNSUPPORTED before launching anything, and tail_last_error()
- * states the bytes needed and the 4 MiB limit.
- * Zeroing: every call clears the grid-barrier counter, the error word and the
- * per-row arrival words with one cudaMemsetAsync on `stream`; the rest of the
+ * states the bytes needed and the 8 MiB limit.
+ * Zeroing: every call clears the error word and the per-row arrival words
+ * with one cudaMemsetAsync on `stream`; the rest of the
  * scratch is fully written by the kernels before it is read.
  * First call on a device: sets up that device (looks up the static array's
  * address with cudaGetSymbolAddress, which loads the library's device image
