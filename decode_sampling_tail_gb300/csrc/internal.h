@@ -11,7 +11,13 @@ constexpr int MTILE_ROWS = 8;        // batch rows per m-tile (hi and lo parts s
 constexpr int APACK_TILE_BYTES = 512;  // one 16x16 bf16 A fragment set: 32 lanes x 16 bytes
 constexpr int MAX_ROWS_PER_PASS = 64;  // rows one lm_head pass covers (mt <= 8)
 constexpr int GEMV_CONSUMER_WARPS = 8;
-constexpr int GEMV_THREADS = (GEMV_CONSUMER_WARPS + 1) * 32;
+constexpr int GEMV_PRODUCER_WARP = GEMV_CONSUMER_WARPS;      // weight (and packed activation) copies
+constexpr int GEMV_PACK_WARP = GEMV_CONSUMER_WARPS + 1;      // activations built in-kernel (fused RMSNorm)
+constexpr int GEMV_THREADS = (GEMV_CONSUMER_WARPS + 2) * 32;
+constexpr int FUSED_MAX_MT = 2;      // the lm_head kernel forms the activations itself for up to 16 rows
+constexpr int HID_DEPTH = 4;         // fused: stages of hidden columns in flight (async copies)
+constexpr int HID_ROW_BYTES = 128;   // one row's 32 k columns, fp32 at most
+constexpr int HID_SLOT_BYTES = FUSED_MAX_MT * 8 * HID_ROW_BYTES;
 constexpr int GEMV_KPB = 2;          // ring stage = 32 rows of W
 constexpr int GEMV_MAX_STAGES = 8;
 constexpr int MAX_K = 1024;
@@ -48,8 +54,16 @@ struct RmsArgs {
 
 struct GemvArgs {
   const uint16_t* w;        // [H, V] bf16
-  const uint8_t* apack;     // [ksteps][mt][512 B]
-  const float* row_scale;   // [B_pad]
+  const uint8_t* apack;     // [ksteps][mt][512 B] (not fused)
+  const float* row_scale;   // [B_pad] (not fused)
+  // fused: the kernel forms the activations x * gamma (deferred RMSNorm) and rstd itself
+  int fused;
+  const void* hidden;       // [B, H] of hidden_dtype
+  int dtype;
+  const float* gamma;       // [H]
+  int Hu;
+  float eps;
+  int zero_pad;
   float* logits_out;        // [B, V] caller logits for this pass, or null
   int64_t logits_out_ld;    // row stride of logits_out in floats
   float* logits_scratch;    // [B, V] the logits when the caller takes none (the row owner rescans it)

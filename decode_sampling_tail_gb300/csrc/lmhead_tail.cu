@@ -54,7 +54,23 @@ constexpr int NLEAD_L = SLAB_BOUND_KEYS * ((MAX_SLABS + 31) / 32);  // leader ke
 constexpr int NGATHER = (MAX_SLABS * SLAB_CAND + GEMV_THREADS - 33) / (GEMV_THREADS - 32);  // slots per gatherer
 static_assert(SLAB_BOUND_KEYS == 4 && SLAB_META_WORDS == 8, "a slab's publication is two 16-byte stores");
 static_assert(SLAB_LEADERS >= SLAB_BOUND_KEYS && SLAB_LEADERS <= 32, "leaders are distinct lane maxima");
+static_assert(GEMV_KPB <= 2, "the pack warp's 32 lanes cover one stage's k columns");
 static_assert(SLAB_CAND == 32 && (GEMV_THREADS - 32) % 32 == 0, "the owner's gather reads one slab per warp step");
+
+// hidden element i widened exactly to fp32 (dtype 0: fp32, 1: fp16, 2: bf16)
+__device__ __forceinline__ float widen_elem(const void* p, int dtype, int64_t i) {
+  if (dtype == 0) return static_cast<const float*>(p)[i];
+  if (dtype == 1) return __half2float(static_cast<const __half*>(p)[i]);
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+
+__device__ __forceinline__ uint32_t bf16_bits_rn(float v) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t x, uint32_t y) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
+}
 
 __device__ __forceinline__ void consumer_barrier() {
   asm volatile("bar.sync 1, %0;" ::"r"(GEMV_CONSUMER_WARPS * 32) : "memory");
@@ -135,50 +151,6 @@ __device__ __forceinline__ void publish_rows(const GemvArgs& a, const float* sla
     if (lane == 0)
       asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(a.row_sync + r), "l"(1ull) : "memory");
   }
-}
-
-// sorted[0, want) = the largest `want` of the m distinct composites comp[0, m),
-// in descending order, with every thread of the CTA.  comp must have room for
-// m rounded up to a multiple of 32.  Each warp sorts runs of 32 in registers
-// (bitonic network over the lanes); an element's position is then its place
-// in its own run plus, for every other run, the number of its elements above
-// it (a binary search of that sorted run).
-__device__ __forceinline__ void sort_runs(uint64_t* comp, uint64_t* sorted, int m, int want) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const int R = (m + 31) >> 5;
-  for (int r = warp; r < R; r += nw) {
-    const int i = r * 32 + lane;
-    uint64_t v = i < m ? comp[i] : 0ull;  // 0 is below every composite
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
-        // blocks with (lane & k) == 0 run descending; the lower lane of a pair keeps the larger
-        const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
-        v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
-      }
-    }
-    comp[i] = v;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < m; i += blockDim.x) {
-    const uint64_t v = comp[i];
-    const int own = i >> 5;
-    int pos = i & 31;
-#pragma unroll 4
-    for (int q = 0; q < R; ++q) {
-      const uint64_t* run = comp + q * 32;
-      int above = 0;  // elements of run q greater than v (the run is descending)
-#pragma unroll
-      for (int step = 16; step > 0; step >>= 1)
-        if (run[above + step - 1] > v) above += step;
-      if (run[above] > v) ++above;
-      pos += q == own ? 0 : above;
-    }
-    if (pos < want) sorted[pos] = v;
-  }
-  __syncthreads();
 }
 
 // sorted[0, min(K, m)) = the top of keys/idx[0, m) in (value desc, index asc)
@@ -362,9 +334,9 @@ __device__ __forceinline__ void own_rows(const GemvArgs& a, uint8_t* ring, int c
       a.topk_val[static_cast<int64_t>(row) * a.topk_ld + j] = key_float(composite_key(sorted[j]));
       a.topk_idx[static_cast<int64_t>(row) * a.topk_ld + j] = composite_idx(sorted[j]);
     }
-    if (a.params != nullptr && a.tokens != nullptr) {  // every thread takes part in the draw
-      const int32_t tok = sample_sorted_row(prm, sorted, want, ebuf, reinterpret_cast<float*>(s_red));
-      if (tid == 0) a.tokens[row] = tok;
+    if (a.params != nullptr && a.tokens != nullptr && warp == 0) {  // the draw: warp 0
+      const int32_t tok = sample_sorted_warp(prm, sorted, want, ebuf);
+      if (lane == 0) a.tokens[row] = tok;
     }
     __syncthreads();
   }
@@ -377,12 +349,14 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
   __shared__ uint32_t s_list[SEL_BLOCK_BUCKET_MAX];
   __shared__ uint32_t s_misc[4];
   __shared__ uint32_t s_own[4];  // owner: x, |F|, wait failed, slabs to rescan
+  __shared__ float s_scale[MAX_ROWS_PER_PASS];  // fused: the rows' rstd
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + MAX_STAGES);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + 2 * MAX_STAGES * 8);
   int* s_consumed_min = reinterpret_cast<int*>(smem + 2 * MAX_STAGES * 8 + 4);
   int* s_issued = reinterpret_cast<int*>(smem + 2 * MAX_STAGES * 8 + 8);
+  const uint32_t scale_bar = smem_u32(smem + 192);  // fused: s_scale is ready
   uint8_t* ring = smem + BAR_REGION;
   const uint32_t ring_u32 = smem_u32(ring);
 
@@ -401,9 +375,10 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, a.fused ? 33 : 1);  // fused: the producer and the pack warp's 32 lanes
       mbar_init(empty0 + 8 * s, GEMV_CONSUMER_WARPS);
     }
+    mbar_init(scale_bar, 1);
     *s_abort = 0;
     *s_consumed_min = total;
     *s_issued = 0;
@@ -411,12 +386,12 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
   }
   __syncthreads();
 
-  if (warp == GEMV_CONSUMER_WARPS) {
+  if (warp == GEMV_PRODUCER_WARP) {
     // ================================================================ producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
-      const uint32_t abytes = static_cast<uint32_t>(MT * APACK_TILE_BYTES);
+      const uint32_t abytes = a.fused ? 0u : static_cast<uint32_t>(MT * APACK_TILE_BYTES);
       auto stage_of = [&](int it) { return ring_u32 + static_cast<uint32_t>((it % NST) * a.stage_bytes); };
       auto issue_w = [&](int it) {
         const int blk = it / spb, js = it % spb;
@@ -443,9 +418,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
       const int npre = min(NST, total);
       for (int it = 0; it < npre; ++it)
         if (it != a.drop_iter) issue_w(it);
-      pdl_wait();  // the packed activations come from the RMSNorm kernel
-      for (int it = 0; it < npre; ++it)
-        if (it != a.drop_iter) issue_a(it);
+      if (!a.fused) {
+        pdl_wait();  // the packed activations come from the RMSNorm kernel
+        for (int it = 0; it < npre; ++it)
+          if (it != a.drop_iter) issue_a(it);
+      }
       int issued = npre;
       for (int it = npre; it < total; ++it) {
         if (*s_abort) break;
@@ -457,11 +434,107 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
         }
         if (it != a.drop_iter) {
           issue_w(it);
-          issue_a(it);
+          if (!a.fused) issue_a(it);
         }
         issued = it + 1;
       }
       *s_issued = issued;
+    }
+  } else if (warp == GEMV_PACK_WARP) {
+    // ================================================================ activations (fused RMSNorm)
+    // Deferred form: a = x * gamma feeds the GEMM and rstd scales its output, so
+    // stage it needs only k columns [32 js, 32 js + 32) of every row.  Lane j
+    // widens x[r][32 js + j] exactly, adds x^2 to row r's running sum, splits
+    // a = hi + lo into two bf16 values and writes them in the mma.sync
+    // A-fragment order the RMSNorm kernel uses; its arrival on the stage's full
+    // barrier releases them.  After the last stage, rstd = 1 / sqrt(ss / H_u +
+    // eps) per row (fixed order: lane sums, then an xor butterfly).
+    if constexpr (MT <= FUSED_MAX_MT) {  // larger batches take the RMSNorm kernel (registers)
+    if (a.fused) {
+      pdl_wait();  // hidden may come from the previous kernel
+      const int active_end = a.zero_pad ? a.H : a.Hu;
+      const int kc = lane & (KSTEP - 1), ksub = lane >> 4;  // a stage is at most two k-steps: 32 columns
+      const int esz = a.dtype == 0 ? 4 : 2;
+      const uint32_t stg = ring_u32 + static_cast<uint32_t>(NST * a.stage_bytes);  // hidden staging ring
+      const char* hid = static_cast<const char*>(a.hidden);
+      // stage `it`'s k columns of every row -> staging slot it % HID_DEPTH, 16-byte async copies
+      auto issue_hidden = [&](int it) {
+        if (it < total) {
+          const int js = it % spb;
+          const int kn = min(KPB, a.ksteps - js * KPB);
+          const int cpr = kn * KSTEP * esz / 16;  // 16-byte chunks per row
+          const uint32_t slot = stg + static_cast<uint32_t>((it % HID_DEPTH) * HID_SLOT_BYTES);
+          for (int q = lane; q < a.B * cpr; q += 32) {
+            const int r = q / cpr, c = q - r * cpr;
+            const char* src = hid + (static_cast<int64_t>(r) * a.H + js * KPB * KSTEP) * esz + c * 16;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(slot + r * HID_ROW_BYTES + c * 16),
+                         "l"(src) : "memory");
+          }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      };
+      float ss[MT * MTILE_ROWS];
+#pragma unroll
+      for (int r = 0; r < MT * MTILE_ROWS; ++r) ss[r] = 0.f;
+      for (int p = 0; p < HID_DEPTH - 1; ++p) issue_hidden(p);
+      for (int it = 0; it < total; ++it) {
+        issue_hidden(it + HID_DEPTH - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(HID_DEPTH - 1) : "memory");
+        __syncwarp();
+        const int js = it % spb;
+        const int kn = min(KPB, a.ksteps - js * KPB);
+        const int h = (js * KPB + ksub) * KSTEP + kc;
+        const bool act = ksub < kn && h < active_end;
+        const float gc = act ? a.gamma[h] : 0.f;
+        const uint8_t* srow = smem + BAR_REGION + NST * a.stage_bytes + (it % HID_DEPTH) * HID_SLOT_BYTES +
+                              (ksub * KSTEP + kc) * esz;
+        float xc[MT * MTILE_ROWS];
+#pragma unroll
+        for (int r = 0; r < MT * MTILE_ROWS; ++r) {
+          float x = 0.f;
+          if (act && r < a.B) {
+            const uint8_t* e = srow + r * HID_ROW_BYTES;
+            x = a.dtype == 0 ? *reinterpret_cast<const float*>(e)
+                : a.dtype == 1 ? __half2float(*reinterpret_cast<const __half*>(e))
+                               : __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(e));
+          }
+          xc[r] = x;
+        }
+        __syncwarp();  // the slot is refilled by the next iteration's copies
+        if (*s_abort) break;
+        if (it >= NST && !mbar_wait_bounded(empty0 + 8 * (it % NST), static_cast<uint32_t>((it / NST) - 1) & 1u,
+                                            a.timeout_ns)) {
+          raise_error(a.err, DEV_TIMEOUT_EMPTY);
+          *s_abort = 1;
+          break;
+        }
+        const uint32_t wbase = ring_u32 + static_cast<uint32_t>((it % NST) * a.stage_bytes + KPB * KSTEP * a.pitch +
+                                                                ksub * MT * APACK_TILE_BYTES + ((kc & 7) >> 1) * 16 +
+                                                                (kc < 8 ? 0 : 8));
+#pragma unroll
+        for (int r = 0; r < MT * MTILE_ROWS; ++r) {
+          ss[r] = fmaf(xc[r], xc[r], ss[r]);
+          const float v = xc[r] * gc;
+          const uint32_t hi = bf16_bits_rn(v);
+          const uint32_t lo = bf16_bits_rn(v - __uint_as_float(hi << 16));
+          const uint32_t hi1 = __shfl_down_sync(0xffffffffu, hi, 1);
+          const uint32_t lo1 = __shfl_down_sync(0xffffffffu, lo, 1);
+          if (ksub < kn && (kc & 1) == 0)
+            st_shared_v2(wbase + static_cast<uint32_t>(((r >> 3) * 32 + (r & 7) * 4) * 16), hi | (hi1 << 16),
+                         lo | (lo1 << 16));
+        }
+        mbar_arrive(full0 + 8 * (it % NST));  // each lane releases its own stores
+      }
+      asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy lands after the warp moves on
+#pragma unroll
+      for (int r = 0; r < MT * MTILE_ROWS; ++r) {
+        float t = ss[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) s_scale[r] = r < a.B ? 1.0f / sqrtf(t / static_cast<float>(a.Hu) + a.eps) : 0.f;
+      }
+      if (lane == 0) mbar_arrive(scale_bar);
+    }
     }
   } else {
     // ================================================================ consumers
@@ -479,7 +552,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
       for (int m = 0; m < MT; ++m) {
         const int r = m * MTILE_ROWS + g;
         if (r >= a.B) continue;
-        const float sc = a.row_scale[r];
+        const float sc = a.fused ? s_scale[r] : a.row_scale[r];
 #pragma unroll
         for (int q = 0; q < PW; ++q) {
           const int pr = warp + GEMV_CONSUMER_WARPS * q;
@@ -561,7 +634,11 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
     // Every consumer warp reaches both barriers whatever happened above; the
     // abort decision is read once, after the first of them.
     consumer_barrier();  // all stages consumed: the ring may now hold the slab logits
-    const bool aborted_c = *s_abort != 0;
+    bool aborted_c = *s_abort != 0;
+    if (!aborted_c && a.fused && !mbar_wait_bounded(scale_bar, 0u, a.timeout_ns)) {
+      raise_error(a.err, DEV_TIMEOUT_FULL);
+      aborted_c = true;
+    }
     if (!aborted_c && a.logits_in_smem) block_epilogue(last_bp0, last_npb);
     __threadfence_block();
     consumer_barrier();
@@ -635,13 +712,14 @@ GemvPlan plan_gemv(int B, int H, int V, int K, int nslab, int max_smem, int kpb,
   p.kpb = kpb;
   p.stage_bytes = ((kpb * (KSTEP * p.pitch + p.mt * APACK_TILE_BYTES)) + 127) & ~127;
   const int budget = max_smem - BAR_REGION;
-  p.nstages = budget / p.stage_bytes;
+  const int hid = p.mt <= FUSED_MAX_MT ? HID_DEPTH * HID_SLOT_BYTES : 0;  // fused: hidden staging after the ring
+  p.nstages = (budget - hid) / p.stage_bytes;
   if (p.nstages > max_stages) p.nstages = max_stages;
   if (p.nstages > MAX_STAGES) p.nstages = MAX_STAGES;
   p.max_slab_cols = max_slab_pairs * 16;
   const int nblk = (max_slab_pairs + p.cb_pairs - 1) / p.cb_pairs;
   const int smem_logits = (B * p.max_slab_cols * 4 + 127) & ~127;
-  const int ring = p.nstages * p.stage_bytes;
+  const int ring = p.nstages * p.stage_bytes + hid;
   p.logits_in_smem = (nblk == 1 && smem_logits <= budget) ? 1 : 0;
   // owner phase: candidate buffer (capc keys + ids), sort buffer, sampler scratch, slab counts and bounds
   // composite buffer: the top-K selection writes up to K entries, the direct rank sort up to RANK_SORT_MAX

@@ -249,29 +249,13 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
       block_top_composites(keys, idx, ncand, want, comp, s_red, s_list, s_misc);
       nr = want;
     }
-    // composites are distinct: rank(i) = #{j : comp[j] > comp[i]} is i's position
-    for (int i = tid; i < nr; i += nt) {
-      const uint64_t ci = comp[i];
-      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-      int j = 0;
-      for (; j + 4 <= nr; j += 4) {
-        r0 += comp[j] > ci;
-        r1 += comp[j + 1] > ci;
-        r2 += comp[j + 2] > ci;
-        r3 += comp[j + 3] > ci;
-      }
-      for (; j < nr; ++j) r0 += comp[j] > ci;
-      const int rank = (r0 + r1) + (r2 + r3);
-      if (rank < want) sorted[rank] = ci;
-    }
-    __syncthreads();
+    sort_runs(comp, sorted, nr, want);
     for (int j = tid; j < want; j += nt) {
       a.topk_val[static_cast<int64_t>(row) * a.topk_ld + j] = key_float(composite_key(sorted[j]));
       a.topk_idx[static_cast<int64_t>(row) * a.topk_ld + j] = composite_idx(sorted[j]);
     }
-    if (a.params != nullptr && a.tokens != nullptr) {  // every thread takes part in the draw
-      const int32_t tok = sample_sorted_row(prm, sorted, want, ebuf,
-                                            reinterpret_cast<float*>(s_red));
+    if (a.params != nullptr && a.tokens != nullptr && (tid >> 5) == 0) {  // the draw: warp 0
+      const int32_t tok = sample_sorted_warp(prm, sorted, want, ebuf);
       if (tid == 0) a.tokens[row] = tok;
     }
     __syncthreads();

@@ -220,13 +220,23 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
     ra.deferred = cfg->deferred_rms ? 1 : 0;
     ra.apack = reinterpret_cast<uint32_t*>(base + L.apack);
     ra.row_scale = reinterpret_cast<float*>(base + L.row_scale);
-    e = launch_rms_pack(ra, s);
-    if (e != cudaSuccess) return cuda_fail(e, "tail_run_noalloc: kernel launch");
+    const bool fused = cfg->deferred_rms && plan.logits_in_smem && plan.mt <= FUSED_MAX_MT;
+    if (!fused) {
+      e = launch_rms_pack(ra, s);
+      if (e != cudaSuccess) return cuda_fail(e, "tail_run_noalloc: kernel launch");
+    }
 
     GemvArgs ga;
     ga.w = w_t;
     ga.apack = base + L.apack;
     ga.row_scale = reinterpret_cast<const float*>(base + L.row_scale);
+    ga.fused = fused ? 1 : 0;
+    ga.hidden = ra.hidden;
+    ga.dtype = cfg->hidden_dtype;
+    ga.gamma = gamma;
+    ga.Hu = Hu;
+    ga.eps = cfg->eps;
+    ga.zero_pad = ra.zero_pad;
     ga.logits_out = out_logits_opt ? out_logits_opt + static_cast<int64_t>(r0) * V : nullptr;
     ga.logits_out_ld = V;
     ga.logits_scratch = (has_out && plan.logits_in_smem) ? nullptr : reinterpret_cast<float*>(base + L.lscr);

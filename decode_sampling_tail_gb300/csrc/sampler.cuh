@@ -1,16 +1,17 @@
 // Per-row sampler of the tail ("GPT-OSS Tail Chunked Megakernel Kernel API
 // Reference", parameter `sampling_params`: per row [top_k, top_p, temperature]
 // and an optional inverse-transform draw u in [0, 1), 0.5 when the 4th column
-// is absent).  All threads of the CTA, over the row's candidates sorted by
-// (logit desc, index asc), l_0 >= l_1 >= ...:
+// is absent).  One warp, over the row's candidates sorted by (logit desc,
+// index asc), l_0 >= l_1 >= ...:
 //   kk = trunc(top_k) when 1 <= top_k < n + 1, else n (the cut is disabled);
 //   temperature <= 0 (or NaN) or kk == 1: greedy, token = idx_0;
 //   e_i = exp((l_i - l_0) / T) for i < kk, S_j = sum_{i<=j} e_i, Z = S_{kk-1};
 //   m = kk when top_p >= 1, else the smallest j+1 with S_j >= top_p * Z;
 //   token = idx_j for the smallest j < m with u * S_{m-1} < S_j, else idx_{m-1}.
-// The running sums use one fixed order (each thread sums a contiguous chunk on
-// top of the block-scanned sum of the chunks before it), so a row's token never
-// depends on the batch it runs in.
+// The running sums use one fixed order: lane l sums its contiguous chunk of
+// E = ceil(kk / 32) candidates on top of the warp-scanned sum of the chunks
+// before it.  It depends on kk only, so a row's token never depends on the
+// batch, the kernel or the block size it runs in.
 #pragma once
 
 #include "common.cuh"
@@ -18,47 +19,6 @@
 
 namespace tail {
 
-// Block-wide exclusive prefix sum of one float per thread (fixed order: within
-// a warp by its shuffle scan, then the warp totals in warp order).  red: 64
-// floats of shared scratch.  Returns the exclusive prefix; *total the sum.
-__device__ __forceinline__ float block_excl_scan(float v, float* red, float* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  float incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) red[warp] = incl;
-  __syncthreads();
-  float base = 0.f, tot = 0.f;
-  for (int w = 0; w < nw; ++w) {
-    const float x = red[w];
-    if (w < warp) base += x;
-    tot += x;
-  }
-  *total = tot;
-  __syncthreads();  // red is reused by the caller
-  return base + incl - v;
-}
-
-__device__ __forceinline__ unsigned block_min_u32(unsigned v, unsigned* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  v = __reduce_min_sync(0xffffffffu, v);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  unsigned m = 0xffffffffu;
-  for (int w = 0; w < nw; ++w) m = min(m, red[w]);
-  __syncthreads();
-  return m;
-}
-
-// The draw, with every thread of the CTA.  sorted[0..nc): composites in
-// descending order; ebuf: nc floats and red: 64 words of shared scratch.
-// Thread t owns the contiguous candidates [t*E, (t+1)*E) (E = ceil(kk / threads)),
-// so S_j = (sum over the chunks before t's) + e_{tE} + ... + e_j in one fixed
-// order: a row's token does not depend on the batch it runs in.  Every
-// thread returns the token.
 // The row's parameters, read once (early, so their latency overlaps other work).
 struct SampleParams {
   float top_k, top_p, temp, u;
@@ -72,66 +32,69 @@ __device__ __forceinline__ SampleParams load_sample_params(const float* p, int n
   return sp;
 }
 
-__device__ __forceinline__ int32_t sample_sorted_row(const SampleParams& sp, const uint64_t* sorted, int nc,
-                                                     float* ebuf, float* red) {
-  const int tid = threadIdx.x, nt = blockDim.x;
+// The draw, by one whole warp (every lane returns the token).  sorted[0, nc):
+// composites in descending order; ebuf: nc floats of shared scratch (each lane
+// writes and reads only its own chunk).
+__device__ __forceinline__ int32_t sample_sorted_warp(const SampleParams& sp, const uint64_t* sorted, int nc,
+                                                      float* ebuf) {
+  const int lane = threadIdx.x & 31;
   const float top_k = sp.top_k, top_p = sp.top_p, temp = sp.temp, u = sp.u;
   auto val_at = [&](int i) { return key_float(composite_key(sorted[i])); };
   const int kk = (top_k >= 1.0f && top_k < static_cast<float>(nc) + 1.0f) ? static_cast<int>(top_k) : nc;
   if (!(temp > 0.0f) || kk == 1) return composite_idx(sorted[0]);
   const float l0 = val_at(0);
-  const int E = (kk + nt - 1) / nt;
-  const int i0 = min(kk, tid * E), i1 = min(kk, i0 + E);
+  const int E = (kk + 31) >> 5;
+  const int i0 = min(kk, lane * E), i1 = min(kk, i0 + E);
   float ls = 0.f;
   for (int i = i0; i < i1; ++i) {
     const float e = expf((val_at(i) - l0) / temp);
     ebuf[i] = e;
     ls += e;
   }
-  float Z;
-  const float excl = block_excl_scan(ls, red, &Z);  // Z = S_{kk-1}
-  unsigned* ured = reinterpret_cast<unsigned*>(red);
+  float incl = ls;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  float excl = __shfl_up_sync(0xffffffffu, incl, 1);      // sum of the chunks before this lane's
+  if (lane == 0) excl = 0.f;
+  const float Z = __shfl_sync(0xffffffffu, incl, 31);     // S_{kk-1}
   int m = kk;
+  float Cm = Z;                                           // S_{m-1}
   if (top_p < 1.0f) {
     const float tp = top_p * Z;
-    unsigned found = 0xffffffffu;
-    float S = excl;
+    int found = -1;
+    float S = excl, Sf = 0.f;
     for (int i = i0; i < i1; ++i) {
       S += ebuf[i];
       if (S >= tp) {
-        found = static_cast<unsigned>(i);
+        found = i;
+        Sf = S;
         break;
       }
     }
-    found = block_min_u32(found, ured);
-    m = found == 0xffffffffu ? kk : static_cast<int>(found) + 1;
-  }
-  // C_{m-1}, from the thread that owns candidate m - 1
-  float Cm = Z;
-  if (m < kk) {
-    if (i0 <= m - 1 && m - 1 < i1) {
-      float S = excl;
-      for (int i = i0; i <= m - 1; ++i) S += ebuf[i];
-      red[32] = S;
+    const uint32_t who = __ballot_sync(0xffffffffu, found >= 0);
+    if (who != 0u) {
+      const int src = __ffs(who) - 1;
+      m = __shfl_sync(0xffffffffu, found, src) + 1;
+      Cm = __shfl_sync(0xffffffffu, Sf, src);
     }
-    __syncthreads();
-    Cm = red[32];
-    __syncthreads();
   }
   const float target = u * Cm;
-  unsigned pick = 0xffffffffu;
+  int pick = -1;
   {
     float S = excl;
     for (int i = i0; i < min(i1, m); ++i) {
       S += ebuf[i];
       if (target < S) {
-        pick = static_cast<unsigned>(i);
+        pick = i;
         break;
       }
     }
   }
-  pick = block_min_u32(pick, ured);
-  const int j = pick == 0xffffffffu ? m - 1 : static_cast<int>(pick);
+  const uint32_t who = __ballot_sync(0xffffffffu, pick >= 0);
+  const int j = who != 0u ? __shfl_sync(0xffffffffu, pick, __ffs(who) - 1) : m - 1;
   return composite_idx(sorted[j]);
 }
 

@@ -330,4 +330,48 @@ __device__ __forceinline__ void block_bitonic_desc(uint64_t* comp, int P) {
   }
 }
 
+// sorted[0, want) = the largest `want` of the m distinct composites comp[0, m),
+// in descending order, with every thread of the CTA.  comp must have room for
+// m rounded up to a multiple of 32.  Each warp sorts runs of 32 in registers
+// (bitonic network over the lanes); an element's position is then its place
+// in its own run plus, for every other run, the number of its elements above
+// it (a binary search of that sorted run).
+__device__ __forceinline__ void sort_runs(uint64_t* comp, uint64_t* sorted, int m, int want) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int R = (m + 31) >> 5;
+  for (int r = warp; r < R; r += nw) {
+    const int i = r * 32 + lane;
+    uint64_t v = i < m ? comp[i] : 0ull;  // 0 is below every composite
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+        // blocks with (lane & k) == 0 run descending; the lower lane of a pair keeps the larger
+        const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+        v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
+      }
+    }
+    comp[i] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    const uint64_t v = comp[i];
+    const int own = i >> 5;
+    int pos = i & 31;
+#pragma unroll 4
+    for (int q = 0; q < R; ++q) {
+      const uint64_t* run = comp + q * 32;
+      int above = 0;  // elements of run q greater than v (the run is descending)
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1)
+        if (run[above + step - 1] > v) above += step;
+      if (run[above] > v) ++above;
+      pos += q == own ? 0 : above;
+    }
+    if (pos < want) sorted[pos] = v;
+  }
+  __syncthreads();
+}
+
 }  // namespace tail

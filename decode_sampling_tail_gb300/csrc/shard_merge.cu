@@ -60,26 +60,13 @@ __global__ void __launch_bounds__(SHARD_THREADS) shard_merge_kernel(const ShardM
       block_top_composites(keys, ids, n, K, comp, s_red, s_list, s_misc);
       nr = K;
     }
-    // composites are distinct: rank(i) = #{j : comp[j] > comp[i]} is i's position
-    for (int i = tid; i < nr; i += nt) {
-      const uint64_t ci = comp[i];
-      int r0 = 0, r1 = 0;
-      int j = 0;
-      for (; j + 2 <= nr; j += 2) {
-        r0 += comp[j] > ci;
-        r1 += comp[j + 1] > ci;
-      }
-      for (; j < nr; ++j) r0 += comp[j] > ci;
-      const int rank = r0 + r1;
-      if (rank < K) sorted[rank] = ci;
-    }
-    __syncthreads();
+    sort_runs(comp, sorted, nr, K);
     if (a.topk_val != nullptr)
       for (int j = tid; j < K; j += nt) a.topk_val[static_cast<int64_t>(row) * K + j] = key_float(composite_key(sorted[j]));
     if (a.topk_idx != nullptr)
       for (int j = tid; j < K; j += nt) a.topk_idx[static_cast<int64_t>(row) * K + j] = composite_idx(sorted[j]);
-    if (a.params != nullptr && a.tokens != nullptr) {
-      const int32_t tok = sample_sorted_row(prm, sorted, K, ebuf, reinterpret_cast<float*>(s_red));
+    if (a.params != nullptr && a.tokens != nullptr && (tid >> 5) == 0) {  // the draw: warp 0
+      const int32_t tok = sample_sorted_warp(prm, sorted, K, ebuf);
       if (tid == 0) a.tokens[row] = tok;
     }
     __syncthreads();

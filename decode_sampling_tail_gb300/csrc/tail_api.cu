@@ -422,14 +422,25 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     ra.deferred = c.deferred_rms ? 1 : 0;
     ra.apack = h->apack;
     ra.row_scale = h->row_scale;
-    e = launch_rms_pack(ra, stream);
-    if (e != cudaSuccess) break;
+    // deferred RMSNorm with the slab logits in shared memory: the lm_head kernel forms the activations
+    const bool fused = c.deferred_rms && plan.logits_in_smem && plan.mt <= FUSED_MAX_MT;
+    if (!fused) {
+      e = launch_rms_pack(ra, stream);
+      if (e != cudaSuccess) break;
+    }
     if (ev) cudaEventRecord(ev[1], stream);
 
     GemvArgs ga;
     ga.w = w_t;
     ga.apack = reinterpret_cast<const uint8_t*>(h->apack);
     ga.row_scale = h->row_scale;
+    ga.fused = fused ? 1 : 0;
+    ga.hidden = ra.hidden;
+    ga.dtype = c.hidden_dtype;
+    ga.gamma = gamma;
+    ga.Hu = c.hidden_actual;
+    ga.eps = c.eps;
+    ga.zero_pad = ra.zero_pad;
     ga.logits_out = out_logits ? out_logits + static_cast<int64_t>(r0) * c.V : nullptr;
     ga.logits_out_ld = c.V;
     ga.logits_scratch = h->logit_scratch;
@@ -645,7 +656,12 @@ int tail_get_info(const tail_t* h, tail_info* out) {
   out->merge_groups = 0;
   out->lmhead_path = h->pdl_ok ? 2 : 1;
   out->rows_per_pass = h->rows_pass;
+  // one launch per pass when the lm_head kernel forms the activations itself, else RMSNorm + lm_head
   out->kernels_per_run = 2;
+  if (h->rows_pass > 0 && h->cfg.deferred_rms) {
+    const GemvPlan p = plan_gemv(h->rows_pass, h->cfg.H, h->cfg.V, h->cfg.k, h->nslab, h->max_smem);
+    if (p.logits_in_smem && p.mt <= FUSED_MAX_MT) out->kernels_per_run = 1;
+  }
   out->scratch_bytes = h->scratch_bytes;
   out->tc_min_rows = h->tc_min;
   return TAIL_OK;

@@ -90,7 +90,10 @@ typedef struct {
   int32_t lmhead_path;      /* 1: cooperative mma.sync lm_head + top-k + sampler launch;
                                2: the same, overlapped with the RMSNorm kernel (programmatic launch) */
   int32_t rows_per_pass;    /* rows one mma.sync lm_head pass covers */
-  int32_t kernels_per_run;  /* kernel launches of one tail_run on the mma.sync path */
+  int32_t kernels_per_run;  /* kernel launches of one full pass on the mma.sync path: 1 when the
+                               lm_head kernel forms the deferred-RMSNorm activations itself (up to
+                               16 rows whose slab logits fit in shared memory), else 2 (RMSNorm
+                               kernel + lm_head) */
   int64_t scratch_bytes;    /* device scratch owned by the handle */
   int32_t tc_min_rows;      /* runs with gbs >= this take the tensor-core path (split, tcgen05
                                lm_head with per-tile candidate lists, merge + sampler: 3 kernels,
