@@ -342,7 +342,7 @@ def main():
     tc_path = t.info.tc_min_rows > 0 and w.B >= t.info.tc_min_rows
     if tc_path:  # split -> tensor-core lm_head -> merge + sampler, one pass
         passes, launches_per_step, kernel = 1, 3, "lmhead_tc_kernel"
-    else:        # rms_rows -> cooperative lm_head + top-k + sampler, per pass
+    else:        # [rms_rows ->] cooperative lm_head + top-k + sampler, per pass
         passes = (w.B + t.info.rows_per_pass - 1) // t.info.rows_per_pass
         launches_per_step, kernel = t.info.kernels_per_run * passes, "lmhead_tail_kernel"
 
@@ -420,6 +420,12 @@ def main():
             step()
     kms, npass = dst.tail_profile_read(t.h)
     dst.tail_profile_enable(t.h, False)
+    # report only the kernels this path launches: the mma.sync path has no merge kernel, and when the
+    # lm_head kernel forms the activations itself (one launch per pass) no RMSNorm kernel either
+    if not tc_path:
+        kms.pop("merge", None)
+        if t.info.kernels_per_run == 1:
+            kms.pop("rms_rows", None)
     lm_ms = kms["lm_head"] / max(1, npass)  # the dominant kernel (per pass)
     kshare = {k: v / max(1e-9, sum(kms.values())) for k, v in kms.items()}
 

@@ -92,8 +92,8 @@ struct GemvArgs {
   int drop_iter;            // test hook: ring iteration the producer never issues (-1: none)
 };
 
-// Launchers (all enqueue on `stream`; the lm_head tail is a cooperative launch,
-// chained to the RMSNorm kernel with programmatic dependent launch when pdl).
+// Launchers (all enqueue on `stream`; the lm_head tail is one launch,
+// chained to the previous kernel on the stream with programmatic dependent launch when pdl).
 cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream);
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t stream, bool pdl);
 // per device: opt the lm_head kernels into the largest dynamic shared memory

@@ -1,5 +1,5 @@
 // The lm_head projection and everything after it -- the global top-k and the
-// sampler -- in one cooperative launch.
+// sampler -- in one launch.
 //
 // Computes logit[b, v] = row_scale[b] * sum_h a[b, h] * W[h, v] for a batch of
 // up to 64 rows ("GPT-OSS Tail Chunked Megakernel Kernel API Reference",
@@ -26,8 +26,9 @@
 //   * Every column's k-reduction runs through the same mma sequence wherever
 //     the column sits, so duplicated W columns give bitwise-equal logits.
 //
-// Top-k and sampler, in two phases with one exchange between them (the launch
-// is cooperative, so every CTA is resident and the owners' waits end; each
+// Top-k and sampler, in two phases with one exchange between them (only the
+// row owners wait, for the slabs' publications, and a slab publishes without
+// waiting for anything, so the waits end whatever order the CTAs run in; each
 // wait is bounded):
 //   P  per (row, slab), no waiting: b = the 8th largest of the 32 lane maxima
 //      of the slab's logits (8 distinct elements are >= b).  The slab
@@ -676,13 +677,13 @@ cudaError_t launch_t(const GemvArgs& a, cudaStream_t stream, bool pdl) {
   cfg.blockDim = dim3(GEMV_THREADS);
   cfg.dynamicSmemBytes = a.smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  // A plain launch: no CTA waits for one that has not started (slabs publish without waiting; only
+  // the row owners wait, for the publications), so the grid needs no co-residency guarantee.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, lmhead_tail_kernel<MT, PW>, a);
 }
 

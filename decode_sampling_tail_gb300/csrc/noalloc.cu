@@ -1,6 +1,6 @@
 // tail_run_noalloc: the tail without a handle and without any device
 // allocation.  It launches the same two kernels as tail_run (rms_pack, then the
-// cooperative lm_head + global top-k + sampler), but their scratch lives in one
+// lm_head + global top-k + sampler), but their scratch lives in one
 // file-scope device array of fixed size instead of handle-owned cudaMalloc
 // memory.
 //
@@ -33,7 +33,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH
 
 struct NoallocDevice {
   std::atomic<int> ready;   // 1 once setup on this device succeeded
-  std::atomic<int> pdl_ok;  // 0 once a cooperative launch with programmatic serialization was refused
+  std::atomic<int> pdl_ok;  // 0 once a launch with programmatic serialization was refused
   uint8_t* base;            // device address of g_noalloc_scratch on this device
   int num_sms;
   int max_dyn;              // dynamic shared memory the lm_head kernels may use
@@ -55,15 +55,14 @@ int setup_device(int dev, NoallocDevice** out) {
   }
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (!d.ready.load(std::memory_order_relaxed)) {
-    int major = 0, minor = 0, sms = 0, coop = 0, optin = 0;
+    int major = 0, minor = 0, sms = 0, optin = 0;
     cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return cuda_fail(e, "tail_run_noalloc: cudaDeviceGetAttribute");
-    if (major != 10 || minor != 3 || !coop) {
-      set_last_error("tail_run_noalloc: the current device is not an sm_103 device with cooperative launch");
+    if (major != 10 || minor != 3) {
+      set_last_error("tail_run_noalloc: the current device is not an sm_103 device");
       return TAIL_ERR_UNSUPPORTED;
     }
     void* base = nullptr;
@@ -272,7 +271,7 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
     ga.drop_iter = -1;
     if (d->pdl_ok.load(std::memory_order_relaxed)) {
       e = launch_gemv(ga, s, true);
-      if (e != cudaSuccess) {  // this runtime refuses cooperative + programmatic: launch without the overlap
+      if (e != cudaSuccess) {  // this runtime refuses programmatic serialization: launch without the overlap
         cudaGetLastError();
         d->pdl_ok.store(0, std::memory_order_relaxed);
       }

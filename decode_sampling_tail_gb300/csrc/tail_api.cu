@@ -1,6 +1,6 @@
 // C ABI of the decode sampling tail: handle lifetime, argument validation,
 // scratch ownership and the launch sequence of one step
-//   rms_rows -> lm_head + global top-k + sampler (one cooperative launch),
+//   [rms_rows ->] lm_head + global top-k + sampler (one launch),
 // on the caller's stream, chained with programmatic dependent launch.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -29,7 +29,7 @@ struct tail_s {
   int nslab;
   int rows_pass;  // rows per lm_head pass
   int tc_min;     // batches of at least this many rows take the tensor-core path; 0: none do
-  int pdl_ok;     // 0 once a cooperative launch with programmatic serialization was refused
+  int pdl_ok;     // 0 once a launch with programmatic serialization was refused
   int64_t scratch_bytes;
   // device scratch
   uint32_t* apack;
@@ -208,10 +208,6 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   h->max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
   const int64_t npairs = cfg->V / 16;
   h->nslab = slab_count(npairs, h->num_sms, MAX_SLABS);
-  if (!prop.cooperativeLaunch) {
-    delete h;
-    return TAIL_ERR_UNSUPPORTED;
-  }
   // the tensor-core path, when the merge can be planned for k and V: batches of
   // TC_MIN_ROWS rows or more always take it; narrow vocabularies take it for
   // every batch (the mma.sync kernel's per-row bulk copies make it no faster there)
@@ -476,7 +472,7 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     ga.drop_iter = h->drop_iter;
     if (h->pdl_ok) {
       e = launch_gemv(ga, stream, true);
-      if (e != cudaSuccess) {  // this runtime refuses cooperative + programmatic: launch without the overlap
+      if (e != cudaSuccess) {  // this runtime refuses programmatic serialization: launch without the overlap
         cudaGetLastError();
         h->pdl_ok = 0;
       }

@@ -66,7 +66,7 @@ typedef struct {
 } tail_config;
 
 /*
- * lm_head realisations.  The cooperative mma.sync kernel streams W once for up
+ * lm_head realisations.  The mma.sync kernel streams W once for up
  * to 8 rows and fuses the top-k and the sampler; it issues one bulk copy per
  * W row per stage, so its time hardly falls below ~150 us however narrow the
  * vocabulary.  The tensor-core path (split, tcgen05 lm_head with per-tile
@@ -87,8 +87,9 @@ typedef struct {
   int32_t num_sms;          /* SMs of the device */
   int32_t nslab;            /* vocabulary slabs = CTAs of the lm_head kernel */
   int32_t merge_groups;     /* 0: the top-k merge runs inside the lm_head launch */
-  int32_t lmhead_path;      /* 1: cooperative mma.sync lm_head + top-k + sampler launch;
-                               2: the same, overlapped with the RMSNorm kernel (programmatic launch) */
+  int32_t lmhead_path;      /* 1: mma.sync lm_head + top-k + sampler launch;
+                               2: the same, launched with programmatic serialization (it overlaps
+                               the previous kernel on the stream until its dependency wait) */
   int32_t rows_per_pass;    /* rows one mma.sync lm_head pass covers */
   int32_t kernels_per_run;  /* kernel launches of one full pass on the mma.sync path: 1 when the
                                lm_head kernel forms the deferred-RMSNorm activations itself (up to
