@@ -92,12 +92,21 @@ __device__ __forceinline__ void publish_rows(const GemvArgs& a, const float* sla
                                          int64_t vbase, int c) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto load_row_keys = [&](int r, uint32_t (&k)[SEL_NPL]) {
-    const float* src = a.logits_in_smem ? slab_logits + r * max_cols
-                                        : a.logits_scratch + static_cast<int64_t>(r) * a.V + vbase;
+    if (a.logits_in_smem) {  // explicit shared-memory loads (a generic pointer would not say so)
+      const uint32_t src = smem_u32(slab_logits + r * max_cols) + 4u * lane;
 #pragma unroll
-    for (int i = 0; i < SEL_NPL; ++i) {
-      const int pos = i * 32 + lane;
-      k[i] = pos < n ? float_key(src[pos]) : 0u;
+      for (int i = 0; i < SEL_NPL; ++i) {
+        uint32_t v = 0u;
+        if (i * 32 + lane < n) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(src + 128u * i));
+        k[i] = i * 32 + lane < n ? float_key(__uint_as_float(v)) : 0u;
+      }
+    } else {
+      const float* src = a.logits_scratch + static_cast<int64_t>(r) * a.V + vbase;
+#pragma unroll
+      for (int i = 0; i < SEL_NPL; ++i) {
+        const int pos = i * 32 + lane;
+        k[i] = pos < n ? float_key(src[pos]) : 0u;
+      }
     }
   };  for (int r = warp; r < a.B; r += GEMV_CONSUMER_WARPS) {
     uint32_t k[SEL_NPL];
@@ -110,17 +119,21 @@ __device__ __forceinline__ void publish_rows(const GemvArgs& a, const float* sla
       m2 = max(m2, k[i + 2]);
       m3 = max(m3, k[i + 3]);
     }
+    // the 32 lane maxima sorted descending over the lanes (bitonic network): lane j then holds the
+    // (j+1)-th largest, so lanes 0..3 are the leaders and lane SLAB_LEADERS-1 holds b
     uint32_t lm = max(max(m0, m1), max(m2, m3));
-    uint32_t lead[SLAB_BOUND_KEYS];
-    uint32_t b = 0u;
 #pragma unroll
-    for (int j = 0; j < SLAB_LEADERS; ++j) {
-      const uint32_t best = __reduce_max_sync(0xffffffffu, lm);
-      const uint32_t who = __ballot_sync(0xffffffffu, lm == best);
-      if (j < SLAB_BOUND_KEYS) lead[j] = best;
-      b = best;
-      if (lane == __ffs(who) - 1) lm = 0u;  // each lane maximum counts once
+    for (int kb = 2; kb <= 32; kb <<= 1) {
+#pragma unroll
+      for (int j = kb >> 1; j > 0; j >>= 1) {
+        const uint32_t o = __shfl_xor_sync(0xffffffffu, lm, j);
+        lm = (((lane & j) == 0) == ((lane & kb) == 0)) ? max(lm, o) : min(lm, o);
+      }
     }
+    uint32_t lead[SLAB_BOUND_KEYS];
+#pragma unroll
+    for (int j = 0; j < SLAB_BOUND_KEYS; ++j) lead[j] = __shfl_sync(0xffffffffu, lm, j);
+    const uint32_t b = __shfl_sync(0xffffffffu, lm, SLAB_LEADERS - 1);
     uint32_t mine = 0;
 #pragma unroll
     for (int i = 0; i < SEL_NPL; ++i) mine += (i * 32 + lane < n && k[i] >= b) ? 1u : 0u;
@@ -351,6 +364,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
   __shared__ uint32_t s_misc[4];
   __shared__ uint32_t s_own[4];  // owner: x, |F|, wait failed, slabs to rescan
   __shared__ float s_scale[MAX_ROWS_PER_PASS];  // fused: the rows' rstd
+  // the post-stream phases read their arguments from here: fields first touched after the long
+  // stream would otherwise miss the constant cache one line at a time
+  __shared__ __align__(16) GemvArgs s_args;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + MAX_STAGES);
@@ -380,6 +396,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
       mbar_init(empty0 + 8 * s, GEMV_CONSUMER_WARPS);
     }
     mbar_init(scale_bar, 1);
+    s_args = a;
     *s_abort = 0;
     *s_consumed_min = total;
     *s_issued = 0;
@@ -665,8 +682,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
   const int64_t vbase = pair_lo * 16;
 
 
-  if (!aborted && warp < GEMV_CONSUMER_WARPS) publish_rows(a, slab_logits, max_cols, n, vbase, c);
-  if (!aborted) own_rows(a, ring, c, s_red, s_list, s_misc, s_own);
+  if (!aborted && warp < GEMV_CONSUMER_WARPS) publish_rows(s_args, slab_logits, max_cols, n, vbase, c);
+  if (!aborted) own_rows(s_args, ring, c, s_red, s_list, s_misc, s_own);
   pdl_launch_dependents();
 }
 
