@@ -5,7 +5,7 @@
 //
 // One CTA per batch row.  Input: for every column tile the row's top TC_LIST
 // composites (value desc, index asc), written by the tensor-core lm_head, and
-// the row's fp32 logits.
+// the row's fp32 logits.  The row's lists reach shared memory in one bulk copy.
 //   1. x = a lower bound (exact in its top 16 bits) of the K-th largest key
 //      among the list heads, each tile's largest element.  These are distinct
 //      elements of the row, so the row's K-th largest element has key >= x.
@@ -16,7 +16,7 @@
 //      last entry is >= x (a tile with TC_LIST or more elements at or above x)
 //      is replaced by a scan of that tile's logits row.
 //   3. The exact top K of the gathered set, sorted by (value desc, index asc),
-//      is written out and the row's token is drawn from it.
+//      is written out and the row's token is drawn from it (one warp).
 #include "common.cuh"
 #include "internal.h"
 #include "sampler.cuh"
@@ -28,6 +28,8 @@ namespace tail {
 namespace {
 
 constexpr int MERGE_HEADS_PER_LANE = 48;  // list heads one warp holds in registers: up to 1536 tiles
+constexpr int MERGE_LISTS_PB = 1;  // lists a thread takes per gather batch
+constexpr int MERGE_SCAN_PT = 8;   // logits loads in flight per thread in the saturated-tile scan
 
 int next_pow2_host(int x) {
   int p = 1;
@@ -42,20 +44,29 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
   __shared__ uint32_t s_misc[4];
   __shared__ uint32_t s_x;
   __shared__ int s_nsat;
+  __shared__ uint32_t s_nc;  // candidates gathered
+  __shared__ int s_fail;
+  __shared__ __align__(8) uint64_t s_bar;  // the lists' bulk copy
   pdl_wait();  // lists and logits come from the lm_head kernel
 
   const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
   const int K = a.K, ntn = a.ntn;
-  const int nl = ntn * TC_LIST;                           // list entries of a row
-  uint32_t* lk = reinterpret_cast<uint32_t*>(smem);       // [nl]: the keys of every list entry
-  uint32_t* keys = lk + nl;                               // [capc]: gathered candidates
+  const int nl = ntn * TC_LIST;  // list entries of a row
+  const bool heads_bound = ntn >= K && ntn <= 32 * MERGE_HEADS_PER_LANE;
+  uint64_t* ls = reinterpret_cast<uint64_t*>(smem);     // [nl]: the row's lists, copied in whole
+  uint32_t* lk = reinterpret_cast<uint32_t*>(ls + nl);  // [nl] every entry's key, only for few tiles
+  uint32_t* keys = lk + (heads_bound ? 0 : nl);         // [capc]: gathered candidates
   int32_t* idx = reinterpret_cast<int32_t*>(keys + a.capc);
   uint64_t* comp = reinterpret_cast<uint64_t*>(idx + a.capc);
   uint64_t* sorted = comp + a.sortP;
   float* ebuf = reinterpret_cast<float*>(sorted + K);
-  int* cnt = reinterpret_cast<int*>(ebuf + K);  // [ntn]: list entries >= x (0 for a saturated list)
-  int* off = cnt + ntn;                         // [ntn + 1]: exclusive scan of the counts
-  int* sat = off + ntn + 1;                     // [ntn]: saturated lists
+  int* sat = reinterpret_cast<int*>(ebuf + K);  // [ntn]: saturated lists
+  const uint32_t bar = smem_u32(&s_bar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
 
   // keeps the top K of keys/idx[0..n) (n > K), in place; returns K
   auto fold = [&](int n) {
@@ -66,52 +77,44 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
       keys[j] = composite_key(comp[j]);
       idx[j] = composite_idx(comp[j]);
     }
+    if (tid == 0) s_nc = static_cast<uint32_t>(K);
     __syncthreads();
     return K;
   };
 
-  for (int row = blockIdx.x; row < a.B; row += gridDim.x) {
+  int parity = 0;
+  for (int row = blockIdx.x; row < a.B; row += gridDim.x, parity ^= 1) {
     SampleParams prm = {};
     if (a.params != nullptr) prm = load_sample_params(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols);
     const uint64_t* L = a.lists + static_cast<int64_t>(row) * ntn * TC_LIST;
     const float* lg = a.logits + static_cast<int64_t>(row) * a.ld;
 
-    // ---- 1. the bound x: K-th largest key of all list entries (x = 0 when there are fewer than K:
-    // every list is then saturated and all logits are scanned)
-    constexpr int LPT = 4;  // lists per thread whose loads are in flight together
-    for (int j0 = 0; j0 < ntn; j0 += LPT * nt) {
-      uint4 w[LPT][TC_LIST / 2];
-#pragma unroll
-      for (int q = 0; q < LPT; ++q) {
-        const int j = j0 + q * nt + tid;
-        const uint4* src = reinterpret_cast<const uint4*>(L + static_cast<int64_t>(j < ntn ? j : 0) * TC_LIST);
-#pragma unroll
-        for (int i = 0; i < TC_LIST / 2; ++i) w[q][i] = j < ntn ? __ldcg(src + i) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int q = 0; q < LPT; ++q) {
-        const int j = j0 + q * nt + tid;
-        if (j < ntn) {
-#pragma unroll
-          for (int i = 0; i < TC_LIST / 2; ++i) {
-            lk[j * TC_LIST + 2 * i] = w[q][i].y;  // composite key = high word
-            lk[j * TC_LIST + 2 * i + 1] = w[q][i].w;
-          }
-        }
-      }
+    // ---- 1. the row's lists into shared memory: one bulk copy
+    if (tid == 0) {
+      s_nsat = 0;
+      s_nc = 0u;
+      s_fail = 0;
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nl) * 8u);
+      bulk_g2s(smem_u32(ls), L, static_cast<uint32_t>(nl) * 8u, bar, policy_evict_first());
     }
-    if (tid == 0) s_nsat = 0;
+    if (!mbar_wait_bounded(bar, static_cast<uint32_t>(parity), a.timeout_ns)) {
+      raise_error(a.err, DEV_TIMEOUT_FULL);
+      s_fail = 1;
+    }
     __syncthreads();
+    if (s_fail) break;  // uniform (the error flag is raised)
+
+    // ---- 2. the bound x: K-th largest key of the list heads (distinct elements of the row), or of every
+    // list entry when the tiles are fewer than K, or 0 when the entries are fewer than K (every list is
+    // then saturated and all logits are scanned)
     uint32_t x;
-    if (ntn >= K && ntn <= 32 * MERGE_HEADS_PER_LANE) {
-      // the list heads (each tile's largest element) are K or more distinct elements: one warp finds
-      // a lower bound of their K-th largest key, exact in its top 16 bits
+    if (heads_bound) {
       if (warp == 0) {
         uint32_t hk[MERGE_HEADS_PER_LANE];
 #pragma unroll
         for (int i = 0; i < MERGE_HEADS_PER_LANE; ++i) {
           const int j = i * 32 + lane;
-          hk[i] = j < ntn ? lk[j * TC_LIST] : 0u;
+          hk[i] = j < ntn ? composite_key(ls[j * TC_LIST]) : 0u;
         }
         const uint32_t b = warp_bound16_span_regs(hk, K);
         if (lane == 0) s_x = b;
@@ -119,95 +122,107 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
       __syncthreads();
       x = s_x;
     } else {
-      // few tiles (or very many): the K-th largest key over every list entry, or 0 when they are fewer than K
+      for (int e = tid; e < nl; e += nt) lk[e] = composite_key(ls[e]);
+      __syncthreads();
       x = nl >= K ? block_kth_key(lk, nl, K, s_red, s_list, s_misc).key : 0u;
     }
 
-    // ---- 2a. per list: how many entries reach x, or saturated
-    for (int j = tid; j < ntn; j += nt) {
-      int c = 0;
+    // ---- 3. a list whose last entry is below x holds all of its tile's elements >= x (its first c
+    // entries); a list whose last entry is >= x is saturated and its tile's logits are scanned below.
+    // Batches of MERGE_LISTS_PB lists a thread, one reservation per warp; the buffer is folded to the
+    // top K before a batch that might not fit.  A thread reads list j's entries starting at j mod 8
+    // (the lists are 64 bytes apart: in entry order the lanes would share banks).
+    int ncand = 0;
+    for (int j0 = 0; j0 < ntn; j0 += nt * MERGE_LISTS_PB) {
+      if (ncand + nt * MERGE_LISTS_PB * TC_LIST > a.capc) ncand = fold(ncand);
+      uint64_t le[MERGE_LISTS_PB][TC_LIST];
+      int c[MERGE_LISTS_PB];
+      int tot = 0;
 #pragma unroll
-      for (int i = 0; i < TC_LIST; ++i) c += lk[j * TC_LIST + i] >= x ? 1 : 0;
-      if (lk[j * TC_LIST + TC_LIST - 1] >= x) {
-        cnt[j] = 0;
-        sat[atomicAdd(&s_nsat, 1)] = j;
-      } else {
-        cnt[j] = c;
+      for (int r = 0; r < MERGE_LISTS_PB; ++r) {
+        const int j = j0 + r * nt + tid;
+        const uint64_t* lj = ls + static_cast<int64_t>(j < ntn ? j : 0) * TC_LIST;
+#pragma unroll
+        for (int e = 0; e < TC_LIST; ++e) {
+          const int er = (e + j) & (TC_LIST - 1);
+          const uint64_t v = lj[er];
+#pragma unroll
+          for (int t = 0; t < TC_LIST; ++t)  // le[r][er] = v, with er only known at run time
+            if (t == er) le[r][t] = v;
+        }
+        c[r] = 0;
+        if (j < ntn) {
+          if (composite_key(le[r][TC_LIST - 1]) >= x) {
+            sat[atomicAdd(&s_nsat, 1)] = j;
+          } else {
+#pragma unroll
+            for (int e = 0; e < TC_LIST; ++e) c[r] += composite_key(le[r][e]) >= x ? 1 : 0;
+          }
+        }
+        tot += c[r];
       }
-    }
-    __syncthreads();
-    if (warp == 0) {  // exclusive scan of cnt into off
-      const int per = (ntn + 31) / 32;
-      const int s0 = min(ntn, lane * per), s1 = min(ntn, s0 + per);
-      int loc = 0;
-      for (int s = s0; s < s1; ++s) loc += cnt[s];
-      int incl = loc;
+      int incl = tot;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int t = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += t;
       }
-      int run = incl - loc;
-      for (int s = s0; s < s1; ++s) {
-        off[s] = run;
-        run += cnt[s];
-      }
-      if (lane == 31) off[ntn] = incl;
-    }
-    __syncthreads();
-
-    // ---- 2b. gather the list entries >= x (in capacity-sized runs of lists, folding between runs)
-    int ncand = 0;
-    int start = 0;
-    while (start < ntn) {
-      // lists [start, end) whose entries fit behind the ncand already held
-      int lo = start, hi = ntn;
-      while (lo < hi) {  // largest end with off[end] - off[start] + ncand <= capc
-        const int mid = (lo + hi + 1) >> 1;
-        if (off[mid] - off[start] + ncand <= a.capc) lo = mid; else hi = mid - 1;
-      }
-      const int end = lo > start ? lo : start + 1;  // one list (<= TC_LIST entries) always fits after a fold
-      for (int j = start + tid; j < end; j += nt) {
-        const int c = cnt[j];
-        const int p = ncand + off[j] - off[start];
-        const uint64_t* src = L + static_cast<int64_t>(j) * TC_LIST;
-        for (int i = 0; i < c; ++i) {
-          const uint64_t e = __ldcg(src + i);
-          keys[p + i] = composite_key(e);
-          idx[p + i] = composite_idx(e);
-        }
-      }
-      ncand += off[end] - off[start];
-      __syncthreads();
-      start = end;
-      if (start < ntn && ncand > K) ncand = fold(ncand);
-    }
-
-    // ---- 2c. saturated lists: scan their tiles' logits, as many tiles per pass as the buffer takes
-    const int nsat = s_nsat;
-    for (int s0 = 0; s0 < nsat;) {
-      if (ncand + TC_N > a.capc) ncand = fold(ncand);
-      const int ng = min(nsat - s0, (a.capc - ncand) / TC_N);  // >= 1 after the fold
-      if (tid == 0) s_misc[3] = 0u;
-      __syncthreads();
-      for (int i = tid; i < ng * TC_N; i += nt) {
-        const int cidx = sat[s0 + i / TC_N] * TC_N + i % TC_N;
-        if (cidx < a.V) {
-          const uint32_t kv = float_key(__ldcg(lg + cidx));
-          if (kv >= x) {
-            const int p = ncand + static_cast<int>(atomicAdd(&s_misc[3], 1u));
-            keys[p] = kv;
-            idx[p] = cidx;
+      uint32_t base = 0u;
+      if (lane == 31 && incl > 0) base = atomicAdd(&s_nc, static_cast<uint32_t>(incl));
+      int pos = static_cast<int>(__shfl_sync(0xffffffffu, base, 31)) + incl - tot;
+#pragma unroll
+      for (int r = 0; r < MERGE_LISTS_PB; ++r) {
+#pragma unroll
+        for (int e = 0; e < TC_LIST; ++e) {
+          if (e < c[r]) {
+            keys[pos] = composite_key(le[r][e]);
+            idx[pos] = composite_idx(le[r][e]);
+            ++pos;
           }
         }
       }
       __syncthreads();
-      ncand += static_cast<int>(s_misc[3]);
+      ncand = static_cast<int>(s_nc);
+    }
+
+    // ---- 4. saturated lists: scan their tiles' logits, as many tiles per pass as the buffer takes,
+    // MERGE_SCAN_PT loads in flight per thread
+    const int nsat = s_nsat;
+    for (int s0 = 0; s0 < nsat;) {
+      if (ncand + TC_N > a.capc) ncand = fold(ncand);
+      const int ng = min(nsat - s0, (a.capc - ncand) / TC_N);  // >= 1 after the fold
+      const int ne = ng * TC_N;
+      for (int i0 = 0; i0 < ne; i0 += nt * MERGE_SCAN_PT) {  // warp-uniform trip counts
+        uint32_t kv[MERGE_SCAN_PT];
+        int ci[MERGE_SCAN_PT];
+#pragma unroll
+        for (int u = 0; u < MERGE_SCAN_PT; ++u) {
+          const int i = i0 + u * nt + tid;
+          ci[u] = i < ne ? sat[s0 + i / TC_N] * TC_N + i % TC_N : a.V;
+          kv[u] = ci[u] < a.V ? float_key(__ldcg(lg + ci[u])) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < MERGE_SCAN_PT; ++u) {
+          const bool take = ci[u] < a.V && kv[u] >= x;
+          const uint32_t bt = __ballot_sync(0xffffffffu, take);
+          if (bt != 0u) {
+            uint32_t b0 = 0u;
+            if (lane == 0) b0 = atomicAdd(&s_nc, static_cast<uint32_t>(__popc(bt)));
+            b0 = __shfl_sync(0xffffffffu, b0, 0);
+            if (take) {
+              const int p = static_cast<int>(b0) + __popc(bt & lanemask_lt());
+              keys[p] = kv[u];
+              idx[p] = ci[u];
+            }
+          }
+        }
+      }
       __syncthreads();
+      ncand = static_cast<int>(s_nc);
       s0 += ng;
     }
 
-    // ---- 3. exact top K, sorted; tokens
+    // ---- 5. exact top K, sorted; tokens
     const int want = min(K, ncand);
     int nr = ncand;
     if (ncand > RANK_SORT_MAX && ncand <= 32 * MERGE_HEADS_PER_LANE) {
@@ -266,21 +281,20 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
 }  // namespace
 
 bool plan_merge(int K, int ntn, int dyn_max, int* capc, int* sortP, int* smem_bytes) {
+  const int nl = ntn * TC_LIST;
+  const bool heads_bound = ntn >= K && ntn <= 32 * MERGE_HEADS_PER_LANE;
   const int sp = next_pow2_host(K) > RANK_SORT_MAX ? next_pow2_host(K) : RANK_SORT_MAX;
-  const int fixed = ntn * TC_LIST * 4 + sp * 8 + K * 8 + K * 4 + (3 * ntn + 1) * 4;
-  // the candidate buffer holds the gathered elements and folds to the top K when full: sized for the
-  // usual few hundred (ties in groups of a few) with room for K plus one saturated tile, small enough
-  // for several rows' merges to share an SM
-  int want = 4 * K + TC_N;
-  if (want < 4096) want = 4096;  // room for ~20 rescanned tiles per pass
+  const int fixed = nl * 8 + (heads_bound ? 0 : nl * 4) + sp * 8 + K * 8 + K * 4 + ntn * 4;
+  // the candidate buffer: the gathered elements, folded to the top K before a gather batch or a
+  // saturated tile might not fit; sized for the usual few hundred with room for ~20 rescanned tiles
+  int want = 4096;
+  if (want < K + MERGE_THREADS * MERGE_LISTS_PB * TC_LIST) want = K + MERGE_THREADS * MERGE_LISTS_PB * TC_LIST;
+  if (want < 2 * K) want = 2 * K;
   want = (want + 3) & ~3;
-  int cap = (dyn_max - fixed) / 8;
-  cap &= ~3;
-  if (cap > want) cap = want;
-  if (cap < K + TC_N || cap < 2 * K) return false;
-  *capc = cap;
+  if (fixed + want * 8 > dyn_max) return false;
+  *capc = want;
   *sortP = sp;
-  *smem_bytes = fixed + cap * 8;
+  *smem_bytes = fixed + want * 8;
   return true;
 }
 
@@ -304,8 +318,9 @@ cudaError_t prepare_tc(int max_smem_optin, int* merge_dyn_max) {
   cudaFuncAttributes fa;
   e = cudaFuncGetAttributes(&fa, merge_lists_kernel);
   if (e != cudaSuccess) return e;
-  // at most half the opt-in limit, so two rows' merges share an SM
-  int dyn = (max_smem_optin - static_cast<int>(fa.sharedSizeBytes)) / 2 - 1024;
+  // the whole opt-in limit; at the GPT-OSS shape (1048 tiles, k = 256) a row takes ~111 KB, so two
+  // rows' merges still share an SM
+  int dyn = max_smem_optin - static_cast<int>(fa.sharedSizeBytes);
   e = cudaFuncSetAttribute(merge_lists_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
   *merge_dyn_max = dyn;

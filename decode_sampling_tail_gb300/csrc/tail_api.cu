@@ -378,6 +378,8 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   ma.capc = h->merge_capc;
   ma.sortP = h->merge_sortP;
   ma.smem_bytes = h->merge_smem;
+  ma.err = h->err;
+  ma.timeout_ns = h->wait_limit_ns;
   e = launch_merge(ma, gbs, stream, true);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch (merge)");
   if (ev) cudaEventRecord(ev[3], stream);

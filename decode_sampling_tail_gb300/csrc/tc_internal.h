@@ -60,6 +60,8 @@ struct MergeArgs {
   int32_t* tokens;         // [B] or null
   int B, V, K, ntn;
   int capc, sortP, smem_bytes;
+  int* err;                // device error flag (a bounded wait ran out)
+  uint64_t timeout_ns;
 };
 
 cudaError_t launch_split(const SplitArgs& a, cudaStream_t stream);
