@@ -303,6 +303,60 @@ def test_tensor_core_saturated_tiles_scan_the_logits(V):
     assert exact + exempt == w.B
 
 
+def _scale_columns(w, c0, c1, pow2):
+    """Multiplies W columns [c0, c1) by 2**pow2 (exact on bf16 values)."""
+    f = (w.w_t[:, c0:c1].astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** pow2)
+    w.w_t[:, c0:c1] = (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _slabs_hiding_top_k(logits, nslab, k):
+    """Per row, the slabs whose publication (every element >= the 8th largest of its 32 lane maxima,
+    none when more than 32 pass) may leave out a top-k element -- computed from the GPU's own fp32
+    logits the way the mma.sync path publishes them."""
+    B, V = logits.shape
+    npairs = V // 16
+    out = []
+    for r in range(B):
+        v = np.sort(logits[r])[::-1][k - 1]
+        hidden = 0
+        for c in range(nslab):
+            lo, hi = 16 * (npairs * c // nslab), 16 * (npairs * (c + 1) // nslab)
+            seg = logits[r, lo:hi]
+            lane_max = np.full(32, -np.inf, np.float32)
+            for lane in range(32):
+                if seg[lane::32].size:
+                    lane_max[lane] = seg[lane::32].max()
+            b = np.sort(lane_max)[::-1][7]
+            if np.count_nonzero(seg >= b) > 32 or b > v:
+                hidden += 1
+        out.append(hidden)
+    return np.array(out)
+
+
+@pytest.mark.parametrize("emit", [True, False], ids=["logits_out", "logits_scratch"])
+@pytest.mark.parametrize("case", ["clustered", "saturated"])
+def test_row_owner_rescans_slabs_that_may_hide_top_k(case, emit):
+    # top-k elements crowded into a few slabs: "clustered" scales 240 columns by 4, so one or two slabs
+    # hold most of a row's top 64 but publish only ~10; "saturated" repeats every column 64 times, so
+    # slabs hold more than 32 elements at their bound and publish none.  The row owner must rescan them.
+    if case == "clustered":
+        w = gen.custom(6, 128, 24576, 64, hidden_dtype="bf16", seed=93)
+        _scale_columns(w, 1600, 1840, 2)
+    else:
+        w = gen.custom(6, 128, 24576, 64, hidden_dtype="bf16", seed=94, dup_cols=64)
+    with make_tail(w, path="gemv") as t:
+        assert t.info.tc_min_rows == 0  # the mma.sync path
+        ref = tc.run_gpu(t, w, torch, emit=True)
+        res = ref if emit else tc.run_gpu(t, w, torch, emit=False)
+        nslab = t.info.nslab
+    assert np.all(_slabs_hiding_top_k(ref.logits, nslab, w.k) > 0)  # the inputs do force rescans
+    if not emit:
+        assert np.array_equal(res.topk_idx, ref.topk_idx) and np.array_equal(res.tokens, ref.tokens)
+        res.logits = ref.logits
+    exact, exempt = full_check(w, res)
+    assert exact + exempt == w.B
+
+
 def test_tensor_core_emit_off_matches_emit_on():
     w = gen.custom(40, 128, 8192, 128, hidden_dtype="bf16", seed=92)
     with make_tail(w) as t:
