@@ -70,6 +70,7 @@ struct GemvArgs {
   uint32_t* meta;           // [B][nslab][SLAB_META_WORDS] each slab's publication per row
   uint64_t* cand;           // [B][nslab][SLAB_CAND] published candidates as (key, id) composites
   unsigned long long* row_sync;  // [B]: slabs that have published the row; 0 between runs
+  unsigned long long* row_copy;  // [B]: slabs whose logits copy of the row is written; 0 between runs
   float* topk_val;          // [B][topk_ld] sorted top-k logits
   int32_t* topk_idx;        // [B][topk_ld] their vocabulary ids
   int64_t topk_ld;

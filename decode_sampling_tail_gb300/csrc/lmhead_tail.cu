@@ -246,6 +246,27 @@ __device__ __forceinline__ void own_rows(const GemvArgs& a, uint8_t* ring, int c
   uint32_t* s_cnt = reinterpret_cast<uint32_t*>(ebuf + a.K);  // slab counts, then the rescan list
   uint32_t* s_b = s_cnt + a.nslab;
   const int nflat = a.nslab * SLAB_CAND;
+  // rescans read the slabs' logits copies (written after the publications) unless the caller's logits
+  const bool copied = a.logits_in_smem && !a.logits_out;
+  auto wait_copies = [&](int row) {  // bounded wait until every slab's copy of the row is written
+    if (tid == 0) {
+      unsigned long long v = 0;
+      int ok = 1;
+      const uint64_t t0 = global_timer_ns();
+      while (true) {
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.row_copy + row) : "memory");
+        if (v >= static_cast<unsigned long long>(a.nslab)) break;
+        if (global_timer_ns() - t0 > a.timeout_ns) {
+          raise_error(a.err, DEV_TIMEOUT_BARRIER);
+          ok = 0;
+          break;
+        }
+      }
+      s_own[2] = ok ? 0u : 1u;
+    }
+    __syncthreads();
+    return s_own[2] == 0u;
+  };
   for (int row = c; row < a.B; row += a.nslab) {
     SampleParams prm = {};
     if (a.params != nullptr) prm = load_sample_params(a.params + static_cast<int64_t>(row) * a.ncols, a.ncols);
@@ -341,6 +362,7 @@ __device__ __forceinline__ void own_rows(const GemvArgs& a, uint8_t* ring, int c
     __syncthreads();
     const int nbad = static_cast<int>(s_own[3]);
     if (nbad > 0) {
+      if (copied && !wait_copies(row)) break;  // uniform: a copy never arrived (the error flag is raised)
       m = rescan_slabs(a, row, thr, nbad, s_cnt, s_b, keys, idx, comp, m, s_red, s_list, s_misc, s_own);
       want = rank_top(a, keys, idx, comp, sorted, m, s_red, s_list, s_misc);
     }
@@ -353,6 +375,10 @@ __device__ __forceinline__ void own_rows(const GemvArgs& a, uint8_t* ring, int c
       if (lane == 0) a.tokens[row] = tok;
     }
     __syncthreads();
+    if (copied) {  // every copy of the row has landed by now, normally: clear the word for the next run
+      if (!wait_copies(row)) break;
+      if (tid == 0) a.row_copy[row] = 0ull;
+    }
   }
 }
 
@@ -584,8 +610,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
             if (a.logits_out) *reinterpret_cast<float2*>(a.logits_out + r * a.logits_out_ld + col) = v;
             if (a.logits_in_smem)
               *reinterpret_cast<float2*>(slab_logits + r * max_cols + (col - pair_lo * 16)) = v;
-            // a global copy for the row owner's rescans (and for the slab scan when it is not in smem)
-            if (!a.logits_out || !a.logits_in_smem)
+            else  // the slab's logits live in global memory
               *reinterpret_cast<float2*>(a.logits_scratch + static_cast<int64_t>(r) * a.V + col) = v;
           }
         }
@@ -683,6 +708,21 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
 
 
   if (!aborted && warp < GEMV_CONSUMER_WARPS) publish_rows(s_args, slab_logits, max_cols, n, vbase, c);
+  if (!aborted && a.logits_in_smem && !a.logits_out) {
+    // a global copy of the slab's logits for the row owners' rescans, written after the publication
+    // so that its release does not wait for these stores; counted per row on its own word
+    const int n4 = n / 4;
+    for (int q = tid; q < a.B * n4; q += blockDim.x) {
+      const int r = q / n4, i = q - r * n4;
+      reinterpret_cast<float4*>(a.logits_scratch + static_cast<int64_t>(r) * a.V + vbase)[i] =
+          reinterpret_cast<const float4*>(slab_logits + r * max_cols)[i];
+    }
+    __syncthreads();
+    if (tid < a.B) {
+      __threadfence();
+      asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(a.row_copy + tid), "l"(1ull) : "memory");
+    }
+  }
   if (!aborted) own_rows(s_args, ring, c, s_red, s_list, s_misc, s_own);
   pdl_launch_dependents();
 }

@@ -102,8 +102,8 @@ Layout layout_for(const GemvPlan& plan, int B, int H, int V, int K, int nslab, b
   size_t o = 0;
   L.err = 8;
   o = 256;
-  L.rsync = o;
-  o += up256(static_cast<size_t>(B) * 8);
+  L.rsync = o;  // arrivals [B], then copies [B]
+  o += up256(static_cast<size_t>(B) * 16);
   L.apack = o;
   o += up256(static_cast<size_t>(H / KSTEP) * plan.mt * APACK_TILE_BYTES);
   L.row_scale = o;
@@ -242,6 +242,7 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
     ga.meta = reinterpret_cast<uint32_t*>(base + L.meta);
     ga.cand = reinterpret_cast<uint64_t*>(base + L.cand);
     ga.row_sync = reinterpret_cast<unsigned long long*>(base + L.rsync);
+    ga.row_copy = ga.row_sync + B;
     ga.topk_val = reinterpret_cast<float*>(base + L.tkv);
     ga.topk_idx = reinterpret_cast<int32_t*>(base + L.tki);
     ga.topk_ld = K;

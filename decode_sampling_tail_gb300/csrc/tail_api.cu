@@ -266,7 +266,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   e = e ? e : dalloc(&h->cand, static_cast<size_t>(R) * h->nslab * SLAB_CAND, &tot);
   e = e ? e : dalloc(&h->logit_scratch, static_cast<size_t>(R) * cfg->V, &tot);
   e = e ? e : dalloc(&h->meta, static_cast<size_t>(R) * h->nslab * SLAB_META_WORDS, &tot);
-  e = e ? e : dalloc(&h->row_sync, static_cast<size_t>(R), &tot);
+  e = e ? e : dalloc(&h->row_sync, static_cast<size_t>(2 * R), &tot);  // arrivals, then copies
   e = e ? e : dalloc(&h->topk_val, static_cast<size_t>(cfg->gbs_max) * K, &tot);
   e = e ? e : dalloc(&h->topk_idx, static_cast<size_t>(cfg->gbs_max) * K, &tot);
   e = e ? e : dalloc(&h->err, 1, &tot);
@@ -285,7 +285,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
       e = cudaMemset(h->tc_act, 0, static_cast<size_t>(tc_act_rows(cfg->gbs_max)) * cfg->H * sizeof(uint16_t));
   }
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
-  if (e == cudaSuccess && R > 0) e = cudaMemset(h->row_sync, 0, static_cast<size_t>(R) * sizeof(unsigned long long));
+  if (e == cudaSuccess && R > 0) e = cudaMemset(h->row_sync, 0, static_cast<size_t>(2 * R) * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(h->apack, 0, ksteps * mt_max * APACK_TILE_BYTES);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -462,6 +462,7 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     ga.smem_bytes = plan.smem_bytes;
     ga.meta = h->meta;
     ga.row_sync = h->row_sync;
+    ga.row_copy = h->row_sync + h->rows_pass;
     ga.topk_val = (out_topk_vals ? out_topk_vals : h->topk_val) + static_cast<int64_t>(r0) * K;
     ga.topk_idx = (out_topk_idx ? out_topk_idx : h->topk_idx) + static_cast<int64_t>(r0) * K;
     ga.topk_ld = K;
@@ -585,7 +586,7 @@ int tail_check(tail_t* h) {
   if (flag != 0) {
     cudaMemset(h->err, 0, sizeof(int));
     // a wait that ran out leaves the per-row arrival words of the interrupted run behind
-    if (h->rows_pass > 0) cudaMemset(h->row_sync, 0, static_cast<size_t>(h->rows_pass) * sizeof(unsigned long long));
+    if (h->rows_pass > 0) cudaMemset(h->row_sync, 0, static_cast<size_t>(2 * h->rows_pass) * sizeof(unsigned long long));
     cudaDeviceSynchronize();
     return TAIL_ERR_DEVICE;
   }

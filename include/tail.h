@@ -179,7 +179,7 @@ int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const 
  *                  bounded device wait that ran out, in which case the
  *                  outputs are undefined.
  * Size limit: one pass of B rows needs, each part rounded up to 256 bytes,
- * 256 (error word) + 8 * B (per-row arrival words)
+ * 256 (error word) + 16 * B (per-row arrival and copy words)
  * + 32 * H * mt (activation pack; mt = 1,
  * 2, 4 or 8 for B up to 8, 16, 32, 64) + 32 * mt (row scales)
  * + 32 * B * nslab (per-slab publications) + 256 * B * nslab (published
