@@ -342,7 +342,7 @@ def main():
     tc_path = t.info.tc_min_rows > 0 and w.B >= t.info.tc_min_rows
     if tc_path:  # split -> tensor-core lm_head -> merge + sampler, one pass
         passes, launches_per_step, kernel = 1, 3, "lmhead_tc_kernel"
-    else:        # [rms_rows ->] cooperative lm_head + top-k + sampler, per pass
+    else:        # [rms_rows ->] lm_head + top-k + sampler in one launch, per pass
         passes = (w.B + t.info.rows_per_pass - 1) // t.info.rows_per_pass
         launches_per_step, kernel = t.info.kernels_per_run * passes, "lmhead_tail_kernel"
 

@@ -18,7 +18,7 @@ enum DeviceError : int {
   DEV_TIMEOUT_FULL = 1,   // consumer waited too long for a stage to land
   DEV_TIMEOUT_EMPTY = 2,  // producer waited too long for a stage to be released
   DEV_TIMEOUT_DRAIN = 3,  // copies still in flight when an aborting CTA left
-  DEV_TIMEOUT_BARRIER = 4,  // a CTA waited too long at the grid barrier
+  DEV_TIMEOUT_BARRIER = 4,  // a row owner waited too long for the slabs' publications (or copies)
 };
 
 __device__ __forceinline__ void raise_error(int* flag, int code) {

@@ -390,9 +390,6 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
   __shared__ uint32_t s_misc[4];
   __shared__ uint32_t s_own[4];  // owner: x, |F|, wait failed, slabs to rescan
   __shared__ float s_scale[MAX_ROWS_PER_PASS];  // fused: the rows' rstd
-  // the post-stream phases read their arguments from here: fields first touched after the long
-  // stream would otherwise miss the constant cache one line at a time
-  __shared__ __align__(16) GemvArgs s_args;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + MAX_STAGES);
@@ -422,7 +419,6 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
       mbar_init(empty0 + 8 * s, GEMV_CONSUMER_WARPS);
     }
     mbar_init(scale_bar, 1);
-    s_args = a;
     *s_abort = 0;
     *s_consumed_min = total;
     *s_issued = 0;
@@ -582,7 +578,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
     }
   } else {
     // ================================================================ consumers
-    pdl_wait();  // row_scale is read and outputs are written only after the RMSNorm kernel
+    pdl_wait();  // row_scale (RMSNorm kernel) is read and outputs are written only after the previous kernel
     const int g = lane >> 2, tq = lane & 3;
     const int mi = lane >> 3;  // ldmatrix: this lane addresses a row of matrix mi
     const uint32_t lrow_off = static_cast<uint32_t>(((mi & 1) * 8 + (lane & 7)) * a.pitch + (mi >> 1) * 16);
@@ -707,7 +703,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
   const int64_t vbase = pair_lo * 16;
 
 
-  if (!aborted && warp < GEMV_CONSUMER_WARPS) publish_rows(s_args, slab_logits, max_cols, n, vbase, c);
+  if (!aborted && warp < GEMV_CONSUMER_WARPS) publish_rows(a, slab_logits, max_cols, n, vbase, c);
   if (!aborted && a.logits_in_smem && !a.logits_out) {
     // a global copy of the slab's logits for the row owners' rescans, written after the publication
     // so that its release does not wait for these stores; counted per row on its own word
@@ -723,7 +719,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
       asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(a.row_copy + tid), "l"(1ull) : "memory");
     }
   }
-  if (!aborted) own_rows(s_args, ring, c, s_red, s_list, s_misc, s_own);
+  if (!aborted) own_rows(a, ring, c, s_red, s_list, s_misc, s_own);
   pdl_launch_dependents();
 }
 

@@ -27,7 +27,7 @@ def make_tail(w, gbs_max=None, **kw):
 
 @pytest.fixture(params=["gemv", "tensor"])
 def path(request):
-    """The lm_head realisation a small-batch test runs on: the cooperative mma.sync kernel, or the
+    """The lm_head realisation a small-batch test runs on: the mma.sync kernel, or the
     tensor-core path that narrow vocabularies take for every batch size."""
     return request.param
 
