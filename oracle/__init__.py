@@ -76,6 +76,9 @@ def lib():
             L.oracle_sample_row.argtypes = [P, P, i32, P, i32, P, P, P, P, P]
             L.oracle_tail.argtypes = [P, i32, P, P, i32, i32, i32, i32, i32, f32, i32, P, i32,
                                       i32, P, P, P, P]
+            L.oracle_f32_to_bf16_rne.argtypes = [f32]
+            L.oracle_f32_to_bf16_rne.restype = ctypes.c_uint16
+            L.oracle_moe_combine.argtypes = [P, P, i32, i32, P, i32, i32, P]
             _lib = L
     return _lib
 
@@ -191,3 +194,27 @@ def tail(hidden, dtype, gamma, w_t, Hu, k, eps, zero_pad, params=None, nthreads=
     if rc:
         raise ValueError(f"oracle_tail failed: {rc}")
     return L, tv, ti, (toks if params is not None else None)
+
+
+def f32_to_bf16(v: float) -> int:
+    """bf16 bits of an fp32 value, rounded to nearest, ties to even."""
+    return int(lib().oracle_f32_to_bf16_rne(ctypes.c_float(v)))
+
+
+def moe_combine(x_bits: np.ndarray, slots: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """The tail's producer step: h = bf16(x + bf16(fp32 fma chain of w[s] * slots[s] over s = 0, 1, ...)).
+
+    x_bits [B, H] bf16 bits; slots [B, S, H] float32, or uint16 bf16 bits; w [B, S] float32.
+    Returns h [B, H] as bf16 bits."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    B, H = x.shape
+    y = np.ascontiguousarray(slots)
+    S = y.shape[1] if y.ndim == 3 else 0
+    sd = DTYPE_CODES["f32"] if y.dtype == np.float32 else DTYPE_CODES["bf16"]
+    wt = np.ascontiguousarray(w, dtype=np.float32).reshape(B, S)
+    h = np.empty((B, H), np.uint16)
+    rc = lib().oracle_moe_combine(_ptr(x), _ptr(y) if S else None, sd, S, _ptr(wt) if S else None, B, H, _ptr(h))
+    if rc:
+        raise ValueError(f"oracle_moe_combine failed: {rc}")
+    return h
+

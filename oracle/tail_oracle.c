@@ -20,6 +20,12 @@
  *   top-k      = first k of all V columns sorted by (logit desc, index asc)
  *   sampler    = temperature, top-k, softmax, top-p, inverse-CDF draw
  * No blocking, fusion or reordering beyond what these definitions state.
+ *
+ * One producer step may precede the tail: the MoE combine and residual add
+ * that forms the bf16 hidden state ("[WIP] Nemotron RMSNorm ... review",
+ * tf_moe_add_rms_rows_bf16h; oracle_moe_combine below).  Its precision is
+ * fixed by that page (fp32 fmas, bf16 roundings), so it is evaluated in
+ * exactly those operations, not in double precision.
  */
 #include <math.h>
 #include <pthread.h>
@@ -400,3 +406,58 @@ int oracle_tail(const void *x, int dtype, const float *gamma, const uint16_t *w_
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * MoE combine + residual add (the tail's producer).  Page: the Nemotron
+ * RMSNorm review thread, entry tf_moe_add_rms_rows_bf16h (and its contract
+ * kinds moe_bf16_h / moe_f32_h): for every hidden lane, the expert slots are
+ * summed in slot order from 0 with fp32 fused multiply-adds, the sum is
+ * rounded to bf16, added to the bf16 residual x in fp32, and the result is
+ * rounded to bf16 -- the hidden state h that the final RMSNorm reads.
+ *   x     [B, H]      bf16 residual
+ *   slots [B, S, H]   expert outputs, fp32 (OR_F32) or bf16 (OR_BF16)
+ *   w     [B, S]      fp32 slot weights
+ *   h     [B, H]      bf16 output
+ * The fp32 fma is C99's fmaf (one rounding); bf16 rounding is to nearest,
+ * ties to even, NaN kept NaN.
+ * ------------------------------------------------------------------------- */
+
+static float bits_to_float(uint32_t u) {
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* round an fp32 value to bf16 bits: nearest, ties to even */
+uint16_t oracle_f32_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x40u); /* NaN */
+    const uint32_t lower = u & 0xffffu;
+    uint32_t upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+    return (uint16_t)upper;
+}
+
+int oracle_moe_combine(const uint16_t *x, const void *slots, int slot_dtype, int S, const float *w, int B,
+                       int H, uint16_t *h) {
+    if (B < 0 || H < 0 || S < 0 || (S > 0 && (!slots || !w)) || (slot_dtype != OR_F32 && slot_dtype != OR_BF16))
+        return -1;
+    for (int b = 0; b < B; ++b) {
+        for (int j = 0; j < H; ++j) {
+            float acc = 0.0f;
+            for (int s = 0; s < S; ++s) {
+                const int64_t e = ((int64_t)b * S + s) * H + j;
+                const float y = slot_dtype == OR_F32 ? ((const float *)slots)[e]
+                                                     : bits_to_float(((uint32_t)((const uint16_t *)slots)[e]) << 16);
+                acc = fmaf(w[(int64_t)b * S + s], y, acc);
+            }
+            const float d = bits_to_float(((uint32_t)oracle_f32_to_bf16_rne(acc)) << 16);
+            const float xv = bits_to_float(((uint32_t)x[(int64_t)b * H + j]) << 16);
+            const float sum = xv + d;
+            h[(int64_t)b * H + j] = oracle_f32_to_bf16_rne(sum);
+        }
+    }
+    return 0;
+}
+

@@ -11,6 +11,7 @@ import subprocess
 import pytest
 
 import oracle
+import tests.test_oracle_moe as moe
 import tests.test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "tail_oracle.c")
@@ -49,7 +50,26 @@ MUTANTS = [
      [pins.test_widen_bf16_exhaustive]),
     ("f16_subnormal_scale", "ldexp((double)f, -24)", "ldexp((double)f, -25)",
      [pins.test_widen_f16_exhaustive_against_numpy]),
+    # the producer step (MoE combine + residual add)
+    ("combine_not_rounded_before_add",
+     "const float d = bits_to_float(((uint32_t)oracle_f32_to_bf16_rne(acc)) << 16);", "const float d = acc;",
+     [lambda: _moe_golden("round_first")]),
+    ("combine_slots_reversed", "for (int s = 0; s < S; ++s) {", "for (int s = S - 1; s >= 0; --s) {",
+     [lambda: _moe_golden("slot_order")]),
+    ("combine_slot_index_transposed", "((int64_t)b * S + s) * H + j", "((int64_t)s * B + b) * H + j",
+     [lambda: moe.test_moe_combine_exact_sums_match_numpy("f32")]),
+    ("bf16_truncates", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;", "",
+     [moe.test_bf16_rounding_is_nearest_ties_to_even]),
+    ("bf16_ties_away", "(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)",
+     [moe.test_bf16_rounding_is_nearest_ties_to_even]),
 ]
+
+
+def _moe_golden(name):
+    for case in moe._golden_cases():
+        if case[0] == name:
+            return moe.test_moe_combine_hand_worked(case)
+    raise KeyError(name)
 
 
 def _golden(name):
