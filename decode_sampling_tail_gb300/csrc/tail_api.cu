@@ -520,6 +520,44 @@ int tail_run_ex(tail_t* h, const void* hidden, const float* gamma, const uint16_
                   out_topk_vals_opt, out_topk_idx_opt, static_cast<cudaStream_t>(stream));
 }
 
+int tail_run_moe(tail_t* h, const uint16_t* residual, const void* slots, int32_t slot_dtype, int32_t nslots,
+                 const float* slot_w, const float* gamma, const uint16_t* w_t, const float* params,
+                 int32_t n_param_cols, int32_t gbs, int32_t* out_tokens, float* out_logits_opt,
+                 float* out_topk_vals_opt, int32_t* out_topk_idx_opt, uint16_t* out_hidden_opt, void* stream) {
+  if (!h) return TAIL_ERR_INVALID_ARG;
+  if (h->cfg.hidden_dtype != TAIL_BF16) return TAIL_ERR_UNSUPPORTED;  // the residual stream is bf16
+  if (nslots < 0 || nslots > TAIL_MOE_MAX_SLOTS || (slot_dtype != TAIL_F32 && slot_dtype != TAIL_BF16))
+    return TAIL_ERR_INVALID_ARG;
+  if (nslots > 0 && (!slots || !slot_w || !aligned(slots, 4) || !aligned(slot_w, 4))) return TAIL_ERR_INVALID_ARG;
+  if (out_hidden_opt && !aligned(out_hidden_opt, 16)) return TAIL_ERR_INVALID_ARG;
+  int rc = validate_run(h, residual, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt,
+                        out_topk_vals_opt, out_topk_idx_opt);
+  if (rc || gbs == 0) return rc;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return TAIL_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // h lands in the caller's buffer, else in the handle's hidden staging (gbs_max x H bf16)
+  uint16_t* hb = out_hidden_opt ? out_hidden_opt : reinterpret_cast<uint16_t*>(h->st_hidden);
+  MoeArgs ma;
+  ma.x = residual;
+  ma.slots = slots;
+  ma.slot_dtype = slot_dtype == TAIL_F32 ? 0 : 2;
+  ma.w = slot_w;
+  ma.h = hb;
+  ma.B = gbs;
+  ma.H = h->cfg.H;
+  ma.S = nslots;
+  cudaError_t e = launch_moe_combine(ma, s, h->pdl_ok != 0);
+  if (e != cudaSuccess && h->pdl_ok) {  // this runtime refuses programmatic serialization
+    cudaGetLastError();
+    h->pdl_ok = 0;
+    e = launch_moe_combine(ma, s, false);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "tail_run_moe: kernel launch");
+  return run_impl(h, hb, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, out_topk_vals_opt,
+                  out_topk_idx_opt, s);
+}
+
 int tail_run(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
              int32_t n_param_cols, int32_t gbs, int32_t* out_tokens, float* out_logits_opt, void* stream) {
   return tail_run_ex(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, nullptr,

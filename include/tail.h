@@ -143,6 +143,35 @@ int tail_run_ex(tail_t* h, const void* hidden, const float* gamma, const uint16_
                 void* stream);
 
 /*
+ * The tail fused with its producer: the MoE combine and residual add that form
+ * the bf16 hidden state ("nemotron CUDA: RMSNorm rows run on the shared norms
+ * and combine (#548, step 1)", TensorFold pull request #1353, section "What
+ * moves", entry tf_nemo_add_moe_norm / tf_moe_add_rms_rows_bf16h; "GPT-OSS
+ * Tail Chunked Megakernel Kernel API
+ * Reference", parameter `hidden_states`: a 16-bit producer output feeds the
+ * norm directly).  For every row b and hidden lane j:
+ *   acc = 0;  acc = fp32 fma(slot_w[b][s], slots[b][s][j], acc) for s = 0 .. nslots-1
+ *   h[b][j] = bf16(residual[b][j] + bf16(acc))     (bf16: nearest, ties to even)
+ * then the tail of tail_run_ex on h.  Requires cfg.hidden_dtype == TAIL_BF16.
+ *   residual       [gbs, H] bf16 bit patterns, 16-byte aligned.
+ *   slots          [gbs, nslots, H] expert outputs, fp32 (slot_dtype TAIL_F32) or bf16
+ *                  bit patterns (TAIL_BF16), 4-byte aligned; may be NULL when nslots == 0.
+ *   nslots         0 .. TAIL_MOE_MAX_SLOTS (8 for Nemotron: 6 routed + 2 shared).
+ *   slot_w         [gbs, nslots] fp32 weights, 4-byte aligned.
+ *   out_hidden_opt [gbs, H] bf16 h, 16-byte aligned, or NULL (h then stays in the
+ *                  handle's scratch).
+ * The other arguments are those of tail_run_ex.  Two launches (the combine,
+ * then the tail) chained with programmatic dependent launch.  Returns
+ * TAIL_ERR_UNSUPPORTED for a non-bf16 config, TAIL_ERR_INVALID_ARG for bad
+ * pointers, alignment, sizes or slot dtype.
+ */
+#define TAIL_MOE_MAX_SLOTS 256
+int tail_run_moe(tail_t* h, const uint16_t* residual, const void* slots, int32_t slot_dtype, int32_t nslots,
+                 const float* slot_w, const float* gamma, const uint16_t* w_t, const float* params,
+                 int32_t n_param_cols, int32_t gbs, int32_t* out_tokens, float* out_logits_opt,
+                 float* out_topk_vals_opt, int32_t* out_topk_idx_opt, uint16_t* out_hidden_opt, void* stream);
+
+/*
  * End-to-end form for callers holding the per-step inputs in host memory:
  * copies hidden_host [gbs, H] and params_host [gbs, n_param_cols] into
  * handle-owned device staging, runs the tail on `stream`, copies the tokens

@@ -22,8 +22,9 @@
  * No blocking, fusion or reordering beyond what these definitions state.
  *
  * One producer step may precede the tail: the MoE combine and residual add
- * that forms the bf16 hidden state ("[WIP] Nemotron RMSNorm ... review",
- * tf_moe_add_rms_rows_bf16h; oracle_moe_combine below).  Its precision is
+ * that forms the bf16 hidden state ("nemotron CUDA: RMSNorm rows run on the
+ * shared norms and combine (#548, step 1)", TensorFold pull request #1353,
+ * entry tf_nemo_add_moe_norm; oracle_moe_combine below).  Its precision is
  * fixed by that page (fp32 fmas, bf16 roundings), so it is evaluated in
  * exactly those operations, not in double precision.
  */
@@ -408,9 +409,10 @@ int oracle_tail(const void *x, int dtype, const float *gamma, const uint16_t *w_
 }
 
 /* ---------------------------------------------------------------------------
- * MoE combine + residual add (the tail's producer).  Page: the Nemotron
- * RMSNorm review thread, entry tf_moe_add_rms_rows_bf16h (and its contract
- * kinds moe_bf16_h / moe_f32_h): for every hidden lane, the expert slots are
+ * MoE combine + residual add (the tail's producer).  Page: "nemotron CUDA:
+ * RMSNorm rows run on the shared norms and combine (#548, step 1)" (TensorFold
+ * pull request #1353), section "What moves", entry tf_nemo_add_moe_norm, and
+ * the contract kinds moe_bf16_h / moe_f32_h: for every hidden lane, the expert slots are
  * summed in slot order from 0 with fp32 fused multiply-adds, the sum is
  * rounded to bf16, added to the bf16 residual x in fp32, and the result is
  * rounded to bf16 -- the hidden state h that the final RMSNorm reads.

@@ -1,6 +1,7 @@
 """Pins of the oracle's producer step, the MoE combine + residual add (CPU only).
 
-The step ("Nemotron RMSNorm review", tf_moe_add_rms_rows_bf16h): per hidden
+The step ("nemotron CUDA: RMSNorm rows run on the shared norms and combine
+(#548, step 1)", TensorFold pull request #1353, entry tf_nemo_add_moe_norm): per hidden
 lane, an fp32 fma chain over the expert slots in slot order from 0, rounded to
 bf16, added to the bf16 residual and rounded to bf16.  The pins below do not
 restate that formula: hand-worked values (tests/golden/moe_combine_cases.txt,
