@@ -53,6 +53,9 @@ def parse():
                     help="sampling_params columns: 4 (explicit u), 3 (u = 0.5), none (no sampler)")
     ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tensor"],
                     help="lm_head realisation: auto (by vocabulary width), mma.sync up to 8 rows, or tensor cores")
+    ap.add_argument("--moe-slots", type=int, default=0,
+                    help="time tail_run_moe: the hidden state formed from the residual and this many fp32 "
+                         "expert slots (the producer step) inside each step; 0 = off")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -349,6 +352,18 @@ def main():
     def step():
         t.run(hidden, gamma, w_t, params, out_tokens=tokens, out_logits=logits, stream=stream)
 
+    if args.moe_slots > 0:  # the producer step inside every step: hidden = bf16(residual + bf16(combine))
+        if w.hidden_dtype != "bf16":
+            raise SystemExit("--moe-slots needs a bf16 workload (the residual stream is bf16)")
+        grng = np.random.default_rng(w.seed + 777)
+        m_slots = torch.from_numpy((grng.standard_normal((w.B, args.moe_slots, w.H)) * 0.5).astype(np.float32)).to(dev)
+        m_w = torch.from_numpy(grng.uniform(0.1, 1.0, (w.B, args.moe_slots)).astype(np.float32)).to(dev)
+
+        def step():  # noqa: F811
+            t.run_moe(hidden, m_slots, m_w, gamma, w_t, params, out_tokens=tokens, out_logits=logits, stream=stream)
+
+        launches_per_step += 1  # the combine kernel
+
     # a weight at least twice the L2 streams from HBM every step by itself; a smaller one is flushed
     # from L2 between timed steps
     flush_buf = None
@@ -431,7 +446,8 @@ def main():
 
     # ---------------- end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e and params is not None:  # without the sampler a step returns no tokens to read back
+    # without the sampler a step returns no tokens to read back; the host entry point has no producer step
+    if not args.no_e2e and params is not None and args.moe_slots == 0:
         hid_h = torch.from_numpy(np.ascontiguousarray(w.hidden.view(np.int16) if w.hidden_dtype != "f32"
                                                       else w.hidden)).pin_memory()
         ncols = int(params.shape[1])
@@ -465,6 +481,8 @@ def main():
 
     pk, pk_kind = peaks()
     ab = algorithmic_bytes(w, emit)
+    if args.moe_slots > 0:  # the slots and their weights are read once per step as well
+        ab["step"] += w.B * args.moe_slots * (w.H * 4 + 4)
     lm_bytes = ab["lm_head"] if passes == 1 else 2 * w.H * w.V + (4 * (w.B // passes) * w.V if emit else 0)
     achieved = lm_bytes / (lm_ms / 1e3) / 1e9
     step_gbs = ab["step"] / (ms_step / 1e3) / 1e9
@@ -504,6 +522,8 @@ def main():
                           f"no flush: the {2 * w.H * w.V / 1e9:.2f} GB weight is larger than L2 and streams "
                           "from HBM every step"),
                    "lm_head_path": "tensor" if tc_path else "mma.sync",
+                   "producer": (f"MoE combine + residual add, {args.moe_slots} fp32 slots (tail_run_moe)"
+                                if args.moe_slots > 0 else "none"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "step_hbm_gbs": step_gbs,
         "step_frac_of_spec_8tbs": step_gbs / SPEC_HBM_GBS,
