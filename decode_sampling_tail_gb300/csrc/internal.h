@@ -93,17 +93,6 @@ struct GemvArgs {
   int drop_iter;            // test hook: ring iteration the producer never issues (-1: none)
 };
 
-// The producer step (MoE combine + residual add) that forms the bf16 hidden state.
-struct MoeArgs {
-  const uint16_t* x;        // [B][H] bf16 residual
-  const void* slots;        // [B][S][H] expert outputs, fp32 (slot_dtype 0) or bf16 (2)
-  int slot_dtype;
-  const float* w;           // [B][S] slot weights
-  uint16_t* h;              // [B][H] bf16 hidden state (4-byte aligned)
-  int B, H, S;
-};
-cudaError_t launch_moe_combine(const MoeArgs& a, cudaStream_t stream, bool pdl);
-
 // Launchers (all enqueue on `stream`; the lm_head tail is one launch,
 // chained to the previous kernel on the stream with programmatic dependent launch when pdl).
 cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream);

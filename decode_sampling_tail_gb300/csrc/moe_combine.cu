@@ -11,6 +11,7 @@
 // first kernel with programmatic dependent launch.
 #include "common.cuh"
 #include "internal.h"
+#include "moe_internal.h"
 
 namespace tail {
 

@@ -17,6 +17,7 @@
 #include "../../include/tail.h"
 #include "abi_common.h"
 #include "internal.h"
+#include "moe_internal.h"
 #include "tc_internal.h"
 
 using namespace tail;
