@@ -76,6 +76,30 @@ def test_small_shapes_match_oracle(shape, path):
     assert exact + exempt == B and exact >= B - max(1, B // 8)
 
 
+# odd k-step counts on the one-launch mma.sync path: the last ring stage holds a single k-step, so half
+# of the activation warp's lanes sit it out; with and without lanes beyond hidden_actual, both forms
+ODD_KSTEPS = [
+    # B, H, V, k, dtype, Hu, zero_pad
+    (4, 80, 2400, 24, "bf16", None, 1),    # 5 k-steps
+    (8, 112, 4096, 64, "f16", 100, 0),     # 7 k-steps, lanes [100, 112) ignored
+    (3, 208, 1600, 40, "f32", 200, 1),     # 13 k-steps, zero pads
+]
+
+
+@pytest.mark.parametrize("deferred", [True, False], ids=["deferred", "legacy"])
+@pytest.mark.parametrize("shape", ODD_KSTEPS, ids=lambda s: f"B{s[0]}_H{s[1]}_V{s[2]}_k{s[3]}_{s[4]}")
+def test_odd_kstep_counts_on_the_mma_sync_path(shape, deferred):
+    B, H, V, k, dt, Hu, zp = shape
+    w = gen.custom(B, H, V, k, hidden_dtype=dt, Hu=Hu, zero_pad=zp, seed=2000 + H)
+    if Hu is not None and not zp:
+        w.hidden[:, Hu:] = 3.0 if dt == "f32" else 0x4040  # garbage beyond hidden_actual is ignored
+    with make_tail(w, path="gemv", deferred_rms=deferred) as t:
+        assert t.info.tc_min_rows == 0 and t.info.kernels_per_run == (1 if deferred else 2)
+        res = tc.run_gpu(t, w, torch)
+    exact, exempt = full_check(w, res)
+    assert exact + exempt == B
+
+
 @pytest.mark.parametrize("ncols", ["3col", "none"])
 def test_param_column_forms(ncols, path):
     w = gen.custom(6, 64, 2048, 32, hidden_dtype="bf16", seed=77)
