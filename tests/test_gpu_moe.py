@@ -76,6 +76,21 @@ def test_producer_fused_tail_matches_oracle(slot_dtype, path):
     assert exact + exempt == w.B
 
 
+def test_producer_step_with_many_slots():
+    # 40 slots of small weights (the kernel's fma chain runs over a runtime slot count)
+    w = gen.custom(4, 128, 4096, 16, hidden_dtype="bf16", seed=307)
+    rng = np.random.default_rng(308)
+    y = (rng.standard_normal((w.B, 40, w.H)) * 0.25).astype(np.float32)
+    wts = rng.uniform(0.0, 0.2, (w.B, 40)).astype(np.float32)
+    h_ref = oracle.moe_combine(w.hidden, y, wts)
+    with make_tail(w, path="gemv") as t:
+        res, h_gpu = _run_moe(t, w, y, wts)
+        plain = tc.run_gpu(t, dataclasses.replace(w, hidden=h_ref), torch)
+    assert np.array_equal(h_gpu, h_ref)
+    assert np.array_equal(res.logits.view(np.uint32), plain.logits.view(np.uint32))
+    assert np.array_equal(res.tokens, plain.tokens)
+
+
 def test_producer_fused_tail_gptoss_g8():
     # the bench's shape: gbs=8, H=2880, V=201088, k=256, one launch of the tail after the combine
     w = gen.custom(8, 2880, 201088, 256, hidden_dtype="bf16", seed=303)
