@@ -414,6 +414,32 @@ def main():
     ms_step = total_ms / args.steps
     rows_s = job_rows_per_s(w.B, args.steps, world, total_ms)
 
+    # ---------------- the same steps replayed from a CUDA graph of 10 (launch gaps stripped; not the headline)
+    graph = None
+    if flush_buf is None:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                step()  # warm state on the capture stream
+                torch.cuda.synchronize(dev)
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(10):
+                        step()
+                g.replay()
+                torch.cuda.synchronize(dev)
+                ge0, ge1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = max(1, args.steps // 10)
+                ge0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                ge1.record(stream)
+            torch.cuda.synchronize(dev)
+            graph = {"us_per_step": 1e3 * ge0.elapsed_time(ge1) / (10 * reps), "steps_per_graph": 10,
+                     "replays": reps}
+            t.check()
+        except Exception as e:  # noqa: BLE001  (a runtime that refuses the capture: report, don't fail)
+            graph = {"error": str(e)[:160]}
+
     # ---------------- spread of single steps (own loop, events around each step; not the headline)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * min(args.steps, 50))]
     with torch.cuda.stream(stream):
@@ -511,6 +537,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
         "single_step_us_p10": 1e3 * float(np.percentile(per_step, 10)),
         "single_step_us_p90": 1e3 * float(np.percentile(per_step, 90)),
+        "cuda_graph": graph,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generators, distributions of the named workload)",
         "config": {"workload": w.name, "gbs": w.B, "H": w.H, "hidden_actual": w.Hu, "V": w.V, "k": w.k,
