@@ -42,7 +42,7 @@ typedef enum { TAIL_F32 = 0, TAIL_F16 = 1, TAIL_BF16 = 2 } tail_dtype;
 typedef enum {
   TAIL_OK = 0,
   TAIL_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, bad size, gbs > gbs_max, bad n_param_cols */
-  TAIL_ERR_UNSUPPORTED = -2,  /* shape, dtype or device this build cannot run: caller falls back */
+  TAIL_ERR_UNSUPPORTED = -2,  /* shape, dtype or device the library cannot run: caller falls back */
   TAIL_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
   TAIL_ERR_OOM = -4,          /* scratch allocation failed at create */
   TAIL_ERR_DEVICE = -5        /* a kernel raised its error flag (a bounded wait ran out) */
