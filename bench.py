@@ -181,10 +181,10 @@ def job_rows_per_s(rows_per_rank_step: int, steps: int, world: int, job_ms: floa
     return rows_per_rank_step * steps * world / (job_ms / 1e3)
 
 
-def cpu_oracle_step(w, nthreads):
-    """One oracle pass over the workload's first min(B, CPU_SAMPLE_ROWS) rows; returns the rows done."""
+def cpu_oracle_step(w, nthreads, max_rows=CPU_SAMPLE_ROWS):
+    """One oracle pass over the workload's first min(B, max_rows) rows; returns the rows done."""
     import oracle
-    n = min(w.B, CPU_SAMPLE_ROWS)
+    n = min(w.B, max_rows)
     oracle.tail(w.hidden[:n], w.hidden_dtype, w.gamma, w.w_t, w.Hu, w.k, w.eps, w.zero_pad, w.params[:n],
                 nthreads=nthreads)
     return n
@@ -203,9 +203,15 @@ def cpu_baseline(w, budget_s=12.0, max_steps=20):
         times.append(time.perf_counter() - t0)
     sec = statistics.median(times)
     what = "whole steps" if rows == w.B else f"passes over the first {rows} of its {w.B} rows"
+    # the same oracle on one thread: one pass over at most 8 rows (a few seconds at V=201088)
+    t0 = time.perf_counter()
+    rows1 = cpu_oracle_step(w, 1, max_rows=8)
+    sec1 = time.perf_counter() - t0
     return {"value": rows / sec, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
             "us_per_step": sec * 1e6 * w.B / rows,
-            "sample": f"{len(times)} {what} of the {w.name} workload (V={w.V}), median"}
+            "sample": f"{len(times)} {what} of the {w.name} workload (V={w.V}), median",
+            "single_thread": {"value": rows1 / sec1, "unit": "rows/s", "cores": 1,
+                              "sample": f"one pass over the first {rows1} rows"}}
 
 
 def run_reference(args, w):

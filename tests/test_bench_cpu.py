@@ -118,3 +118,13 @@ def test_peaks_come_from_the_measured_file():
         pytest.skip("no measured peaks here")
     assert kind == "measured"
     assert pk["hbm_gbs"] > 1000 and pk["bf16_tflops_sustained"] > 100
+
+
+def test_cpu_baseline_times_the_oracle_on_all_cores_and_on_one():
+    import gen
+    w = gen.make("tiny")
+    rec = bench.cpu_baseline(w, budget_s=0.5, max_steps=3)
+    assert rec["kind"] == "oracle" and rec["unit"] == "rows/s" and rec["value"] > 0
+    assert rec["cores"] >= 1 and "tiny" in rec["sample"]
+    one = rec["single_thread"]
+    assert one["cores"] == 1 and one["value"] > 0 and one["unit"] == "rows/s"
