@@ -181,6 +181,33 @@ def test_logits_zero_pad_off_ignores_weights_beyond_hidden_actual():
     np.testing.assert_allclose(L, Ls, rtol=1e-13, atol=1e-14)
 
 
+def _bf16_round(a32: np.ndarray) -> np.ndarray:
+    return gen.bf16_bits_to_f32(gen.f32_to_bf16_bits(a32.astype(np.float32)))
+
+
+def test_planted_bf16_activation_fails_tolerance():
+    """Planted control for the activation precision.  The NKI tail's deferred form rounds x*gamma
+    to bf16 once per element ("GPT-OSS Tail Chunked Megakernel Kernel API Reference", parameter
+    `deferred_rms`); at H=2880 with W ~ N(0, 0.02) that single rounding moves logits by ~1e-3
+    (up to ~8e-3 over these 32768), far above the 1e-4 logit tolerance, so a kernel built that way
+    must fail parity against the exact oracle.  Carrying the activation as hi + lo (two bf16 parts, the realization the kernels
+    use) stays well inside it (~1e-5 at the largest of these 32768 logits)."""
+    w = gen.custom(8, 2880, 4096, 16, hidden_dtype="bf16", seed=21)
+    L = oracle.logits(w.hidden, "bf16", w.gamma, w.w_t, w.H, w.eps, 1)
+    Wd = gen.bf16_bits_to_f32(w.w_t).astype(np.float64)
+    rstd = oracle.rstd(w.hidden, "bf16", w.H, w.H, w.eps, 1)
+    a32 = (gen.bf16_bits_to_f32(w.hidden) * w.gamma[None, :]).astype(np.float32)  # fp32 x*gamma
+    one = _bf16_round(a32)
+    hi = one
+    lo = _bf16_round(a32 - hi)  # the remainder is exact in fp32
+    err_one = np.abs(rstd[:, None] * (one.astype(np.float64) @ Wd) - L).max()
+    err_hilo = np.abs(rstd[:, None] * ((hi.astype(np.float64) + lo.astype(np.float64)) @ Wd) - L).max()
+    assert err_one > 1e-4          # the page's single rounding: red against the tolerance
+    assert err_hilo < 2.5e-5       # hi + lo: ~16 significant bits, inside it
+    # and the exact fp32 activation (the fused kernels' input to the split) differs only by fp32 rounding
+    assert np.abs(rstd[:, None] * (a32.astype(np.float64) @ Wd) - L).max() < 1e-6
+
+
 # ------------------------------------------------------------------ top-k
 
 def test_topk_matches_lexsort_brute_force():
