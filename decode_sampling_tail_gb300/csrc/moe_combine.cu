@@ -1,9 +1,9 @@
 // The tail's producer step: the MoE combine and residual add that form the
 // bf16 hidden state the final RMSNorm reads ("nemotron CUDA: RMSNorm rows run
 // on the shared norms and combine (#548, step 1)", TensorFold pull request
-// #1353, section "What moves", entry tf_nemo_add_moe_norm: the slots are summed
-// per column in slot order from 0 with fp32 fmas, the sum rounded to bf16 and
-// added to the residual).  Per hidden lane j of row b:
+// #1353, section "What moves", entry tf_nemo_add_moe_norm: one fp32 fma per
+// slot, slots in index order, then a bf16 rounding before the residual add).
+// Per hidden lane j of row b:
 //   acc = 0;  acc = fma(w[b][s], y[b][s][j], acc) for s = 0, 1, ..., S-1
 //   h[b][j] = bf16(x[b][j] + bf16(acc))
 // with IEEE fp32 fmas and adds and bf16 rounding to nearest, ties to even.

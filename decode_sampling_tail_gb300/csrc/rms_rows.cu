@@ -3,7 +3,7 @@
 // `zero_interleaved_pad`, `deferred_rms`).
 //
 // One CTA per batch row:
-//   1. widen the row exactly to fp32 (bf16 and fp16 are subsets of fp32);
+//   1. widen the row to fp32 (exact: every bf16 and fp16 value is an fp32 value);
 //   2. ss = sum of x^2 over the active lanes (all H lanes when the pads are
 //      zero, else lanes [0, H_u)); rstd = 1 / sqrt(ss / H_u + eps);
 //   3. a = x * gamma (deferred: rstd is applied to the GEMM output) or

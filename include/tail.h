@@ -54,7 +54,7 @@ typedef struct {
   int32_t V;                    /* vocabulary: columns of w_t; V % 16 == 0 */
   int32_t k;                    /* candidates kept by the global top-k: 1 <= k <= min(V, 1024) */
   int32_t gbs_max;              /* largest gbs a run may pass: 1 .. 4096 */
-  float eps;                    /* RMSNorm epsilon (1e-5 for GPT-OSS) */
+  float eps;                    /* added to the mean of squares under the root; GPT-OSS: 1e-5 */
   int32_t hidden_dtype;         /* tail_dtype of hidden */
   int32_t zero_interleaved_pad; /* 1: pad lanes are zero in hidden, gamma and w_t wherever they sit,
                                       so all H lanes are summed; 0: lanes [H_u, H) are ignored */
@@ -118,7 +118,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out);
  *   w_t            [H, V] bf16 bit patterns, C-contiguous, V fastest (`lm_head_weight_t`),
  *                  16-byte aligned.  Read once per step; never modified.
  *   params         [gbs, n_param_cols] fp32 rows [top_k, top_p, temperature(, u)]
- *                  (`sampling_params`), or NULL: the sampler is skipped and
+ *                  (`sampling_params`), or NULL: no draw is made and
  *                  out_tokens is not written.  n_param_cols is 3 (u = 0.5) or 4.
  *   gbs            rows in this call, 0 <= gbs <= gbs_max (0 is a no-op).
  *   out_tokens     [gbs] int32 sampled vocabulary ids (may be NULL only if params is NULL).

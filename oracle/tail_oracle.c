@@ -41,9 +41,9 @@
 int oracle_version(void) { return 1; }
 
 /* ---------------------------------------------------------------------------
- * Widening.  Parameter `hidden_states`: a 16-bit input is widened to fp32
- * exactly (both half formats are subsets of fp32).  fp32 -> double is exact
- * as well, so the oracle widens straight to double.
+ * Widening.  Parameter `hidden_states`: fp32, fp16 or bf16 input; every fp16
+ * and bf16 value is representable in fp32 (and every fp32 value in double),
+ * so the conversion loses nothing and the oracle widens straight to double.
  * ------------------------------------------------------------------------- */
 
 /* bfloat16: the upper 16 bits of an IEEE binary32. */
@@ -109,8 +109,9 @@ int oracle_rstd(const void *x, int dtype, int B, int H, int Hu, float eps, int z
 
 /* ---------------------------------------------------------------------------
  * lm_head.  Parameters `lm_head_weight_t` ([H, V] bf16, already transposed,
- * C-contiguous) and `deferred_rms` ("exact algebra": rms is a per-row scalar
- * and the GEMM is linear, so both realizations are this one formula):
+ * C-contiguous) and `deferred_rms` (scaling each row before or after the
+ * product gives the same value mathematically: the scale is one number per
+ * row and the product is linear, so both realizations are this one formula):
  *   logit_bv = rstd_b * sum_h (x_bh * gamma_h) * W_hv
  * ------------------------------------------------------------------------- */
 typedef struct {
@@ -301,8 +302,8 @@ int oracle_topk(const double *logits, int B, int V, int k, int nthreads, double 
 
 /* ---------------------------------------------------------------------------
  * Sampler.  Parameter `sampling_params`: per row [top_k, top_p, temperature]
- * and an optional 4th column u in [0, 1), the inverse-transform draw; with 3
- * columns the draw is the compiled-in deterministic value 0.5.
+ * and an optional 4th column u in [0, 1) that drives an inverse-CDF draw;
+ * without it u is the fixed value 0.5.
  *
  * The page names the columns only.  The order of operations used here is the
  * standard nucleus-sampling one:
@@ -387,8 +388,8 @@ int oracle_sample_row(const double *vals, const int32_t *idx, int n, const float
 
 /* ---------------------------------------------------------------------------
  * The whole tail for B rows: logits, global top-k, sampler.  `params` may be
- * NULL (parameter `sampling_params`: when None the sampler is skipped and no
- * token is produced); then `tokens` is left untouched.
+ * NULL (parameter `sampling_params`: without parameters there is no draw and
+ * the call yields no token); then `tokens` is left untouched.
  * ------------------------------------------------------------------------- */
 int oracle_tail(const void *x, int dtype, const float *gamma, const uint16_t *w_t, int B,
                 int H, int Hu, int V, int k, float eps, int zero_pad, const float *params,
@@ -412,10 +413,11 @@ int oracle_tail(const void *x, int dtype, const float *gamma, const uint16_t *w_
  * MoE combine + residual add (the tail's producer).  Page: "nemotron CUDA:
  * RMSNorm rows run on the shared norms and combine (#548, step 1)" (TensorFold
  * pull request #1353), section "What moves", entry tf_nemo_add_moe_norm, and
- * the contract kinds moe_bf16_h / moe_f32_h: for every hidden lane, the expert slots are
- * summed in slot order from 0 with fp32 fused multiply-adds, the sum is
- * rounded to bf16, added to the bf16 residual x in fp32, and the result is
- * rounded to bf16 -- the hidden state h that the final RMSNorm reads.
+ * the contract kinds moe_bf16_h / moe_f32_h: for every hidden lane, an fp32
+ * accumulator starting at 0 takes one fused multiply-add per slot, slots in
+ * index order 0, 1, ..., S-1; its bf16 rounding is added to the bf16
+ * residual x in fp32 and that sum is rounded to bf16 -- the hidden state h
+ * that the final RMSNorm reads.
  *   x     [B, H]      bf16 residual
  *   slots [B, S, H]   expert outputs, fp32 (OR_F32) or bf16 (OR_BF16)
  *   w     [B, S]      fp32 slot weights

@@ -2,7 +2,7 @@
 
 The step ("nemotron CUDA: RMSNorm rows run on the shared norms and combine
 (#548, step 1)", TensorFold pull request #1353, entry tf_nemo_add_moe_norm): per hidden
-lane, an fp32 fma chain over the expert slots in slot order from 0, rounded to
+lane, an fp32 fma chain over the expert slots taken in index order, rounded to
 bf16, added to the bf16 residual and rounded to bf16.  The pins below do not
 restate that formula: hand-worked values (tests/golden/moe_combine_cases.txt,
 each derived in the file), bf16 rounding checked by nearest distance in
