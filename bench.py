@@ -542,6 +542,7 @@ def main():
         "metric": METRIC, "value": rows_s, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": ms_step * 1e3,
         "single_step_us_p10": 1e3 * float(np.percentile(per_step, 10)),
+        "single_step_us_median": 1e3 * float(np.percentile(per_step, 50)),
         "single_step_us_p90": 1e3 * float(np.percentile(per_step, 90)),
         "cuda_graph": graph,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
