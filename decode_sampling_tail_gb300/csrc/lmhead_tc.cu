@@ -8,13 +8,14 @@
 // with fp32 accumulation in tensor memory.
 //
 // Persistent kernel, one CTA per SM, 7 warps:
-//   warp 0     weight producer: per ring stage the 64 x TC_N weight slice
-//              (TC_N / 64 TMA boxes of 64 x 64, 128-byte swizzle), requested
+//   warp 0     weight producer: per ring stage the 64 x N weight slice
+//              (N / 64 TMA boxes of 64 x 64, 128-byte swizzle; N = 192
+//              columns when hi and lo share a tile, else 256), requested
 //              up to NW stages ahead.
 //   warp 6     activation producer: the matching 64-wide k slice of the
 //              activation tile (hi and lo: two 128 x 64 boxes, or one box
 //              holding both when the batch fits in 64 rows), NA stages ahead.
-//   warp 1     tensor-memory owner and MMA issuer: M = 128, N = TC_N, K = 16
+//   warp 1     tensor-memory owner and MMA issuer: M = 128, N, K = 16
 //              per instruction, A K-major, B (the weight, V contiguous)
 //              MN-major; two accumulators of 256 columns so the epilogue of
 //              one tile overlaps the MMAs of the next.
@@ -45,9 +46,6 @@ constexpr uint32_t TC_TMEM_COLS = 2 * TC_ACC_COLS;  // two accumulators
 constexpr uint32_t W_BOX_BYTES = 64 * 64 * 2;
 constexpr uint32_t A_BOX_BYTES = 128 * 64 * 2;
 constexpr int XBUF_PITCH = 33;                      // floats per row of the stacked hi/lo exchange
-constexpr int TC_CHUNKS = TC_N / 32;
-constexpr int TC_WBOX = TC_N / 64;                  // 64-column weight boxes per stage
-static_assert(TC_N % 64 == 0 && TC_N <= 256, "tile width: whole 64-column boxes, one accumulator");
 
 // Shared memory: the activation ring (NA stages), the weight ring (NW stages), the
 // stacked hi/lo exchange, the logits store boxes and the barriers.  The two
@@ -55,8 +53,12 @@ static_assert(TC_N % 64 == 0 && TC_N <= 256, "tile width: whole 64-column boxes,
 // further ahead than the L2-resident activations.
 template <bool STACKED>
 struct TcGeom {
+  static constexpr int N = STACKED ? TC_N_STACKED : TC_N_SEPARATE;  // vocabulary columns of a tile
+  static_assert(N % 64 == 0 && N <= static_cast<int>(TC_ACC_COLS), "tile width: whole 64-column boxes, one accumulator");
+  static constexpr int CHUNKS = N / 32;  // 32-column blocks of the epilogue
+  static constexpr int WBOX = N / 64;    // 64-column weight boxes per stage
   static constexpr uint32_t A_BYTES = STACKED ? A_BOX_BYTES : 2 * A_BOX_BYTES;  // one activation stage
-  static constexpr uint32_t W_BYTES = TC_WBOX * W_BOX_BYTES;                     // one weight stage
+  static constexpr uint32_t W_BYTES = WBOX * W_BOX_BYTES;                     // one weight stage
   static constexpr int TBUF_N = STACKED ? 1 : 2;  // 32 x 32 fp32 store boxes per epilogue warp
   static constexpr uint32_t TBUF_BYTES = 4 * TBUF_N * 4096;
   static constexpr uint32_t XBUF_BYTES = STACKED ? (64 * XBUF_PITCH * 4 + 1023) / 1024 * 1024 : 0;
@@ -194,10 +196,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int kb = it % a.kblocks;
         const int s = it % NW;
         const uint32_t st = ringW_u + static_cast<uint32_t>(s) * G::W_BYTES;
-        const int x0 = n * TC_N;
+        const int x0 = n * G::N;
         int nbox = 0;
 #pragma unroll
-        for (int j = 0; j < TC_WBOX; ++j) nbox += (x0 + 64 * j < a.V) ? 1 : 0;  // >= 1: x0 < V
+        for (int j = 0; j < G::WBOX; ++j) nbox += (x0 + 64 * j < a.V) ? 1 : 0;  // >= 1: x0 < V
         mbar_arrive_expect_tx(fullW_bar(s), static_cast<uint32_t>(nbox) * W_BOX_BYTES);
         for (int j = 0; j < nbox; ++j)
           tma_load_2d(st + j * W_BOX_BYTES, &mapW, x0 + 64 * j, kb * TC_KB, fullW_bar(s), pol_w);
@@ -250,7 +252,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(TC_M, TC_N);
+      constexpr uint32_t idesc = idesc_bf16_f32(TC_M, G::N);
       int it = 0;
       bool ok = true;
       for (int tile_i = 0; tile_i < my_tiles && ok; ++tile_i) {
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       const int rbase = row - lane;  // first row of this warp's 32
 #pragma unroll 1
-      for (int c = 0; c < TC_CHUNKS; ++c) {
+      for (int c = 0; c < G::CHUNKS; ++c) {
         float v[32];
         tmem_ld32(taddr + 32u * c, v);
         if (STACKED) {
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           named_sync(2, 128);
         }
-        const int col0 = n * TC_N + 32 * c;
+        const int col0 = n * G::N + 32 * c;
         if (owner && col0 < a.V) {  // warp-uniform
           const int nv = min(32, a.V - col0);  // 16 or 32: V is a multiple of 16
 #pragma unroll

@@ -189,16 +189,17 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
     // MERGE_SCAN_PT loads in flight per thread
     const int nsat = s_nsat;
     for (int s0 = 0; s0 < nsat;) {
-      if (ncand + TC_N > a.capc) ncand = fold(ncand);
-      const int ng = min(nsat - s0, (a.capc - ncand) / TC_N);  // >= 1 after the fold
-      const int ne = ng * TC_N;
+      const int tn = a.tile_n;
+      if (ncand + tn > a.capc) ncand = fold(ncand);
+      const int ng = min(nsat - s0, (a.capc - ncand) / tn);  // >= 1 after the fold
+      const int ne = ng * tn;
       for (int i0 = 0; i0 < ne; i0 += nt * MERGE_SCAN_PT) {  // warp-uniform trip counts
         uint32_t kv[MERGE_SCAN_PT];
         int ci[MERGE_SCAN_PT];
 #pragma unroll
         for (int u = 0; u < MERGE_SCAN_PT; ++u) {
           const int i = i0 + u * nt + tid;
-          ci[u] = i < ne ? sat[s0 + i / TC_N] * TC_N + i % TC_N : a.V;
+          ci[u] = i < ne ? sat[s0 + i / tn] * tn + i % tn : a.V;
           kv[u] = ci[u] < a.V ? float_key(__ldcg(lg + ci[u])) : 0u;
         }
 #pragma unroll

@@ -45,9 +45,9 @@ struct tail_s {
   // tensor-core path (gbs >= tc_min)
   uint16_t* tc_act;     // [tc_act_rows(gbs_max)][H] bf16 hi/lo rows
   float* tc_rs;         // [gbs_max] row scales
-  uint64_t* tc_lists;   // [gbs_max][ntn][TC_LIST]
+  uint64_t* tc_lists;   // [gbs_max][tc_ntn_max][TC_LIST]
   float* tc_logits;     // [gbs_max][V] fp32 logits when the caller passes none
-  int tc_ntn;
+  int tc_ntn_max;       // column tiles of the narrower tile width (the most lists a row can have)
   int merge_dyn;
   int merge_capc, merge_sortP, merge_smem;
   const void* tc_map_w_ptr;  // tensor maps cached for (w_t pointer, logits pointer, batch rows)
@@ -212,14 +212,21 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   // the tensor-core path, when the merge can be planned for k and V: batches of
   // TC_MIN_ROWS rows or more always take it; narrow vocabularies take it for
   // every batch (the mma.sync kernel's per-row bulk copies make it no faster there)
-  h->tc_ntn = tc_col_tiles(cfg->V);
+  h->tc_ntn_max = tc_col_tiles(cfg->V, TC_N_STACKED);
   cudaError_t te = prepare_tc(static_cast<int>(prop.sharedMemPerBlockOptin), &h->merge_dyn);
   if (te != cudaSuccess) {
     delete h;
     return cuda_fail(te, "cudaFuncSetAttribute (tensor-core kernels)");
   }
+  // one merge plan for both tile widths: the candidate buffers do not depend on the tile count,
+  // the shared memory for the lists does, so the larger of the two requirements is kept
+  int capc2 = 0, sortP2 = 0, smem2 = 0;
   const bool tc_ok =
-      encode_tiled() && plan_merge(cfg->k, h->tc_ntn, h->merge_dyn, &h->merge_capc, &h->merge_sortP, &h->merge_smem);
+      encode_tiled() &&
+      plan_merge(cfg->k, h->tc_ntn_max, h->merge_dyn, &h->merge_capc, &h->merge_sortP, &h->merge_smem) &&
+      plan_merge(cfg->k, tc_col_tiles(cfg->V, TC_N_SEPARATE), h->merge_dyn, &capc2, &sortP2, &smem2) &&
+      capc2 == h->merge_capc && sortP2 == h->merge_sortP;
+  if (smem2 > h->merge_smem) h->merge_smem = smem2;
   if (cfg->path == TAIL_PATH_TENSOR)
     h->tc_min = 1;
   else if (cfg->path == TAIL_PATH_AUTO && cfg->V <= TAIL_TC_ALL_ROWS_MAX_V && tc_ok)
@@ -279,7 +286,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
     const size_t G = static_cast<size_t>(cfg->gbs_max);
     e = e ? e : dalloc(&h->tc_act, static_cast<size_t>(tc_act_rows(cfg->gbs_max)) * cfg->H, &tot);
     e = e ? e : dalloc(&h->tc_rs, G, &tot);
-    e = e ? e : dalloc(&h->tc_lists, G * h->tc_ntn * TC_LIST, &tot);
+    e = e ? e : dalloc(&h->tc_lists, G * h->tc_ntn_max * TC_LIST, &tot);
     e = e ? e : dalloc(&h->tc_logits, G * cfg->V, &tot);
     // rows of the activation buffer past a batch's rows still feed the MMA: keep them finite
     if (e == cudaSuccess)
@@ -308,6 +315,8 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   const tail_config& c = h->cfg;
   const int stacked = tc_stacked(gbs);
   const int n_mb = tc_mblocks(gbs);
+  const int tile_n = tc_tile_n(gbs);
+  const int ntn = tc_col_tiles(c.V, tile_n);
   float* logits = out_logits ? out_logits : h->tc_logits;
   if (h->tc_map_w_ptr != w_t || h->tc_map_l_ptr != logits || h->tc_map_rows != gbs) {
     if (!encode_2d(&h->tc_map_w, w_t, false, static_cast<uint64_t>(c.V), static_cast<uint64_t>(c.H), 64, 64) ||
@@ -352,11 +361,11 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   ta.err = h->err;
   ta.B = gbs;
   ta.V = c.V;
-  ta.ntn = h->tc_ntn;
+  ta.ntn = ntn;
   ta.n_mb = n_mb;
   ta.kblocks = (c.H + TC_KB - 1) / TC_KB;
   ta.timeout_ns = h->wait_limit_ns;
-  const int ntiles = h->tc_ntn * n_mb;
+  const int ntiles = ntn * n_mb;
   e = launch_tc(ta, h->tc_map_a, h->tc_map_w, h->tc_map_l, stacked, ntiles < h->num_sms ? ntiles : h->num_sms,
                 stream, true);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch (tensor-core lm_head)");
@@ -375,7 +384,8 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   ma.B = gbs;
   ma.V = c.V;
   ma.K = c.k;
-  ma.ntn = h->tc_ntn;
+  ma.ntn = ntn;
+  ma.tile_n = tile_n;
   ma.capc = h->merge_capc;
   ma.sortP = h->merge_sortP;
   ma.smem_bytes = h->merge_smem;

@@ -10,7 +10,13 @@
 namespace tail {
 
 constexpr int TC_M = 128;        // rows of one MMA tile (tensor-memory lanes)
-constexpr int TC_N = 192;        // vocabulary columns of one tile (three 64-column TMA boxes)
+// vocabulary columns of one tile: three 64-column TMA boxes while hi and lo
+// share a tile (the weight-bound sizes, where a narrower stage leaves room for
+// more of the weight in flight), four (the whole 256-column accumulator) when
+// they have tiles of their own (fewer activation bytes per MMA flop, which
+// matters once the tensor pipe is the limit)
+constexpr int TC_N_STACKED = 192;
+constexpr int TC_N_SEPARATE = 256;
 constexpr int TC_KB = 64;        // k extent of one ring stage (one 128-byte swizzle row of bf16)
 constexpr int TC_LIST = 8;       // candidates each (row, tile) keeps: its top 8 by (value desc, index asc)
 constexpr int TC_STACK_MAX = 64; // up to this many rows, hi and lo parts share one 128-row tile
@@ -23,7 +29,8 @@ constexpr int TC_MIN_ROWS = 9;   // batches of at least this many rows take the 
 inline int tc_stacked(int B) { return B <= TC_STACK_MAX ? 1 : 0; }
 inline int tc_mblocks(int B) { return tc_stacked(B) ? 1 : (B + TC_M - 1) / TC_M; }
 inline int64_t tc_act_rows(int B) { return tc_stacked(B) ? TC_M : static_cast<int64_t>(tc_mblocks(B)) * 2 * TC_M; }
-inline int tc_col_tiles(int V) { return (V + TC_N - 1) / TC_N; }
+inline int tc_tile_n(int B) { return tc_stacked(B) ? TC_N_STACKED : TC_N_SEPARATE; }
+inline int tc_col_tiles(int V, int tile_n) { return (V + tile_n - 1) / tile_n; }
 
 struct SplitArgs {
   const void* hidden;
@@ -59,6 +66,7 @@ struct MergeArgs {
   int ncols;
   int32_t* tokens;         // [B] or null
   int B, V, K, ntn;
+  int tile_n;              // vocabulary columns of one tile (tc_tile_n of the batch)
   int capc, sortP, smem_bytes;
   int* err;                // device error flag (a bounded wait ran out)
   uint64_t timeout_ns;
