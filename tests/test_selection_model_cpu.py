@@ -1,6 +1,6 @@
-"""CPU model of the tensor-core path's candidate selection (no GPU, no library).
+"""CPU models of the two candidate selections that make the GPU top-k exact (no GPU, no library).
 
-The lm_head epilogue keeps, per (row, column tile), the tile's top 8 by (value desc, column asc);
+Tensor-core path (9 rows and more): the lm_head epilogue keeps, per (row, column tile), the tile's top 8 by (value desc, column asc);
 the merge takes a lower bound x of the row's K-th largest element from the tile maxima (every
 tile maximum is a distinct element, so K of them at or above x mean K elements at or above x),
 keeps every list entry >= x, and rescans the whole tile of any list whose 8th entry is still
@@ -12,7 +12,8 @@ hi and lo share a tile, 256 otherwise), with the exact bound and with a bound lo
 key resolution (the merge's warp bound is exact only to 16 bits), on random rows and on rows
 built to defeat it (columns tied in groups of 16, a cluster of top values, a constant row), and checks the candidates
 against the oracle's top-k ("GPT-OSS Tail Chunked Megakernel Kernel API Reference", section
-"Background": a per-chunk top-k followed by one merge must give the global top-k).
+"Background": a per-chunk top-k followed by one merge must give the global top-k).  The second
+half models the mma.sync path's slab publications and row owners the same way.
 """
 import numpy as np
 import pytest
@@ -120,3 +121,97 @@ def test_key_order_matches_value_order():
     v = np.array([-np.inf, -2.0, -0.0, 0.0, 1e-45, 1.0, np.inf], np.float32)
     k = _keys(v)
     assert np.all(np.diff(k.astype(np.int64)) >= 0) and k[2] == k[3]
+
+
+# ------------------------------------------------------------------ the mma.sync path (up to 8 rows)
+#
+# Each CTA owns one vocabulary slab (whole 16-column pairs, split evenly over the slabs).  After
+# the stream it sorts the 32 lane maxima of its slab (lane l holds columns l, l + 32, ... of the
+# slab), keeps the 4 largest as leaders and b = the 8th largest, and publishes every element >= b
+# when there are at most 32 of them (else nothing, with b raised to the largest key).  The row
+# owner bounds the K-th largest element by the K-th largest leader (x, exact to 16 bits), keeps the
+# published elements >= x, takes thr = the K-th largest of those (or x when fewer than K remain),
+# and rescans every slab with b > thr.  The argument: a top-K element e of a slab that published
+# is either >= b (published, and >= x) or below b, and then b > e >= v_K >= thr, so that slab is
+# rescanned; a slab that published nothing has b above any thr and is rescanned too.
+
+def _slab_candidates(row, K, nslab, lower16):
+    V = row.size
+    key = _keys(row)
+    npairs = V // 16
+    top = np.uint64(0xFFFFFFFF)
+    pubs, bs, leaders, bounds = [], [], [], []
+    for c in range(nslab):
+        lo, hi = 16 * (npairs * c // nslab), 16 * (npairs * (c + 1) // nslab)
+        seg = key[lo:hi]
+        padded = np.zeros(-(-seg.size // 32) * 32, np.uint64)
+        padded[: seg.size] = seg
+        lane_max = np.sort(padded.reshape(-1, 32).max(axis=0))[::-1]
+        leaders.extend(lane_max[:4])
+        b = lane_max[7]
+        sel = np.nonzero(seg >= b)[0] + lo
+        if sel.size <= 32:
+            pubs.append(sel)
+            bs.append(b)
+        else:
+            pubs.append(np.zeros(0, np.int64))
+            bs.append(top)
+        bounds.append((lo, hi))
+    leaders = np.array(leaders, np.uint64)
+    x = int(np.sort(leaders)[::-1][K - 1]) if leaders.size >= K else 0
+    if lower16:
+        x &= 0xFFFF0000
+    F = np.concatenate([p[key[p] >= x] for p in pubs])
+    if F.size >= K:
+        order = F[np.lexsort((F, -key[F].astype(np.int64)))]
+        thr = int(key[order[K - 1]])
+    else:
+        thr = x
+    cand, rescans = set(F.tolist()), 0
+    for (lo, hi), b in zip(bounds, bs):
+        if int(b) > thr:
+            rescans += 1
+            cand |= set((np.nonzero(key[lo:hi] >= thr)[0] + lo).tolist())
+    return np.array(sorted(cand)), rescans
+
+
+def _slab_rows(kind, V, rng):
+    r = rng.standard_normal((2, V)).astype(np.float32)
+    if kind == "clustered":  # every top element inside one slab: it publishes nothing
+        r[:, 5000:5400] += 10.0
+    elif kind == "tied64":  # columns repeated 64 times: no slab can publish
+        r = np.repeat(r[:, : V // 64], 64, axis=1)
+    elif kind == "constant":
+        r = np.full((2, V), -1.25, np.float32)
+    return r
+
+
+@pytest.mark.parametrize("lower16", [False, True], ids=["exact_bound", "bound_16bit"])
+@pytest.mark.parametrize("kind", ["random", "clustered", "tied64", "constant"])
+def test_slab_publications_and_rescans_hold_the_exact_top_k(kind, lower16):
+    # the GPT-OSS shape: V = 201088 over 152 slabs (82-83 pairs, ~1323 columns each), K = 256
+    rng = np.random.default_rng(21)
+    V, K, nslab = 201_088, 256, 152
+    rows = _slab_rows(kind, V, rng)
+    L = rows.astype(np.float64)
+    _, want = oracle.topk(L, K)
+    for r in range(rows.shape[0]):
+        cand, rescans = _slab_candidates(rows[r], K, nslab, lower16)
+        order = cand[np.lexsort((cand, -L[r, cand]))][:K]
+        assert np.array_equal(order, want[r])
+        if kind == "random":  # the usual case: ~10 elements a slab, no rescan
+            assert rescans == 0 and cand.size < 12 * nslab
+        else:
+            assert rescans > 0
+
+
+@pytest.mark.parametrize("V,nslab,K", [(2016, 15, 40), (1024, 8, 200), (4800, 37, 64)])
+def test_narrow_slabs_and_k_above_the_slab_width(V, nslab, K):
+    rng = np.random.default_rng(22)
+    rows = rng.standard_normal((3, V)).astype(np.float32)
+    L = rows.astype(np.float64)
+    _, want = oracle.topk(L, K)
+    for r in range(3):
+        cand, _ = _slab_candidates(rows[r], K, nslab, True)
+        order = cand[np.lexsort((cand, -L[r, cand]))][:K]
+        assert np.array_equal(order, want[r])
