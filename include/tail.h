@@ -10,9 +10,12 @@
  * the parameter entries `hidden_states`, `gamma`, `lm_head_weight_t`, `eps`,
  * `hidden_actual`, `zero_interleaved_pad`, `k`, `emit_logits`,
  * `sampling_params` and `deferred_rms` define the inputs, options and outputs
- * mirrored below.  On one GPU the whole vocabulary is local (V_s = V), so the
- * page's all-to-all, its bf16 logits mirror and the hop/row-ownership helpers
- * have no counterpart here.
+ * mirrored below.  On one GPU the whole vocabulary is local (V_s = V).  The
+ * page's vocabulary-parallel deployment (a slice per rank, one exchange, row
+ * ownership) is served by tail_merge_shards below, with the exchange left to
+ * the caller (the Python module decode_sampling_tail_gb300.vocab_parallel
+ * does it with torch.distributed); the page's bf16 logits mirror and its
+ * multi-hop meshes have no counterpart here.
  *
  * Conventions for every entry point:
  *   - Device pointers are caller-owned memory on the handle's device.  The
@@ -262,6 +265,12 @@ int tail_merge_shards(int32_t nshard, int32_t k_in, int32_t k, int32_t gbs, cons
                       const int32_t* cand_idx, const int32_t* shard_offsets, const float* params,
                       int32_t n_param_cols, int32_t* out_tokens, float* out_topk_vals_opt,
                       int32_t* out_topk_idx_opt, void* stream);
+
+/*
+ * The calls below are the library's own plumbing (error reporting, timing, the
+ * bound on device waits, a test hook, static facts, lifetime); no page defines
+ * them.
+ */
 
 /*
  * Synchronises the handle's device work and reads the device error flag that
