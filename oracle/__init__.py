@@ -78,7 +78,7 @@ def lib():
                                       i32, P, P, P, P]
             L.oracle_f32_to_bf16_rne.argtypes = [f32]
             L.oracle_f32_to_bf16_rne.restype = ctypes.c_uint16
-            L.oracle_moe_combine.argtypes = [P, P, i32, i32, P, i32, i32, P]
+            L.oracle_moe_combine.argtypes = [P, P, i32, i32, i32, P, i32, i32, P]
             _lib = L
     return _lib
 
@@ -201,20 +201,23 @@ def f32_to_bf16(v: float) -> int:
     return int(lib().oracle_f32_to_bf16_rne(ctypes.c_float(v)))
 
 
-def moe_combine(x_bits: np.ndarray, slots: np.ndarray, w: np.ndarray) -> np.ndarray:
-    """The tail's producer step: h = bf16(x + bf16(fp32 fma chain of w[s] * slots[s] over s = 0, 1, ...)).
+def moe_combine(x_bits: np.ndarray, slots: np.ndarray, w: np.ndarray, n_routed: int | None = None) -> np.ndarray:
+    """The tail's producer step: per lane, r = the fp32 fma chain of w[s] * slots[s] over the routed
+    slots s < n_routed (in order from 0), sh = the same chain over the shared slots s >= n_routed,
+    and h = bf16(x + bf16(r + sh)).
 
-    x_bits [B, H] bf16 bits; slots [B, S, H] float32, or uint16 bf16 bits; w [B, S] float32.
-    Returns h [B, H] as bf16 bits."""
+    x_bits [B, H] bf16 bits; slots [B, S, H] float32, or uint16 bf16 bits; w [B, S] float32;
+    n_routed: routed slots (None: all S, no shared slot).  Returns h [B, H] as bf16 bits."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     B, H = x.shape
     y = np.ascontiguousarray(slots)
     S = y.shape[1] if y.ndim == 3 else 0
+    nr = S if n_routed is None else int(n_routed)
     sd = DTYPE_CODES["f32"] if y.dtype == np.float32 else DTYPE_CODES["bf16"]
     wt = np.ascontiguousarray(w, dtype=np.float32).reshape(B, S)
     h = np.empty((B, H), np.uint16)
-    rc = lib().oracle_moe_combine(_ptr(x), _ptr(y) if S else None, sd, S, _ptr(wt) if S else None, B, H, _ptr(h))
+    rc = lib().oracle_moe_combine(_ptr(x), _ptr(y) if S else None, sd, S, nr, _ptr(wt) if S else None, B, H,
+                                  _ptr(h))
     if rc:
         raise ValueError(f"oracle_moe_combine failed: {rc}")
     return h
-

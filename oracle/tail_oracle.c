@@ -24,9 +24,10 @@
  * One producer step may precede the tail: the MoE combine and residual add
  * that forms the bf16 hidden state ("nemotron CUDA: RMSNorm rows run on the
  * shared norms and combine (#548, step 1)", TensorFold pull request #1353,
- * entry tf_nemo_add_moe_norm; oracle_moe_combine below).  Its precision is
- * fixed by that page (fp32 fmas, bf16 roundings), so it is evaluated in
- * exactly those operations, not in double precision.
+ * entry tf_nemo_add_moe_norm, with the routed chain and the shared sum kept
+ * apart as its fix reply settles; oracle_moe_combine below).  Its precision
+ * is fixed by that page (fp32 fmas and adds, bf16 roundings), so it is
+ * evaluated in exactly those operations, not in double precision.
  */
 #include <math.h>
 #include <pthread.h>
@@ -412,18 +413,25 @@ int oracle_tail(const void *x, int dtype, const float *gamma, const uint16_t *w_
 /* ---------------------------------------------------------------------------
  * MoE combine + residual add (the tail's producer).  Page: "nemotron CUDA:
  * RMSNorm rows run on the shared norms and combine (#548, step 1)" (TensorFold
- * pull request #1353), section "What moves", entry tf_nemo_add_moe_norm, and
- * the contract kinds moe_bf16_h / moe_f32_h: for every hidden lane, an fp32
- * accumulator starting at 0 takes one fused multiply-add per slot, slots in
- * index order 0, 1, ..., S-1; its bf16 rounding is added to the bf16
- * residual x in fp32 and that sum is rounded to bf16 -- the hidden state h
- * that the final RMSNorm reads.
+ * pull request #1353): section "What moves", entry tf_nemo_add_moe_norm, and
+ * the contract kinds moe_bf16_h / moe_f32_h, as settled by the author's fix
+ * reply (commit 8e1115e05): the fused residual keeps the routed chain and the
+ * shared sum apart.  For every hidden lane:
+ *   r  = fp32 accumulator from 0, one fused multiply-add per ROUTED slot
+ *        (slots 0 .. n_routed-1), in index order;
+ *   sh = the same over the SHARED slots (n_routed .. S-1), a chain of its
+ *        own; Nemotron's 2 shared slots carry weight 1, where each fma is the
+ *        plain fp32 add s0 + s1;
+ *   c  = r + sh (one fp32 add: r + (s0 + s1), not ((r + s0) + s1));
+ *   h  = bf16(x + bf16(c)), the add in fp32 -- the hidden state that the
+ *        final RMSNorm reads.
  *   x     [B, H]      bf16 residual
  *   slots [B, S, H]   expert outputs, fp32 (OR_F32) or bf16 (OR_BF16)
  *   w     [B, S]      fp32 slot weights
  *   h     [B, H]      bf16 output
- * The fp32 fma is C99's fmaf (one rounding); bf16 rounding is to nearest,
- * ties to even, NaN kept NaN.
+ * With n_routed == S there is no shared slot and c = r (r + 0 = r: a chain
+ * that starts at +0 never ends at -0).  The fp32 fma is C99's fmaf (one
+ * rounding); bf16 rounding is to nearest, ties to even, NaN kept NaN.
  * ------------------------------------------------------------------------- */
 
 static float bits_to_float(uint32_t u) {
@@ -443,19 +451,25 @@ uint16_t oracle_f32_to_bf16_rne(float f) {
     return (uint16_t)upper;
 }
 
-int oracle_moe_combine(const uint16_t *x, const void *slots, int slot_dtype, int S, const float *w, int B,
-                       int H, uint16_t *h) {
-    if (B < 0 || H < 0 || S < 0 || (S > 0 && (!slots || !w)) || (slot_dtype != OR_F32 && slot_dtype != OR_BF16))
+int oracle_moe_combine(const uint16_t *x, const void *slots, int slot_dtype, int S, int n_routed, const float *w,
+                       int B, int H, uint16_t *h) {
+    if (B < 0 || H < 0 || S < 0 || n_routed < 0 || n_routed > S || (S > 0 && (!slots || !w)) ||
+        (slot_dtype != OR_F32 && slot_dtype != OR_BF16))
         return -1;
     for (int b = 0; b < B; ++b) {
         for (int j = 0; j < H; ++j) {
-            float acc = 0.0f;
+            float r = 0.0f, sh = 0.0f;
             for (int s = 0; s < S; ++s) {
                 const int64_t e = ((int64_t)b * S + s) * H + j;
                 const float y = slot_dtype == OR_F32 ? ((const float *)slots)[e]
                                                      : bits_to_float(((uint32_t)((const uint16_t *)slots)[e]) << 16);
-                acc = fmaf(w[(int64_t)b * S + s], y, acc);
+                const float ws = w[(int64_t)b * S + s];
+                if (s < n_routed)
+                    r = fmaf(ws, y, r);
+                else
+                    sh = fmaf(ws, y, sh);
             }
+            const float acc = r + sh;
             const float d = bits_to_float(((uint32_t)oracle_f32_to_bf16_rne(acc)) << 16);
             const float xv = bits_to_float(((uint32_t)x[(int64_t)b * H + j]) << 16);
             const float sum = xv + d;
@@ -464,4 +478,3 @@ int oracle_moe_combine(const uint16_t *x, const void *slots, int slot_dtype, int
     }
     return 0;
 }
-

@@ -1,9 +1,11 @@
 """Pins of the oracle's producer step, the MoE combine + residual add (CPU only).
 
 The step ("nemotron CUDA: RMSNorm rows run on the shared norms and combine
-(#548, step 1)", TensorFold pull request #1353, entry tf_nemo_add_moe_norm): per hidden
-lane, an fp32 fma chain over the expert slots taken in index order, rounded to
-bf16, added to the bf16 residual and rounded to bf16.  The pins below do not
+(#548, step 1)", TensorFold pull request #1353, entry tf_nemo_add_moe_norm, and
+the author's fix reply, which keeps the routed chain and the shared sum apart):
+per hidden lane, an fp32 fma chain over the routed slots taken in index order,
+plus the shared slots' own chain, rounded to bf16, added to the bf16 residual
+and rounded to bf16.  The pins below do not
 restate that formula: hand-worked values (tests/golden/moe_combine_cases.txt,
 each derived in the file), bf16 rounding checked by nearest distance in
 float64, and sums that are exact in every precision checked against numpy.
@@ -24,14 +26,14 @@ def _golden_cases():
         line = line.strip()
         if not line or line.startswith("#"):
             continue
-        name, x, sd, slots, weights, want = (f.strip() for f in line.split("|"))
-        cases.append((name, int(x, 16), sd, slots, weights, int(want, 16)))
+        name, x, sd, slots, weights, routed, want = (f.strip() for f in line.split("|"))
+        cases.append((name, int(x, 16), sd, slots, weights, int(routed), int(want, 16)))
     return cases
 
 
 @pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c[0])
 def test_moe_combine_hand_worked(case):
-    name, x, sd, slots, weights, want = case
+    name, x, sd, slots, weights, routed, want = case
     vals = [v for v in slots.split(",") if v]
     S = len(vals)
     if sd == "bf16":
@@ -39,7 +41,7 @@ def test_moe_combine_hand_worked(case):
     else:
         y = np.array([float(v) for v in vals], np.float32).reshape(1, S, 1)
     w = np.array([float(v) for v in weights.split(",") if v], np.float32).reshape(1, S)
-    h = oracle.moe_combine(np.array([[x]], np.uint16), y, w)
+    h = oracle.moe_combine(np.array([[x]], np.uint16), y, w, n_routed=routed)
     assert int(h[0, 0]) == want, f"{name}: {int(h[0, 0]):04x} != {want:04x}"
 
 
@@ -87,9 +89,11 @@ def _exact_case(seed, sd):
 
 @pytest.mark.parametrize("sd", ["f32", "bf16"])
 def test_moe_combine_exact_sums_match_numpy(sd):
+    # exact sums do not depend on how the slots split into routed and shared chains
     for seed in range(4):
         x, y, w, want = _exact_case(seed, sd)
-        assert np.array_equal(oracle.moe_combine(x, y, w), want)
+        for n_routed in (None, 0, 2, 5):
+            assert np.array_equal(oracle.moe_combine(x, y, w, n_routed=n_routed), want)
 
 
 def test_moe_combine_without_slots_is_the_residual():
@@ -99,3 +103,12 @@ def test_moe_combine_without_slots_is_the_residual():
     h = oracle.moe_combine(x, np.zeros((4, 0, 96), np.float32), np.zeros((4, 0), np.float32))
     # -0 + 0 = +0: the only pattern the add may change
     assert np.array_equal(h, np.where(x == 0x8000, np.uint16(0), x))
+
+
+def test_moe_combine_rejects_a_routed_count_beyond_the_slots():
+    x = np.zeros((1, 8), np.uint16)
+    y = np.zeros((1, 2, 8), np.float32)
+    w = np.ones((1, 2), np.float32)
+    for bad in (-1, 3):
+        with pytest.raises(ValueError):
+            oracle.moe_combine(x, y, w, n_routed=bad)

@@ -51,6 +51,15 @@ MUTANTS = [
     ("f16_subnormal_scale", "ldexp((double)f, -24)", "ldexp((double)f, -25)",
      [pins.test_widen_f16_exhaustive_against_numpy]),
     # the producer step (MoE combine + residual add)
+    ("shared_slots_folded_into_the_routed_chain",
+     "if (s < n_routed)\n                    r = fmaf(ws, y, r);\n                else\n                    sh = fmaf(ws, y, sh);",
+     "r = fmaf(ws, y, r);",
+     [lambda: _moe_golden("shared_apart"), lambda: _moe_golden("nemotron_8")]),
+    ("shared_weight_ignored", "sh = fmaf(ws, y, sh);", "sh = sh + y;",
+     [lambda: _moe_golden("shared_weighted")]),
+    ("shared_sum_rounded_apart", "const float acc = r + sh;",
+     "const float acc = r + bits_to_float(((uint32_t)oracle_f32_to_bf16_rne(sh)) << 16);",
+     [lambda: _moe_golden("shared_unrounded")]),
     ("combine_not_rounded_before_add",
      "const float d = bits_to_float(((uint32_t)oracle_f32_to_bf16_rne(acc)) << 16);", "const float d = acc;",
      [lambda: _moe_golden("round_first")]),
