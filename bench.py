@@ -365,10 +365,16 @@ def main():
         m_slots = torch.from_numpy((grng.standard_normal((w.B, args.moe_slots, w.H)) * 0.5).astype(np.float32)).to(dev)
         m_w = torch.from_numpy(grng.uniform(0.1, 1.0, (w.B, args.moe_slots)).astype(np.float32)).to(dev)
 
-        def step():  # noqa: F811
-            t.run_moe(hidden, m_slots, m_w, gamma, w_t, params, out_tokens=tokens, out_logits=logits, stream=stream)
+        m_routed = max(0, args.moe_slots - 2)  # Nemotron's order: the routed slots, then 2 shared ones
 
-        launches_per_step += 1  # the combine kernel
+        def step():  # noqa: F811
+            t.run_moe(hidden, m_slots, m_w, gamma, w_t, params, out_tokens=tokens, out_logits=logits,
+                      n_routed=m_routed, stream=stream)
+
+        # up to 8 slots the first kernel of the tail forms h itself; more take a combine kernel first
+        moe_fused = args.moe_slots <= 8 and (tc_path or (not args.legacy_rms and t.info.kernels_per_run == 1))
+        if not moe_fused:
+            launches_per_step += 1
 
     # a weight at least twice the L2 streams from HBM every step by itself; a smaller one is flushed
     # from L2 between timed steps
@@ -556,7 +562,7 @@ def main():
                           f"no flush: the {2 * w.H * w.V / 1e9:.2f} GB weight is larger than L2 and streams "
                           "from HBM every step"),
                    "lm_head_path": "tensor" if tc_path else "mma.sync",
-                   "producer": (f"MoE combine + residual add, {args.moe_slots} fp32 slots (tail_run_moe)"
+                   "producer": (f"MoE combine + residual add, {args.moe_slots} fp32 slots, the last 2 shared (tail_run_moe)"
                                 if args.moe_slots > 0 else "none"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "step_hbm_gbs": step_gbs,

@@ -89,7 +89,7 @@ def lib(path: str | None = None):
         L.tail_run.restype = ctypes.c_int
         L.tail_run_ex.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P, P]
         L.tail_run_ex.restype = ctypes.c_int
-        L.tail_run_moe.argtypes = [P, P, P, i32, i32, P, P, P, P, i32, i32, P, P, P, P, P, P]
+        L.tail_run_moe.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, i32, i32, P, P, P, P, P, P]
         L.tail_run_moe.restype = ctypes.c_int
         L.tail_run_host.argtypes = [P, P, P, P, P, i32, i32, P, P, P]
         L.tail_run_host.restype = ctypes.c_int
@@ -146,10 +146,10 @@ def tail_run_ex(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, ou
                              out_topk_vals_opt, out_topk_idx_opt, stream)
 
 
-def tail_run_moe(h, residual, slots, slot_dtype, nslots, slot_w, gamma, w_t, params, n_param_cols, gbs,
+def tail_run_moe(h, residual, slots, slot_dtype, nslots, n_routed, slot_w, gamma, w_t, params, n_param_cols, gbs,
                  out_tokens, out_logits_opt, out_topk_vals_opt, out_topk_idx_opt, out_hidden_opt, stream) -> int:
-    return lib().tail_run_moe(h, residual, slots, slot_dtype, nslots, slot_w, gamma, w_t, params, n_param_cols,
-                              gbs, out_tokens, out_logits_opt, out_topk_vals_opt, out_topk_idx_opt,
+    return lib().tail_run_moe(h, residual, slots, slot_dtype, nslots, n_routed, slot_w, gamma, w_t, params,
+                              n_param_cols, gbs, out_tokens, out_logits_opt, out_topk_vals_opt, out_topk_idx_opt,
                               out_hidden_opt, stream)
 
 
@@ -304,15 +304,17 @@ class Tail:
         return out_tokens
 
     def run_moe(self, residual, slots, slot_w, gamma, w_t, params=None, out_tokens=None, out_logits=None,
-                out_topk_vals=None, out_topk_idx=None, out_hidden=None, stream=None):
+                out_topk_vals=None, out_topk_idx=None, out_hidden=None, n_routed=None, stream=None):
         """The tail fused with its producer (tail_run_moe): residual [gbs, H] bf16, slots [gbs, S, H]
-        float32 or bf16, slot_w [gbs, S] float32; out_hidden [gbs, H] bf16 receives the combined h."""
+        float32 or bf16, slot_w [gbs, S] float32, n_routed the leading slots of the routed chain (None:
+        all S; the rest are shared slots, summed apart); out_hidden [gbs, H] bf16 receives the combined h."""
         import torch
         gbs = int(residual.shape[0])
         S = int(slots.shape[1]) if slots is not None else 0
+        nr = S if n_routed is None else int(n_routed)
         sd = TAIL_F32 if slots is None or slots.dtype == torch.float32 else TAIL_BF16
         ncols = int(params.shape[1]) if params is not None else 4
-        rc = tail_run_moe(self.h, _ptr(residual), _ptr(slots), sd, S, _ptr(slot_w), _ptr(gamma), _ptr(w_t),
+        rc = tail_run_moe(self.h, _ptr(residual), _ptr(slots), sd, S, nr, _ptr(slot_w), _ptr(gamma), _ptr(w_t),
                           _ptr(params), ncols, gbs, _ptr(out_tokens), _ptr(out_logits), _ptr(out_topk_vals),
                           _ptr(out_topk_idx), _ptr(out_hidden), self._stream(stream))
         if rc != TAIL_OK:

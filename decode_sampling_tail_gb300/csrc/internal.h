@@ -1,8 +1,11 @@
 // Host-side declarations shared by the translation units of libtail.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include "moe_internal.h"
 
 namespace tail {
 
@@ -91,7 +94,20 @@ struct GemvArgs {
   int sortP;                // composite buffer entries: max(next power of two >= K, RANK_SORT_MAX)
   uint64_t timeout_ns;
   int drop_iter;            // test hook: ring iteration the producer never issues (-1: none)
+  // fused form only: bytes of one slot of the hidden staging ring, and the producer step (the
+  // activation warp forms each row from the residual and up to MOE_FUSED_MAX_SLOTS expert slots)
+  int hid_slot_bytes = HID_SLOT_BYTES;
+  int use_moe = 0;
+  MoeIn moe;
+  // producer step: tensor maps of this pass's residual rows (2-D [B][H] bf16, box 32 x B) and
+  // slots (3-D [B][S][H], box 32 x MOE_FUSED_MAX_SLOTS x B: slots past S read as zeros)
+  CUtensorMap moe_map_x;
+  CUtensorMap moe_map_y;
 };
+// Byte offsets inside a staging slot of the producer-step form: the residual rows (64 bytes each),
+// then, from moe_y_offset, MOE_FUSED_MAX_SLOTS slot rows of 32 elements per batch row.
+__host__ __device__ inline int moe_y_offset(int B) { return (B * 64 + 127) & ~127; }
+__host__ __device__ inline int moe_slot_bytes_for(int B) { return moe_y_offset(B) + B * MOE_FUSED_MAX_SLOTS * 32 * 4; }
 
 // Launchers (all enqueue on `stream`; the lm_head tail is one launch,
 // chained to the previous kernel on the stream with programmatic dependent launch when pdl).
@@ -105,11 +121,14 @@ cudaError_t prepare_gemv(int max_smem_optin, int* max_dynamic);
 struct GemvPlan {
   int mt, pw, cb_pairs, pitch, kpb, stage_bytes, nstages, logits_in_smem, max_slab_cols, smem_bytes;
   int capc, sortP;
+  int hid_slot_bytes;  // one slot of the fused form's hidden staging ring
   bool ok;
 };
-// kpb: k-steps per ring stage (1 or 2); max_stages caps the ring depth
+// kpb: k-steps per ring stage (1 or 2); max_stages caps the ring depth.  moe_slots >= 0 plans the
+// fused form with the producer step inside the kernel: its hidden staging ring then holds the
+// bf16 residual and that many expert slots of moe_slot_bytes (4: fp32, 2: bf16) per element.
 GemvPlan plan_gemv(int B, int H, int V, int K, int nslab, int max_smem, int kpb = GEMV_KPB,
-                   int max_stages = GEMV_MAX_STAGES);
+                   int max_stages = GEMV_MAX_STAGES, int moe_slots = -1, int moe_slot_bytes = 4);
 constexpr int SEL_NPL = 48;          // register keys per lane of the slab selects: slabs up to 1536 columns
 
 }  // namespace tail

@@ -42,8 +42,10 @@
 //      draw, with every thread of the CTA.
 #include "common.cuh"
 #include "internal.h"
+#include "moe.cuh"
 #include "sampler.cuh"
 #include "select.cuh"
+#include "tc_common.cuh"
 
 namespace tail {
 
@@ -51,19 +53,17 @@ namespace {
 
 constexpr int MAX_STAGES = 8;
 constexpr int BAR_REGION = 256;  // ring barriers and control words at the start of shared memory
+constexpr int MOE_HID_DEPTH = 6;  // producer step: stages of residual and slot columns in flight
+constexpr int MOE_STAGE_BAR_OFF = 200;  // producer step: one mbarrier per staging slot
 constexpr int NLEAD_L = SLAB_BOUND_KEYS * ((MAX_SLABS + 31) / 32);  // leader keys per lane of the owner's bound
 constexpr int NGATHER = (MAX_SLABS * SLAB_CAND + GEMV_THREADS - 33) / (GEMV_THREADS - 32);  // slots per gatherer
 static_assert(SLAB_BOUND_KEYS == 4 && SLAB_META_WORDS == 8, "a slab's publication is two 16-byte stores");
 static_assert(SLAB_LEADERS >= SLAB_BOUND_KEYS && SLAB_LEADERS <= 32, "leaders are distinct lane maxima");
 static_assert(GEMV_KPB <= 2, "the pack warp's 32 lanes cover one stage's k columns");
+static_assert(MOE_FUSED_MAX_SLOTS == 8, "the activation warp reads a row's slot weights as two float4");
+static_assert(MOE_STAGE_BAR_OFF >= 200 && MOE_STAGE_BAR_OFF + 8 * MOE_HID_DEPTH <= BAR_REGION,
+              "the staging barriers sit after the ring barriers, the control words and the scale barrier");
 static_assert(SLAB_CAND == 32 && (GEMV_THREADS - 32) % 32 == 0, "the owner's gather reads one slab per warp step");
-
-// hidden element i widened exactly to fp32 (dtype 0: fp32, 1: fp16, 2: bf16)
-__device__ __forceinline__ float widen_elem(const void* p, int dtype, int64_t i) {
-  if (dtype == 0) return static_cast<const float*>(p)[i];
-  if (dtype == 1) return __half2float(static_cast<const __half*>(p)[i]);
-  return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
-}
 
 __device__ __forceinline__ uint32_t bf16_bits_rn(float v) {
   return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
@@ -382,7 +382,217 @@ __device__ __forceinline__ void own_rows(const GemvArgs& a, uint8_t* ring, int c
   }
 }
 
-template <int MT, int PW>
+// ================================================================ activations with the producer step
+// The activation warp of the fused form when the hidden state is formed in
+// the kernel from the bf16 residual and up to MOE_FUSED_MAX_SLOTS expert
+// slots (moe.cuh).  Per ring stage (k columns [32 js, 32 js + 32)):
+//   * two tensor copies (TMA) bring the stage's columns of every residual row
+//     and of every row's slots into a staging slot (MOE_HID_DEPTH slots in
+//     flight, one mbarrier each): the copy engine's path, as for W, with two
+//     requests a stage.  The slot box always spans MOE_FUSED_MAX_SLOTS slots;
+//     those past S read as zeros and their weights are zero, so the chains
+//     run over all of them (fma(+0, +0, acc) is acc: a chain from +0 never
+//     holds -0), with the routed-slot count as a compile-time constant;
+//   * the combine: lane (g, q) forms h = bf16(x + bf16(r + sh)) for columns
+//     [4q, 4q + 4) of rows g, g + 4, ... (vector loads of four columns, the
+//     routed and shared fma chains per column), writes h over the residual
+//     row in the staging slot, and CTA 0 also writes it to the caller's buffer;
+//   * then the plain fused form on h, lane j on column j as without the
+//     producer step (the same order of the squares' sums, so rstd is the one
+//     the tail computes on h given as its input): x^2 into the row's sum,
+//     a = h * gamma split into hi + lo, stored in A-fragment order and released
+//     by the lane's arrival on the stage's full barrier.
+template <int MT, int SZ, int NR>
+__device__ __forceinline__ void moe_combine_stage(const GemvArgs& a, uint8_t* slot, int ncols, int64_t c0,
+                                                  const float (&wl)[MT * 2][MOE_FUSED_MAX_SLOTS]) {
+  constexpr int NS = MOE_FUSED_MAX_SLOTS;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 3, q = lane & 7;
+  uint8_t* xq = slot + q * 8;
+  const uint8_t* yq = slot + moe_y_offset(a.B) + q * 4 * SZ;
+#pragma unroll
+  for (int p = 0; p < MT * 2; ++p) {
+    const int r = g + 4 * p;
+    if (r < a.B) {
+      float y[NS][4];
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        const uint8_t* e = yq + (r * NS + s) * 32 * SZ;
+        if constexpr (SZ == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(e);
+          y[s][0] = v.x; y[s][1] = v.y; y[s][2] = v.z; y[s][3] = v.w;
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2*>(e);
+          y[s][0] = __uint_as_float(v.x << 16); y[s][1] = __uint_as_float(v.x & 0xffff0000u);
+          y[s][2] = __uint_as_float(v.y << 16); y[s][3] = __uint_as_float(v.y & 0xffff0000u);
+        }
+      }
+      const uint2 xv = *reinterpret_cast<const uint2*>(xq + r * 64);
+      // slots past S are zero rows of zero weight: fma(+0, +0, acc) leaves acc (never -0) as it is
+      float rr[4] = {0.f, 0.f, 0.f, 0.f}, sh[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < NR; ++s)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) rr[j] = __fmaf_rn(wl[p][s], y[s][j], rr[j]);
+#pragma unroll
+      for (int s = NR; s < NS; ++s)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sh[j] = __fmaf_rn(wl[p][s], y[s][j], sh[j]);
+      const uint32_t h0 = moe_finish(xv.x & 0xffffu, rr[0], sh[0]), h1 = moe_finish(xv.x >> 16, rr[1], sh[1]);
+      const uint32_t h2 = moe_finish(xv.y & 0xffffu, rr[2], sh[2]), h3 = moe_finish(xv.y >> 16, rr[3], sh[3]);
+      const uint2 hv = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+      *reinterpret_cast<uint2*>(xq + r * 64) = hv;
+      if (a.moe.h_out != nullptr && blockIdx.x == 0 && q * 4 < ncols)
+        *reinterpret_cast<uint2*>(a.moe.h_out + static_cast<int64_t>(r) * a.H + c0 + q * 4) = hv;
+    }
+  }
+}
+
+// moe_combine_stage with the routed-slot count as a constant (the chains then carry no branch)
+template <int MT, int SZ>
+__device__ __forceinline__ void moe_combine_stage_nr(const GemvArgs& a, uint8_t* slot, int ncols, int64_t c0,
+                                                     const float (&wl)[MT * 2][MOE_FUSED_MAX_SLOTS]) {
+  switch (a.moe.n_routed) {
+    case 0: moe_combine_stage<MT, SZ, 0>(a, slot, ncols, c0, wl); break;
+    case 1: moe_combine_stage<MT, SZ, 1>(a, slot, ncols, c0, wl); break;
+    case 2: moe_combine_stage<MT, SZ, 2>(a, slot, ncols, c0, wl); break;
+    case 3: moe_combine_stage<MT, SZ, 3>(a, slot, ncols, c0, wl); break;
+    case 4: moe_combine_stage<MT, SZ, 4>(a, slot, ncols, c0, wl); break;
+    case 5: moe_combine_stage<MT, SZ, 5>(a, slot, ncols, c0, wl); break;
+    case 6: moe_combine_stage<MT, SZ, 6>(a, slot, ncols, c0, wl); break;
+    case 7: moe_combine_stage<MT, SZ, 7>(a, slot, ncols, c0, wl); break;
+    default: moe_combine_stage<MT, SZ, 8>(a, slot, ncols, c0, wl); break;
+  }
+}
+
+template <int MT>
+__device__ __forceinline__ void moe_activation_warp(const GemvArgs& a, uint8_t* smem, uint32_t full0, uint32_t empty0,
+                                                    uint32_t scale_bar, volatile int* s_abort, float* s_scale,
+                                                    int total, int spb) {
+  constexpr int NS = MOE_FUSED_MAX_SLOTS;
+  constexpr int ROWS = MT * MTILE_ROWS;
+  constexpr int DEPTH = MOE_HID_DEPTH;
+  const int lane = threadIdx.x & 31;
+  const int KPB = a.kpb, NST = a.nstages;
+  const int active_end = a.zero_pad ? a.H : a.Hu;
+  const int kc = lane & (KSTEP - 1), ksub = lane >> 4;  // a stage is at most two k-steps: 32 columns
+  const int col = ksub * KSTEP + kc;
+  const int S = a.moe.S;
+  const int sesz = a.moe.slot_dtype == 0 ? 4 : 2;
+  const int slot_bytes = a.hid_slot_bytes;
+  const int stg_off = BAR_REGION + NST * a.stage_bytes;  // the staging ring, after the weight ring
+  const uint32_t stg = smem_u32(smem) + static_cast<uint32_t>(stg_off);
+  const uint32_t sbar0 = smem_u32(smem + MOE_STAGE_BAR_OFF);
+  const uint32_t ring_u32 = smem_u32(smem + BAR_REGION);
+  const uint32_t xbytes = static_cast<uint32_t>(a.B) * 32u * 2u;
+  const uint32_t ybytes = S > 0 ? static_cast<uint32_t>(a.B) * NS * 32u * static_cast<uint32_t>(sesz) : 0u;
+  if (S == 0)  // no slot copy ever lands: the slot rows read as zeros in every staging slot
+    for (int d = 0; d < DEPTH; ++d) {
+      float* yrow = reinterpret_cast<float*>(smem + stg_off + d * slot_bytes + moe_y_offset(a.B));
+      for (int i = lane; i < a.B * NS * 32; i += 32) yrow[i] = 0.f;
+    }
+  pdl_wait();  // the residual, the slots and their weights may come from the previous kernel
+  float wl[MT * 2][NS];  // the weights of this lane's rows of the combine: g, g + 4, ...
+#pragma unroll
+  for (int p = 0; p < MT * 2; ++p) {
+    const int r = (lane >> 3) + 4 * p;
+#pragma unroll
+    for (int sl = 0; sl < NS; ++sl) wl[p][sl] = (r < a.B && sl < S) ? a.moe.w[r * S + sl] : 0.f;
+  }
+  __syncwarp();
+  const uint64_t pol = policy_evict_last();  // every CTA reads the same rows
+  auto issue = [&](int it) {
+    if (it >= total || lane != 0) return;
+    const int c0 = (it % spb) * KPB * KSTEP;
+    const uint32_t slot = stg + static_cast<uint32_t>((it % DEPTH) * slot_bytes);
+    const uint32_t bar = sbar0 + 8u * static_cast<uint32_t>(it % DEPTH);
+    mbar_arrive_expect_tx(bar, xbytes + ybytes);
+    tma_load_2d(slot, &a.moe_map_x, c0, 0, bar, pol);
+    if (S > 0) tma_load_3d(slot + static_cast<uint32_t>(moe_y_offset(a.B)), &a.moe_map_y, c0, 0, 0, bar, pol);
+  };
+  float ss[ROWS];
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) ss[r] = 0.f;
+  for (int p = 0; p < DEPTH - 1; ++p) issue(p);
+  int issued = min(DEPTH - 1, total);
+  int it = 0;
+  for (; it < total; ++it) {
+    issue(it + DEPTH - 1);  // into the slot the previous iteration finished reading
+    if (it + DEPTH - 1 < total) issued = it + DEPTH;
+    const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(sbar0 + 8u * static_cast<uint32_t>(it % DEPTH),
+                                                                   static_cast<uint32_t>(it / DEPTH) & 1u,
+                                                                   a.timeout_ns));
+    if (!landed) {
+      if (lane == 0) {
+        raise_error(a.err, DEV_TIMEOUT_FULL);
+        *s_abort = 1;
+      }
+      break;
+    }
+    const int js = it % spb;
+    const int kn = min(KPB, a.ksteps - js * KPB);
+    const int h = (js * KPB + ksub) * KSTEP + kc;
+    const bool in = ksub < kn;
+    const float gc = in && h < active_end ? a.gamma[h] : 0.f;
+    uint8_t* slot = smem + stg_off + (it % DEPTH) * slot_bytes;
+    if (sesz == 4)
+      moe_combine_stage_nr<MT, 4>(a, slot, kn * KSTEP, static_cast<int64_t>(js) * KPB * KSTEP, wl);
+    else
+      moe_combine_stage_nr<MT, 2>(a, slot, kn * KSTEP, static_cast<int64_t>(js) * KPB * KSTEP, wl);
+    fence_proxy_async_smem();  // h's stores, before a later tensor copy refills the slot
+    __syncwarp();  // h of every row is in the staging slot
+    float xc[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+      xc[r] = (in && h < active_end && r < a.B)
+                  ? __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(slot + r * 64 + col * 2)) << 16)
+                  : 0.f;
+    __syncwarp();  // the slot is refilled by the next iteration's copies
+    if (*s_abort) break;
+    if (it >= NST && !__all_sync(0xffffffffu, mbar_wait_bounded(empty0 + 8 * (it % NST),
+                                                                 static_cast<uint32_t>((it / NST) - 1) & 1u,
+                                                                 a.timeout_ns))) {
+      if (lane == 0) {
+        raise_error(a.err, DEV_TIMEOUT_EMPTY);
+        *s_abort = 1;
+      }
+      break;
+    }
+    const uint32_t wbase = ring_u32 + static_cast<uint32_t>((it % NST) * a.stage_bytes + KPB * KSTEP * a.pitch +
+                                                            ksub * MT * APACK_TILE_BYTES + ((kc & 7) >> 1) * 16 +
+                                                            (kc < 8 ? 0 : 8));
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      ss[r] = fmaf(xc[r], xc[r], ss[r]);
+      const float v = xc[r] * gc;
+      const uint32_t hi = bf16_bits_rn(v);
+      const uint32_t lo = bf16_bits_rn(v - __uint_as_float(hi << 16));
+      const uint32_t hi1 = __shfl_down_sync(0xffffffffu, hi, 1);
+      const uint32_t lo1 = __shfl_down_sync(0xffffffffu, lo, 1);
+      if (in && (kc & 1) == 0)
+        st_shared_v2(wbase + static_cast<uint32_t>(((r >> 3) * 32 + (r & 7) * 4) * 16), hi | (hi1 << 16),
+                     lo | (lo1 << 16));
+    }
+    mbar_arrive(full0 + 8 * (it % NST));  // each lane releases its own stores
+  }
+  // no copy may land after the warp moves on: wait (bounded) for the staging slots still in flight
+  for (int j = it; j < issued; ++j)
+    if (!mbar_wait_bounded(sbar0 + 8u * static_cast<uint32_t>(j % DEPTH), static_cast<uint32_t>(j / DEPTH) & 1u,
+                           DEFAULT_TIMEOUT_NS)) {
+      if (lane == 0) raise_error(a.err, DEV_TIMEOUT_DRAIN);
+      break;
+    }
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    float t = ss[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) s_scale[r] = r < a.B ? 1.0f / sqrtf(t / static_cast<float>(a.Hu) + a.eps) : 0.f;
+  }
+  if (lane == 0) mbar_arrive(scale_bar);
+}
+
+template <int MT, int PW, bool MOE>
 __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint32_t s_red[64];
@@ -419,6 +629,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
       mbar_init(empty0 + 8 * s, GEMV_CONSUMER_WARPS);
     }
     mbar_init(scale_bar, 1);
+    if constexpr (MOE)
+      for (int d = 0; d < MOE_HID_DEPTH; ++d) mbar_init(smem_u32(smem + MOE_STAGE_BAR_OFF) + 8 * d, 1);
     *s_abort = 0;
     *s_consumed_min = total;
     *s_issued = 0;
@@ -489,6 +701,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
     // A-fragment order the RMSNorm kernel uses; its arrival on the stage's full
     // barrier releases them.  After the last stage, rstd = 1 / sqrt(ss / H_u +
     // eps) per row (fixed order: lane sums, then an xor butterfly).
+    if constexpr (MOE) {  // the same, with the hidden state formed from the residual and the slots
+      if (a.fused) moe_activation_warp<MT>(a, smem, full0, empty0, scale_bar, s_abort, s_scale, total, spb);
+    } else {
     if constexpr (MT <= FUSED_MAX_MT) {  // larger batches take the RMSNorm kernel (registers)
     if (a.fused) {
       pdl_wait();  // hidden may come from the previous kernel
@@ -574,6 +789,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
         if (lane == 0) s_scale[r] = r < a.B ? 1.0f / sqrtf(t / static_cast<float>(a.Hu) + a.eps) : 0.f;
       }
       if (lane == 0) mbar_arrive(scale_bar);
+    }
     }
     }
   } else {
@@ -723,7 +939,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) lmhead_tail_kernel(const __gr
   pdl_launch_dependents();
 }
 
-template <int MT, int PW>
+template <int MT, int PW, bool MOE>
 cudaError_t launch_t(const GemvArgs& a, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nslab);
@@ -737,7 +953,7 @@ cudaError_t launch_t(const GemvArgs& a, cudaStream_t stream, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, lmhead_tail_kernel<MT, PW>, a);
+  return cudaLaunchKernelEx(&cfg, lmhead_tail_kernel<MT, PW, MOE>, a);
 }
 
 int mt_template(int B) {
@@ -753,7 +969,8 @@ int next_pow2(int x) {
 
 }  // namespace
 
-GemvPlan plan_gemv(int B, int H, int V, int K, int nslab, int max_smem, int kpb, int max_stages) {
+GemvPlan plan_gemv(int B, int H, int V, int K, int nslab, int max_smem, int kpb, int max_stages, int moe_slots,
+                   int moe_slot_bytes) {
   (void)H;
   GemvPlan p = {};
   p.mt = mt_template(B);
@@ -766,7 +983,12 @@ GemvPlan plan_gemv(int B, int H, int V, int K, int nslab, int max_smem, int kpb,
   p.kpb = kpb;
   p.stage_bytes = ((kpb * (KSTEP * p.pitch + p.mt * APACK_TILE_BYTES)) + 127) & ~127;
   const int budget = max_smem - BAR_REGION;
-  const int hid = p.mt <= FUSED_MAX_MT ? HID_DEPTH * HID_SLOT_BYTES : 0;  // fused: hidden staging after the ring
+  // fused: hidden staging after the ring (with the producer step: the residual rows, then
+  // MOE_FUSED_MAX_SLOTS slot rows per batch row)
+  p.hid_slot_bytes = moe_slots >= 0 ? moe_slot_bytes_for(B) : HID_SLOT_BYTES;
+  const int hid = p.mt <= FUSED_MAX_MT ? (moe_slots >= 0 ? MOE_HID_DEPTH : HID_DEPTH) * p.hid_slot_bytes : 0;
+  const bool moe_ok = moe_slots < 0 || (moe_slots <= MOE_FUSED_MAX_SLOTS && (moe_slot_bytes == 4 || moe_slot_bytes == 2) &&
+                                        p.mt <= FUSED_MAX_MT);
   p.nstages = (budget - hid) / p.stage_bytes;
   if (p.nstages > max_stages) p.nstages = max_stages;
   if (p.nstages > MAX_STAGES) p.nstages = MAX_STAGES;
@@ -789,17 +1011,19 @@ GemvPlan plan_gemv(int B, int H, int V, int K, int nslab, int max_smem, int kpb,
   if (p.smem_bytes > max_smem) p.smem_bytes = max_smem;
   p.capc = ((p.smem_bytes - BAR_REGION - fixed_c) / 8) & ~3;
   if (p.capc > want_capc) p.capc = want_capc;
-  p.ok = p.nstages >= 2 && p.capc >= 2 * K && p.capc >= need_capc && nslab <= MAX_SLABS &&
+  p.ok = moe_ok && p.nstages >= 2 && p.capc >= 2 * K && p.capc >= need_capc && nslab <= MAX_SLABS &&
          BAR_REGION + ring <= max_smem &&
          (!p.logits_in_smem || BAR_REGION + smem_logits <= max_smem);
   return p;
 }
 
 cudaError_t prepare_gemv(int max_smem_optin, int* max_dynamic) {
-  const void* fns[] = {reinterpret_cast<const void*>(lmhead_tail_kernel<1, 12>),
-                       reinterpret_cast<const void*>(lmhead_tail_kernel<2, 6>),
-                       reinterpret_cast<const void*>(lmhead_tail_kernel<4, 3>),
-                       reinterpret_cast<const void*>(lmhead_tail_kernel<8, 1>)};
+  const void* fns[] = {reinterpret_cast<const void*>(lmhead_tail_kernel<1, 12, false>),
+                       reinterpret_cast<const void*>(lmhead_tail_kernel<2, 6, false>),
+                       reinterpret_cast<const void*>(lmhead_tail_kernel<4, 3, false>),
+                       reinterpret_cast<const void*>(lmhead_tail_kernel<8, 1, false>),
+                       reinterpret_cast<const void*>(lmhead_tail_kernel<1, 12, true>),
+                       reinterpret_cast<const void*>(lmhead_tail_kernel<2, 6, true>)};
   int dyn = max_smem_optin;
   for (const void* fn : fns) {
     cudaFuncAttributes fa;
@@ -817,11 +1041,19 @@ cudaError_t prepare_gemv(int max_smem_optin, int* max_dynamic) {
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t stream, bool pdl) {
+  if (a.use_moe) {  // the producer step inside the activation warp: fused form only
+    if (!a.fused) return cudaErrorInvalidValue;
+    switch (a.mt) {
+      case 1: return launch_t<1, 12, true>(a, stream, pdl);
+      case 2: return launch_t<2, 6, true>(a, stream, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.mt) {
-    case 1: return launch_t<1, 12>(a, stream, pdl);
-    case 2: return launch_t<2, 6>(a, stream, pdl);
-    case 4: return launch_t<4, 3>(a, stream, pdl);
-    case 8: return launch_t<8, 1>(a, stream, pdl);
+    case 1: return launch_t<1, 12, false>(a, stream, pdl);
+    case 2: return launch_t<2, 6, false>(a, stream, pdl);
+    case 4: return launch_t<4, 3, false>(a, stream, pdl);
+    case 8: return launch_t<8, 1, false>(a, stream, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -16,6 +16,7 @@
 // Rows in [B, B_pad) are written as zeros so the last m-tile is complete.
 #include "common.cuh"
 #include "internal.h"
+#include "moe.cuh"
 #include "tc_internal.h"
 
 namespace tail {
@@ -116,20 +117,39 @@ __global__ void __launch_bounds__(RMS_THREADS) rms_pack_kernel(RmsArgs a) {
 // The same RMSNorm for the tensor-core path: the hi and lo parts of row b go
 // to two plain bf16 rows of the activation buffer (K contiguous), laid out as
 // tc_act_rows describes.  rstd is computed exactly as in rms_pack_kernel.
-template <int DT>
+// MOE: the row is first formed by the producer step (moe.cuh) from the
+// residual and the expert slots -- h, kept in shared memory as bf16 and
+// written to the caller's buffer when one is given -- and the RMSNorm runs on
+// it in the same order as on a bf16 input.
+template <int DT, bool MOE>
 __global__ void __launch_bounds__(RMS_THREADS) rms_split_kernel(SplitArgs a) {
   pdl_wait();  // the activation buffer is reused across steps
   pdl_launch_dependents();
   __shared__ float red[RMS_THREADS / 32];
   __shared__ float s_rstd;
+  extern __shared__ uint16_t s_h[];  // MOE: the row's h
   const int b = blockIdx.x;
   const int H = a.H;
   const int64_t row = static_cast<int64_t>(b) * H;
   const int active_end = a.zero_pad ? H : a.Hu;
+  auto elem = [&](int h) -> float {
+    if constexpr (MOE) return __uint_as_float(static_cast<uint32_t>(s_h[h]) << 16);
+    else return load_widen<DT>(a.hidden, row + h);
+  };
   float ss = 0.f;
-  for (int h = threadIdx.x; h < active_end; h += RMS_THREADS) {
-    const float v = load_widen<DT>(a.hidden, row + h);
-    ss = fmaf(v, v, ss);
+  if constexpr (MOE) {
+    for (int h = threadIdx.x; h < H; h += RMS_THREADS) {
+      const uint32_t hb = moe_lane_h(a.moe, b, H, h);
+      s_h[h] = static_cast<uint16_t>(hb);
+      if (a.moe.h_out) a.moe.h_out[row + h] = static_cast<uint16_t>(hb);
+      const float v = __uint_as_float(hb << 16);
+      if (h < active_end) ss = fmaf(v, v, ss);
+    }
+  } else {
+    for (int h = threadIdx.x; h < active_end; h += RMS_THREADS) {
+      const float v = load_widen<DT>(a.hidden, row + h);
+      ss = fmaf(v, v, ss);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -153,7 +173,7 @@ __global__ void __launch_bounds__(RMS_THREADS) rms_split_kernel(SplitArgs a) {
     for (int j = 0; j < 2; ++j) {
       const int h = h2 + j;
       float v = 0.f;
-      if (h < active_end) v = (load_widen<DT>(a.hidden, row + h) * pre) * a.gamma[h];
+      if (h < active_end) v = (elem(h) * pre) * a.gamma[h];
       hi[j] = bf16_bits(v);
       lo[j] = bf16_bits(v - __uint_as_float(hi[j] << 16));
     }
@@ -169,17 +189,21 @@ cudaError_t launch_split(const SplitArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.B);
   cfg.blockDim = dim3(RMS_THREADS);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = a.use_moe ? static_cast<size_t>(a.H) * 2 : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (a.use_moe) {
+    if (a.H > SPLIT_MOE_MAX_H) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, rms_split_kernel<2, true>, a);
+  }
   switch (a.dtype) {
-    case 0: return cudaLaunchKernelEx(&cfg, rms_split_kernel<0>, a);
-    case 1: return cudaLaunchKernelEx(&cfg, rms_split_kernel<1>, a);
-    case 2: return cudaLaunchKernelEx(&cfg, rms_split_kernel<2>, a);
+    case 0: return cudaLaunchKernelEx(&cfg, rms_split_kernel<0, false>, a);
+    case 1: return cudaLaunchKernelEx(&cfg, rms_split_kernel<1, false>, a);
+    case 2: return cudaLaunchKernelEx(&cfg, rms_split_kernel<2, false>, a);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -166,6 +166,32 @@ bool encode_2d(CUtensorMap* map, const void* base, bool fp32, uint64_t cols, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of one producer-step pass of B rows (the lm_head kernel's activation warp loads a
+// stage's 32 columns of every row with one copy each): the residual [B][H] bf16, box 32 x B, and
+// the slots [B][S][H], box 32 x MOE_FUSED_MAX_SLOTS x B (slots past S read as zeros).  No swizzle:
+// the boxes land as plain rows.
+bool encode_moe_maps(GemvArgs& ga, const MoeIn& m, int B, int H) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint64_t xdims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t xstr[1] = {static_cast<cuuint64_t>(H) * 2};
+  const cuuint32_t xbox[2] = {32, static_cast<cuuint32_t>(B)};
+  if (fn(&ga.moe_map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(m.x), xdims, xstr, xbox, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  if (m.S == 0) return true;
+  const cuuint64_t esz = m.slot_dtype == 0 ? 4 : 2;
+  const cuuint64_t ydims[3] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(m.S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t ystr[2] = {static_cast<cuuint64_t>(H) * esz, static_cast<cuuint64_t>(m.S) * H * esz};
+  const cuuint32_t ybox[3] = {32, MOE_FUSED_MAX_SLOTS, static_cast<cuuint32_t>(B)};
+  return fn(&ga.moe_map_y, m.slot_dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(m.slots), ydims, ystr, ybox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -311,7 +337,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
 // Batches of tc_min rows or more: split -> tensor-core lm_head -> merge + sampler, one pass.
 static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
                   int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits, float* out_topk_vals,
-                  int32_t* out_topk_idx, cudaStream_t stream) {
+                  int32_t* out_topk_idx, cudaStream_t stream, const MoeIn* moe) {
   const tail_config& c = h->cfg;
   const int stacked = tc_stacked(gbs);
   const int n_mb = tc_mblocks(gbs);
@@ -349,6 +375,10 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   sa.stacked = stacked;
   sa.act = h->tc_act;
   sa.row_scale = h->tc_rs;
+  if (moe) {  // the split kernel forms each row from the residual and the slots itself
+    sa.use_moe = 1;
+    sa.moe = *moe;
+  }
   cudaError_t e = launch_split(sa, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch (split)");
   if (ev) cudaEventRecord(ev[1], stream);
@@ -397,20 +427,45 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   return TAIL_OK;
 }
 
+// Slot element bytes of a producer step.
+static int moe_slot_bytes(const MoeIn& m) { return m.slot_dtype == 0 ? 4 : 2; }
+
+// Whether every pass of a batch of gbs rows can run the producer step inside its first kernel:
+// the split kernel on the tensor-core path; the lm_head kernel's activation warp (fused deferred
+// form, at most MOE_FUSED_MAX_SLOTS slots, 16-byte aligned slots) on the mma.sync path.
+static bool moe_fusable(const tail_t* h, int gbs, const MoeIn& m) {
+  const tail_config& c = h->cfg;
+  if (h->tc_min > 0 && gbs >= h->tc_min) return c.H <= SPLIT_MOE_MAX_H;
+  if (h->rows_pass <= 0 || !c.deferred_rms || m.S > MOE_FUSED_MAX_SLOTS || !encode_tiled()) return false;
+  if (m.S > 0 && !aligned(m.slots, 16)) return false;
+  const int sizes[2] = {gbs < h->rows_pass ? gbs : h->rows_pass, gbs % h->rows_pass};
+  for (int B : sizes) {
+    if (B == 0) continue;
+    const GemvPlan p = plan_gemv(B, c.H, c.V, c.k, h->nslab, h->max_smem, GEMV_KPB, GEMV_MAX_STAGES, m.S,
+                                 moe_slot_bytes(m));
+    if (!p.ok || !p.logits_in_smem || p.mt > FUSED_MAX_MT) return false;
+  }
+  return true;
+}
+
+// moe: run the producer step inside the first kernel of every pass (moe_fusable holds); hidden is
+// then unused.
 static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t,
                     const float* params, int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits,
-                    float* out_topk_vals, int32_t* out_topk_idx, cudaStream_t stream) {
+                    float* out_topk_vals, int32_t* out_topk_idx, cudaStream_t stream, const MoeIn* moe = nullptr) {
   const tail_config& c = h->cfg;
   if (h->tc_min > 0 && gbs >= h->tc_min)
     return run_tc(h, hidden, gamma, w_t, params, ncols, gbs, out_tokens, out_logits, out_topk_vals, out_topk_idx,
-                  stream);
+                  stream, moe);
   if (h->rows_pass <= 0) return TAIL_ERR_UNSUPPORTED;  // no mma.sync scratch (not reached: tc_min is 1)
   const int K = c.k;
   const int64_t npairs = c.V / 16;
   cudaError_t e = cudaSuccess;
   for (int r0 = 0; r0 < gbs && e == cudaSuccess; r0 += h->rows_pass) {
     const int B = gbs - r0 < h->rows_pass ? gbs - r0 : h->rows_pass;
-    const GemvPlan plan = plan_gemv(B, c.H, c.V, K, h->nslab, h->max_smem);
+    const GemvPlan plan = moe ? plan_gemv(B, c.H, c.V, K, h->nslab, h->max_smem, GEMV_KPB, GEMV_MAX_STAGES, moe->S,
+                                          moe_slot_bytes(*moe))
+                              : plan_gemv(B, c.H, c.V, K, h->nslab, h->max_smem);
     cudaEvent_t* ev = (h->prof_on && h->prof_n < PROF_MAX) ? h->prof_ev + h->prof_n * PROF_EV : nullptr;
     if (ev) {
       ++h->prof_n;
@@ -418,7 +473,8 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     }
 
     RmsArgs ra;
-    ra.hidden = static_cast<const uint8_t*>(hidden) + static_cast<int64_t>(r0) * c.H * elem_bytes(c.hidden_dtype);
+    ra.hidden = hidden ? static_cast<const uint8_t*>(hidden) + static_cast<int64_t>(r0) * c.H * elem_bytes(c.hidden_dtype)
+                       : nullptr;  // null with the producer step: the lm_head kernel forms the rows
     ra.dtype = c.hidden_dtype;
     ra.gamma = gamma;
     ra.B = B;
@@ -433,6 +489,7 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     ra.row_scale = h->row_scale;
     // deferred RMSNorm with the slab logits in shared memory: the lm_head kernel forms the activations
     const bool fused = c.deferred_rms && plan.logits_in_smem && plan.mt <= FUSED_MAX_MT;
+    if (moe && !fused) return TAIL_ERR_UNSUPPORTED;  // not reached: moe_fusable holds
     if (!fused) {
       e = launch_rms_pack(ra, stream);
       if (e != cudaSuccess) break;
@@ -484,6 +541,20 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     ga.sortP = plan.sortP;
     ga.timeout_ns = h->wait_limit_ns;
     ga.drop_iter = h->drop_iter;
+    ga.hid_slot_bytes = plan.hid_slot_bytes;
+    if (moe) {  // this pass's rows of the residual, the slots, their weights and h
+      ga.use_moe = 1;
+      ga.moe = *moe;
+      ga.moe.x = moe->x + static_cast<int64_t>(r0) * c.H;
+      ga.moe.slots = static_cast<const uint8_t*>(moe->slots) +
+                     static_cast<int64_t>(r0) * moe->S * c.H * moe_slot_bytes(*moe);
+      ga.moe.w = moe->w + static_cast<int64_t>(r0) * moe->S;
+      ga.moe.h_out = moe->h_out ? moe->h_out + static_cast<int64_t>(r0) * c.H : nullptr;
+      if (!encode_moe_maps(ga, ga.moe, B, c.H)) {
+        set_last_error("cuTensorMapEncodeTiled rejected a tensor map of the producer step");
+        return TAIL_ERR_CUDA;
+      }
+    }
     if (h->pdl_ok) {
       e = launch_gemv(ga, stream, true);
       if (e != cudaSuccess) {  // this runtime refuses programmatic serialization: launch without the overlap
@@ -532,13 +603,14 @@ int tail_run_ex(tail_t* h, const void* hidden, const float* gamma, const uint16_
 }
 
 int tail_run_moe(tail_t* h, const uint16_t* residual, const void* slots, int32_t slot_dtype, int32_t nslots,
-                 const float* slot_w, const float* gamma, const uint16_t* w_t, const float* params,
+                 int32_t n_routed, const float* slot_w, const float* gamma, const uint16_t* w_t, const float* params,
                  int32_t n_param_cols, int32_t gbs, int32_t* out_tokens, float* out_logits_opt,
                  float* out_topk_vals_opt, int32_t* out_topk_idx_opt, uint16_t* out_hidden_opt, void* stream) {
   if (!h) return TAIL_ERR_INVALID_ARG;
   if (h->cfg.hidden_dtype != TAIL_BF16) return TAIL_ERR_UNSUPPORTED;  // the residual stream is bf16
   if (nslots < 0 || nslots > TAIL_MOE_MAX_SLOTS || (slot_dtype != TAIL_F32 && slot_dtype != TAIL_BF16))
     return TAIL_ERR_INVALID_ARG;
+  if (n_routed < 0 || n_routed > nslots) return TAIL_ERR_INVALID_ARG;
   if (nslots > 0 && (!slots || !slot_w || !aligned(slots, 4) || !aligned(slot_w, 4))) return TAIL_ERR_INVALID_ARG;
   if (out_hidden_opt && !aligned(out_hidden_opt, 16)) return TAIL_ERR_INVALID_ARG;
   int rc = validate_run(h, residual, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt,
@@ -547,25 +619,27 @@ int tail_run_moe(tail_t* h, const uint16_t* residual, const void* slots, int32_t
   DeviceGuard guard(h->device);
   if (!guard.ok) return TAIL_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MoeIn m;
+  m.x = residual;
+  m.slots = slots;
+  m.slot_dtype = slot_dtype == TAIL_F32 ? 0 : 2;
+  m.w = slot_w;
+  m.S = nslots;
+  m.n_routed = n_routed;
+  m.h_out = out_hidden_opt;
+  if (moe_fusable(h, gbs, m))  // one launch fewer: the first kernel of the tail forms h itself
+    return run_impl(h, nullptr, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt,
+                    out_topk_vals_opt, out_topk_idx_opt, s, &m);
   // h lands in the caller's buffer, else in the handle's hidden staging (gbs_max x H bf16)
-  uint16_t* hb = out_hidden_opt ? out_hidden_opt : reinterpret_cast<uint16_t*>(h->st_hidden);
-  MoeArgs ma;
-  ma.x = residual;
-  ma.slots = slots;
-  ma.slot_dtype = slot_dtype == TAIL_F32 ? 0 : 2;
-  ma.w = slot_w;
-  ma.h = hb;
-  ma.B = gbs;
-  ma.H = h->cfg.H;
-  ma.S = nslots;
-  cudaError_t e = launch_moe_combine(ma, s, h->pdl_ok != 0);
+  m.h_out = out_hidden_opt ? out_hidden_opt : reinterpret_cast<uint16_t*>(h->st_hidden);
+  cudaError_t e = launch_moe_combine(m, gbs, h->cfg.H, s, h->pdl_ok != 0);
   if (e != cudaSuccess && h->pdl_ok) {  // this runtime refuses programmatic serialization
     cudaGetLastError();
     h->pdl_ok = 0;
-    e = launch_moe_combine(ma, s, false);
+    e = launch_moe_combine(m, gbs, h->cfg.H, s, false);
   }
   if (e != cudaSuccess) return cuda_fail(e, "tail_run_moe: kernel launch");
-  return run_impl(h, hb, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, out_topk_vals_opt,
+  return run_impl(h, m.h_out, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, out_topk_vals_opt,
                   out_topk_idx_opt, s);
 }
 

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "moe_internal.h"
+
 namespace tail {
 
 constexpr int TC_M = 128;        // rows of one MMA tile (tensor-memory lanes)
@@ -43,7 +45,11 @@ struct SplitArgs {
   int stacked;
   uint16_t* act;     // [tc_act_rows(B)][H] bf16 bits
   float* row_scale;  // [B]: rstd (deferred) or 1
+  int use_moe = 0;   // 1: the rows are formed by the producer step from `moe` (hidden is unused)
+  MoeIn moe;
 };
+// widest hidden state the split kernel forms from the producer step itself (h row in shared memory)
+constexpr int SPLIT_MOE_MAX_H = 24576;
 
 struct TcArgs {
   const float* row_scale;  // [B]

@@ -149,30 +149,41 @@ int tail_run_ex(tail_t* h, const void* hidden, const float* gamma, const uint16_
  * The tail fused with its producer: the MoE combine and residual add that form
  * the bf16 hidden state ("nemotron CUDA: RMSNorm rows run on the shared norms
  * and combine (#548, step 1)", TensorFold pull request #1353, section "What
- * moves", entry tf_nemo_add_moe_norm / tf_moe_add_rms_rows_bf16h; "GPT-OSS
- * Tail Chunked Megakernel Kernel API
- * Reference", parameter `hidden_states`: a 16-bit producer output feeds the
- * norm directly).  For every row b and hidden lane j:
- *   acc = 0;  acc = fp32 fma(slot_w[b][s], slots[b][s][j], acc) for s = 0 .. nslots-1
- *   h[b][j] = bf16(residual[b][j] + bf16(acc))     (bf16: nearest, ties to even)
- * then the tail of tail_run_ex on h.  Requires cfg.hidden_dtype == TAIL_BF16.
+ * moves", entry tf_nemo_add_moe_norm / tf_moe_add_rms_rows_bf16h, and its
+ * author's fix reply: the fused residual keeps the routed chain and the shared
+ * sum apart; "GPT-OSS Tail Chunked Megakernel Kernel API Reference", parameter
+ * `hidden_states`: a 16-bit producer output feeds the norm directly).  For
+ * every row b and hidden lane j:
+ *   r  = 0;  r  = fp32 fma(slot_w[b][s], slots[b][s][j], r)  for s = 0 .. n_routed-1
+ *   sh = 0;  sh = fp32 fma(slot_w[b][s], slots[b][s][j], sh) for s = n_routed .. nslots-1
+ *   h[b][j] = bf16(residual[b][j] + bf16(r + sh))      (bf16: nearest, ties to even)
+ * (Nemotron: 6 routed slots, then 2 shared slots of weight 1, whose chain is
+ * the plain sum s0 + s1), then the tail of tail_run_ex on h.  Requires
+ * cfg.hidden_dtype == TAIL_BF16.
  *   residual       [gbs, H] bf16 bit patterns, 16-byte aligned.
  *   slots          [gbs, nslots, H] expert outputs, fp32 (slot_dtype TAIL_F32) or bf16
  *                  bit patterns (TAIL_BF16), 4-byte aligned; may be NULL when nslots == 0.
- *   nslots         0 .. TAIL_MOE_MAX_SLOTS (8 for Nemotron: 6 routed + 2 shared).
+ *   nslots         0 .. TAIL_MOE_MAX_SLOTS.
+ *   n_routed       0 .. nslots: the leading slots that form the routed chain; the
+ *                  others are shared (n_routed == nslots: no shared slot).
  *   slot_w         [gbs, nslots] fp32 weights, 4-byte aligned.
- *   out_hidden_opt [gbs, H] bf16 h, 16-byte aligned, or NULL (h then stays in the
- *                  handle's scratch).
- * The other arguments are those of tail_run_ex.  Two launches (the combine,
- * then the tail) chained with programmatic dependent launch.  Returns
+ *   out_hidden_opt [gbs, H] bf16 h, 16-byte aligned, or NULL.
+ * The other arguments are those of tail_run_ex.  Launches: the tail's own
+ * (h is formed inside its first kernel: on the tensor-core path by the
+ * RMSNorm split for H <= 24576; on the mma.sync path by the lm_head kernel's
+ * activation warp in the deferred form, for up to 8 slots whose pointer is
+ * 16-byte aligned).  Otherwise one more kernel forms h first (into
+ * out_hidden_opt, else the handle's scratch), chained with programmatic
+ * dependent launch.  h is bitwise the same either way.  Returns
  * TAIL_ERR_UNSUPPORTED for a non-bf16 config, TAIL_ERR_INVALID_ARG for bad
- * pointers, alignment, sizes or slot dtype.
+ * pointers, alignment, sizes, slot counts or slot dtype.
  */
 #define TAIL_MOE_MAX_SLOTS 256
 int tail_run_moe(tail_t* h, const uint16_t* residual, const void* slots, int32_t slot_dtype, int32_t nslots,
-                 const float* slot_w, const float* gamma, const uint16_t* w_t, const float* params,
-                 int32_t n_param_cols, int32_t gbs, int32_t* out_tokens, float* out_logits_opt,
-                 float* out_topk_vals_opt, int32_t* out_topk_idx_opt, uint16_t* out_hidden_opt, void* stream);
+                 int32_t n_routed, const float* slot_w, const float* gamma, const uint16_t* w_t,
+                 const float* params, int32_t n_param_cols, int32_t gbs, int32_t* out_tokens,
+                 float* out_logits_opt, float* out_topk_vals_opt, int32_t* out_topk_idx_opt,
+                 uint16_t* out_hidden_opt, void* stream);
 
 /*
  * End-to-end form for callers holding the per-step inputs in host memory:
