@@ -34,7 +34,7 @@ TC_ALL_ROWS_MAX_V = 131072
 EXPORTS = ("tail_create", "tail_run", "tail_run_ex", "tail_run_host", "tail_check", "tail_get_info",
            "tail_destroy", "tail_status_string", "tail_profile_enable", "tail_profile_read",
            "tail_set_wait_limit", "tail_debug_drop_stage", "tail_last_error", "tail_run_noalloc",
-           "tail_merge_shards", "tail_run_moe")
+           "tail_merge_shards", "tail_run_moe", "tail_tap_shape", "tail_run_taps")
 KERNELS = ("rms_rows", "lm_head", "merge")
 
 
@@ -91,6 +91,10 @@ def lib(path: str | None = None):
         L.tail_run_ex.restype = ctypes.c_int
         L.tail_run_moe.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, i32, i32, P, P, P, P, P, P]
         L.tail_run_moe.restype = ctypes.c_int
+        L.tail_tap_shape.argtypes = [P, i32, P, P, P, P]
+        L.tail_tap_shape.restype = ctypes.c_int
+        L.tail_run_taps.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P, P, P, P, P, P]
+        L.tail_run_taps.restype = ctypes.c_int
         L.tail_run_host.argtypes = [P, P, P, P, P, i32, i32, P, P, P]
         L.tail_run_host.restype = ctypes.c_int
         L.tail_run_noalloc.argtypes = [ctypes.POINTER(tail_config), P, P, P, P, i32, i32, P, P, P, P]
@@ -320,6 +324,37 @@ class Tail:
         if rc != TAIL_OK:
             raise TailError(rc, "tail_run_moe")
         return out_tokens
+
+    def tap_shape(self, gbs):
+        """(kind, n_chunks, cap, chunk_lo) of tail_tap_shape: kind 1 = slabs, 2 = tiles; chunk_lo a list of
+        n_chunks + 1 vocabulary ids (the chunks' first ids, then V)."""
+        kind, n, cap = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        rc = lib().tail_tap_shape(self.h, gbs, ctypes.byref(kind), ctypes.byref(n), ctypes.byref(cap), None)
+        if rc != TAIL_OK:
+            raise TailError(rc, "tail_tap_shape")
+        lo = (ctypes.c_int32 * (n.value + 1))()
+        lib().tail_tap_shape(self.h, gbs, ctypes.byref(kind), ctypes.byref(n), ctypes.byref(cap), lo)
+        return kind.value, n.value, cap.value, list(lo)
+
+    def run_taps(self, hidden, gamma, w_t, params=None, out_tokens=None, out_logits=None, out_topk_vals=None,
+                 out_topk_idx=None, stream=None):
+        """tail_run_taps: the run plus its stage-1 taps, returned as torch tensors
+        (vals [gbs, n, cap] float32, idx [gbs, n, cap] int32, count [gbs, n] int32, bound [gbs, n] float32)."""
+        import torch
+        gbs = int(hidden.shape[0])
+        _, n, cap, _ = self.tap_shape(gbs)
+        dev = hidden.device
+        vals = torch.empty((gbs, n, cap), dtype=torch.float32, device=dev)
+        idx = torch.empty((gbs, n, cap), dtype=torch.int32, device=dev)
+        count = torch.empty((gbs, n), dtype=torch.int32, device=dev)
+        bound = torch.empty((gbs, n), dtype=torch.float32, device=dev)
+        ncols = int(params.shape[1]) if params is not None else 4
+        rc = lib().tail_run_taps(self.h, _ptr(hidden), _ptr(gamma), _ptr(w_t), _ptr(params), ncols, gbs,
+                                 _ptr(out_tokens), _ptr(out_logits), _ptr(out_topk_vals), _ptr(out_topk_idx),
+                                 _ptr(vals), _ptr(idx), _ptr(count), _ptr(bound), self._stream(stream))
+        if rc != TAIL_OK:
+            raise TailError(rc, "tail_run_taps")
+        return vals, idx, count, bound
 
     def run_host(self, hidden_host, gamma, w_t, params_host=None, out_tokens_host=None,
                  out_logits_host=None, stream=None):

@@ -18,6 +18,7 @@
 #include "abi_common.h"
 #include "internal.h"
 #include "moe_internal.h"
+#include "taps_internal.h"
 #include "tc_internal.h"
 
 using namespace tail;
@@ -641,6 +642,69 @@ int tail_run_moe(tail_t* h, const uint16_t* residual, const void* slots, int32_t
   if (e != cudaSuccess) return cuda_fail(e, "tail_run_moe: kernel launch");
   return run_impl(h, m.h_out, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, out_topk_vals_opt,
                   out_topk_idx_opt, s);
+}
+
+int tail_tap_shape(const tail_t* h, int32_t gbs, int32_t* kind, int32_t* n_chunks, int32_t* cap,
+                   int32_t* chunk_lo_host_opt) {
+  if (!h || !kind || !n_chunks || !cap || gbs < 1 || gbs > h->cfg.gbs_max) return TAIL_ERR_INVALID_ARG;
+  const int V = h->cfg.V;
+  if (h->tc_min > 0 && gbs >= h->tc_min) {
+    const int tn = tc_tile_n(gbs);
+    *kind = TAP_TILES;
+    *n_chunks = tc_col_tiles(V, tn);
+    *cap = TC_LIST;
+    if (chunk_lo_host_opt) {
+      for (int c = 0; c < *n_chunks; ++c) chunk_lo_host_opt[c] = c * tn;
+      chunk_lo_host_opt[*n_chunks] = V;
+    }
+  } else {
+    const int64_t npairs = V / 16;
+    *kind = TAP_SLABS;
+    *n_chunks = h->nslab;
+    *cap = SLAB_CAND;
+    if (chunk_lo_host_opt)
+      for (int c = 0; c <= h->nslab; ++c) chunk_lo_host_opt[c] = static_cast<int32_t>(slab_pair_lo(npairs, h->nslab, c) * 16);
+  }
+  return TAIL_OK;
+}
+
+int tail_run_taps(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
+                  int32_t n_param_cols, int32_t gbs, int32_t* out_tokens, float* out_logits_opt,
+                  float* out_topk_vals_opt, int32_t* out_topk_idx_opt, float* tap_vals, int32_t* tap_idx,
+                  int32_t* tap_count, float* tap_bound, void* stream) {
+  if (!tap_vals || !tap_idx || !tap_count || !tap_bound) return TAIL_ERR_INVALID_ARG;
+  if (!aligned(tap_vals, 4) || !aligned(tap_idx, 4) || !aligned(tap_count, 4) || !aligned(tap_bound, 4))
+    return TAIL_ERR_INVALID_ARG;
+  int rc = validate_run(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt,
+                        out_topk_vals_opt, out_topk_idx_opt);
+  if (rc || gbs == 0) return rc;
+  const bool tc = h->tc_min > 0 && gbs >= h->tc_min;
+  if (!tc && gbs > h->rows_pass) return TAIL_ERR_UNSUPPORTED;  // one mma.sync pass holds the taps
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return TAIL_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = run_impl(h, hidden, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, out_topk_vals_opt,
+                out_topk_idx_opt, s);
+  if (rc) return rc;
+  TapArgs ta = {};
+  int32_t kind = 0, nchunk = 0, cap = 0;
+  tail_tap_shape(h, gbs, &kind, &nchunk, &cap, nullptr);
+  ta.kind = kind;
+  ta.meta = h->meta;
+  ta.cand = h->cand;
+  ta.lists = h->tc_lists;
+  ta.B = gbs;
+  ta.V = h->cfg.V;
+  ta.nchunk = nchunk;
+  ta.cap = cap;
+  ta.tile_n = tc ? tc_tile_n(gbs) : 0;
+  ta.vals = tap_vals;
+  ta.idx = tap_idx;
+  ta.count = tap_count;
+  ta.bound = tap_bound;
+  cudaError_t e = launch_tap_export(ta, s);
+  if (e != cudaSuccess) return cuda_fail(e, "tail_run_taps: kernel launch");
+  return TAIL_OK;
 }
 
 int tail_run(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,

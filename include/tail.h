@@ -135,8 +135,8 @@ int tail_run(tail_t* h, const void* hidden, const float* gamma, const uint16_t* 
              float* out_logits_opt, void* stream);
 
 /*
- * tail_run plus the sorted global top-k (the analogue of the page's
- * `debug_taps`, exposing the stage that feeds the sampler):
+ * tail_run plus the sorted global top-k (the merge's output, the stage that
+ * feeds the sampler; the first stage's output is tail_run_taps'):
  *   out_topk_vals_opt [gbs, k] fp32 logits in (value desc, index asc) order, or NULL;
  *   out_topk_idx_opt  [gbs, k] int32 vocabulary ids in the same order, or NULL.
  */
@@ -144,6 +144,42 @@ int tail_run_ex(tail_t* h, const void* hidden, const float* gamma, const uint16_
                 const float* params, int32_t n_param_cols, int32_t gbs, int32_t* out_tokens,
                 float* out_logits_opt, float* out_topk_vals_opt, int32_t* out_topk_idx_opt,
                 void* stream);
+
+/*
+ * Stage-1 taps (the page's `debug_taps`: the chunked top-k's first-stage
+ * output, for defects that show on hardware only).  The vocabulary is cut
+ * into chunks -- the mma.sync lm_head kernel's slabs, or the tensor-core
+ * lm_head's column tiles -- and each (row, chunk) hands the merge a few
+ * candidates (section "Background": the chunked top-k feeds one global top-k).
+ *
+ * tail_tap_shape: for a run of gbs rows on this handle, *kind = 1 (slabs) or
+ * 2 (tiles), *n_chunks chunks a row, *cap candidate slots a chunk, and, when
+ * chunk_lo_host_opt is non-NULL, the first vocabulary id of every chunk and V
+ * after them ([n_chunks + 1] int32, host memory).
+ *
+ * tail_run_taps: tail_run_ex, then the taps of the same run (device memory):
+ *   tap_vals  [gbs, n_chunks, cap] fp32: the chunk's candidates' logits (slots
+ *             past the count hold -inf),
+ *   tap_idx   [gbs, n_chunks, cap] int32: their vocabulary ids (-1 past the count),
+ *   tap_count [gbs, n_chunks] int32: candidates handed over,
+ *   tap_bound [gbs, n_chunks] fp32: every element of the chunk that is not a
+ *             candidate has a logit <= bound.  Slabs: the candidates are every
+ *             element >= bound when they fit the chunk's slots; when they do not,
+ *             count = 0 and bound = +inf (the merge then rescans the slab if its
+ *             hidden elements could reach the top k).  Tiles: the tile's top
+ *             `cap` by (value desc, index asc); bound = the last of them, or -inf
+ *             when they are all of the tile's columns.
+ * Candidates are listed in no particular order for slabs, in (value desc, index
+ * asc) order for tiles.  One extra kernel launch copies them out of the
+ * handle's scratch after the run.  Returns TAIL_ERR_INVALID_ARG for a NULL tap
+ * pointer (any of the four) or misaligned pointers.
+ */
+int tail_tap_shape(const tail_t* h, int32_t gbs, int32_t* kind, int32_t* n_chunks, int32_t* cap,
+                   int32_t* chunk_lo_host_opt);
+int tail_run_taps(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
+                  int32_t n_param_cols, int32_t gbs, int32_t* out_tokens, float* out_logits_opt,
+                  float* out_topk_vals_opt, int32_t* out_topk_idx_opt, float* tap_vals, int32_t* tap_idx,
+                  int32_t* tap_count, float* tap_bound, void* stream);
 
 /*
  * The tail fused with its producer: the MoE combine and residual add that form
