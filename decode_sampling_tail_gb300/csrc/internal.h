@@ -111,7 +111,7 @@ __host__ __device__ inline int moe_slot_bytes_for(int B) { return moe_y_offset(B
 
 // Launchers (all enqueue on `stream`; the lm_head tail is one launch,
 // chained to the previous kernel on the stream with programmatic dependent launch when pdl).
-cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream);
+cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream, bool pdl = true);
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t stream, bool pdl);
 // per device: opt the lm_head kernels into the largest dynamic shared memory
 // the opt-in limit leaves after their static shared memory

@@ -1,8 +1,9 @@
 // tail_run_noalloc: the tail without a handle and without any device
-// allocation.  It launches the same two kernels as tail_run (rms_pack, then the
-// lm_head + global top-k + sampler), but their scratch lives in one
-// file-scope device array of fixed size instead of handle-owned cudaMalloc
-// memory.
+// allocation.  It launches the same mma.sync-path kernels as tail_run -- one
+// launch a pass in the default deferred-RMSNorm form (the lm_head kernel forms
+// the activations, then the global top-k and the sampler), two in the legacy
+// form (rms_pack first) -- but their scratch lives in one file-scope device
+// array of fixed size instead of handle-owned cudaMalloc memory.
 //
 // The array is part of this library's device image: it is created with the
 // module, zero-filled, and its address is looked up once per device (with that
@@ -83,6 +84,21 @@ int setup_device(int dev, NoallocDevice** out) {
   }
   *out = &d;
   return TAIL_OK;
+}
+
+// Launches with programmatic dependent launch while the device takes it.  A
+// launch that fails with the attribute is retried once without it; only when
+// that retry succeeds (the attribute was what the runtime refused) does the
+// device stop using it.  Any other failure is returned as it is.
+template <typename Launch>
+cudaError_t launch_with_pdl_fallback(NoallocDevice* d, Launch launch) {
+  if (!d->pdl_ok.load(std::memory_order_relaxed)) return launch(false);
+  cudaError_t e = launch(true);
+  if (e == cudaSuccess) return e;
+  cudaGetLastError();  // a refused launch leaves a (non-sticky) error behind
+  const cudaError_t e2 = launch(false);
+  if (e2 == cudaSuccess) d->pdl_ok.store(0, std::memory_order_relaxed);
+  return e2 == cudaSuccess ? e2 : e;
 }
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -221,7 +237,7 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
     ra.row_scale = reinterpret_cast<float*>(base + L.row_scale);
     const bool fused = cfg->deferred_rms && plan.logits_in_smem && plan.mt <= FUSED_MAX_MT;
     if (!fused) {
-      e = launch_rms_pack(ra, s);
+      e = launch_with_pdl_fallback(d, [&](bool pdl) { return launch_rms_pack(ra, s, pdl); });
       if (e != cudaSuccess) return cuda_fail(e, "tail_run_noalloc: kernel launch");
     }
 
@@ -270,14 +286,7 @@ extern "C" int tail_run_noalloc(const tail_config* cfg, const void* hidden, cons
     ga.sortP = plan.sortP;
     ga.timeout_ns = DEFAULT_TIMEOUT_NS;
     ga.drop_iter = -1;
-    if (d->pdl_ok.load(std::memory_order_relaxed)) {
-      e = launch_gemv(ga, s, true);
-      if (e != cudaSuccess) {  // this runtime refuses programmatic serialization: launch without the overlap
-        cudaGetLastError();
-        d->pdl_ok.store(0, std::memory_order_relaxed);
-      }
-    }
-    if (!d->pdl_ok.load(std::memory_order_relaxed)) e = launch_gemv(ga, s, false);
+    e = launch_with_pdl_fallback(d, [&](bool pdl) { return launch_gemv(ga, s, pdl); });
     if (e != cudaSuccess) return cuda_fail(e, "tail_run_noalloc: kernel launch");
   }
   if (out_status_opt) {

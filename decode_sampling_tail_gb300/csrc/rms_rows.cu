@@ -208,7 +208,7 @@ cudaError_t launch_split(const SplitArgs& a, cudaStream_t stream) {
   }
 }
 
-cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream) {
+cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.B_pad);
   cfg.blockDim = dim3(RMS_THREADS);
@@ -218,7 +218,7 @@ cudaError_t launch_rms_pack(const RmsArgs& a, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   switch (a.dtype) {
     case 0: return cudaLaunchKernelEx(&cfg, rms_pack_kernel<0>, a);
     case 1: return cudaLaunchKernelEx(&cfg, rms_pack_kernel<1>, a);

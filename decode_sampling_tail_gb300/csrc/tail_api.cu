@@ -335,6 +335,24 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   return TAIL_OK;
 }
 
+// Launches with programmatic dependent launch while the handle's runtime takes it.  A launch that
+// fails with the attribute is retried once without it; only when that retry succeeds (the attribute
+// was what the runtime refused) does the handle stop using it.  Any other failure is returned as it is.
+}  // extern "C"
+
+template <typename Launch>
+static cudaError_t launch_pdl(tail_t* h, Launch launch) {
+  if (!h->pdl_ok) return launch(false);
+  cudaError_t e = launch(true);
+  if (e == cudaSuccess) return e;
+  cudaGetLastError();  // a refused launch leaves a (non-sticky) error behind
+  const cudaError_t e2 = launch(false);
+  if (e2 == cudaSuccess) h->pdl_ok = 0;
+  return e2 == cudaSuccess ? e2 : e;
+}
+
+extern "C" {
+
 // Batches of tc_min rows or more: split -> tensor-core lm_head -> merge + sampler, one pass.
 static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
                   int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits, float* out_topk_vals,
@@ -492,7 +510,7 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
     const bool fused = c.deferred_rms && plan.logits_in_smem && plan.mt <= FUSED_MAX_MT;
     if (moe && !fused) return TAIL_ERR_UNSUPPORTED;  // not reached: moe_fusable holds
     if (!fused) {
-      e = launch_rms_pack(ra, stream);
+      e = launch_pdl(h, [&](bool pdl) { return launch_rms_pack(ra, stream, pdl); });
       if (e != cudaSuccess) break;
     }
     if (ev) cudaEventRecord(ev[1], stream);
@@ -556,14 +574,7 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
         return TAIL_ERR_CUDA;
       }
     }
-    if (h->pdl_ok) {
-      e = launch_gemv(ga, stream, true);
-      if (e != cudaSuccess) {  // this runtime refuses programmatic serialization: launch without the overlap
-        cudaGetLastError();
-        h->pdl_ok = 0;
-      }
-    }
-    if (!h->pdl_ok) e = launch_gemv(ga, stream, false);
+    e = launch_pdl(h, [&](bool pdl) { return launch_gemv(ga, stream, pdl); });
     if (e != cudaSuccess) break;
     if (ev) {
       cudaEventRecord(ev[2], stream);
@@ -633,12 +644,7 @@ int tail_run_moe(tail_t* h, const uint16_t* residual, const void* slots, int32_t
                     out_topk_vals_opt, out_topk_idx_opt, s, &m);
   // h lands in the caller's buffer, else in the handle's hidden staging (gbs_max x H bf16)
   m.h_out = out_hidden_opt ? out_hidden_opt : reinterpret_cast<uint16_t*>(h->st_hidden);
-  cudaError_t e = launch_moe_combine(m, gbs, h->cfg.H, s, h->pdl_ok != 0);
-  if (e != cudaSuccess && h->pdl_ok) {  // this runtime refuses programmatic serialization
-    cudaGetLastError();
-    h->pdl_ok = 0;
-    e = launch_moe_combine(m, gbs, h->cfg.H, s, false);
-  }
+  cudaError_t e = launch_pdl(h, [&](bool pdl) { return launch_moe_combine(m, gbs, h->cfg.H, s, pdl); });
   if (e != cudaSuccess) return cuda_fail(e, "tail_run_moe: kernel launch");
   return run_impl(h, m.h_out, gamma, w_t, params, n_param_cols, gbs, out_tokens, out_logits_opt, out_topk_vals_opt,
                   out_topk_idx_opt, s);

@@ -277,6 +277,10 @@ int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const 
  * address with cudaGetSymbolAddress, which loads the library's device image
  * if it is not loaded yet, and opts the lm_head kernels into their shared
  * memory size).  Make it once before any stream capture on that device.
+ * The set-up is kept for the life of the process: after a reset of the
+ * device's primary context (cudaDeviceReset, or the driver's own) the kept
+ * address and attributes are stale, so this entry point must not be called
+ * on that device again.
  * Overlapping calls race: all calls on one device share the one static
  * array, so two calls whose kernels may overlap (different streams, threads
  * or processes sharing a context, without ordering between them) corrupt

@@ -128,3 +128,27 @@ def test_cpu_baseline_times_the_oracle_on_all_cores_and_on_one():
     assert rec["cores"] >= 1 and "tiny" in rec["sample"]
     one = rec["single_thread"]
     assert one["cores"] == 1 and one["value"] > 0 and one["unit"] == "rows/s"
+
+
+def test_gpus_n_without_torchrun_starts_n_ranks(monkeypatch):
+    # --gpus 2 outside torchrun re-launches the bench as 2 ranks on one node (rendezvous on 127.0.0.1)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    calls = []
+    monkeypatch.setattr(bench.subprocess, "call", lambda cmd: calls.append(cmd) or 0)
+    with pytest.raises(SystemExit) as ex:
+        bench.main(["--gpus", "2", "--steps", "5", "--warmup", "3"])
+    assert ex.value.code == 0 and len(calls) == 1
+    cmd = calls[0]
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"]
+    assert "--nproc-per-node=2" in cmd and "--master-addr=127.0.0.1" in cmd
+    assert cmd[cmd.index(bench.os.path.abspath(bench.__file__)) + 1:] == ["--gpus", "2", "--steps", "5", "--warmup", "3"]
+
+
+def test_world_size_must_match_gpus(monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "4")
+    monkeypatch.setenv("RANK", "0")
+    with pytest.raises(SystemExit) as ex:
+        bench.main(["--gpus", "2"])
+    assert "WORLD_SIZE=4" in str(ex.value.code)
+    assert bench.world_mismatch(2, 2) is None and bench.world_mismatch(1, 1) is None
