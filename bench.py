@@ -89,9 +89,10 @@ def algorithmic_bytes(w, emit: bool) -> dict:
 
 # per dominant kernel: its translation unit and the headers it includes
 ROOFLINE_KERNEL_SOURCES = {
-    "lmhead_tail_kernel": ("common.cuh", "internal.h", "lmhead_tail.cu", "sampler.cuh", "select.cuh"),
-    "lmhead_tc_kernel": ("common.cuh", "internal.h", "lmhead_tc.cu", "select.cuh", "tc_common.cuh",
-                         "tc_internal.h"),
+    "lmhead_tail_kernel": ("common.cuh", "internal.h", "lmhead_tail.cu", "moe.cuh", "moe_internal.h", "sampler.cuh",
+                           "select.cuh", "tc_common.cuh"),
+    "lmhead_tc_kernel": ("common.cuh", "internal.h", "lmhead_tc.cu", "moe_internal.h", "select.cuh",
+                         "tc_common.cuh", "tc_internal.h"),
 }
 
 

@@ -13,8 +13,11 @@
 //              columns when hi and lo share a tile, else 256), requested
 //              up to NW stages ahead.
 //   warp 6     activation producer: the matching 64-wide k slice of the
-//              activation tile (hi and lo: two 128 x 64 boxes, or one box
-//              holding both when the batch fits in 64 rows), NA stages ahead.
+//              activation tile (hi and lo: two 128 x 64 tiles, or one tile
+//              holding both when the batch fits in 64 rows), NA stages ahead,
+//              by one bulk copy of the split kernel's pre-swizzled image: the
+//              copy engine then spends its per-row request rate on the
+//              weight alone.
 //   warp 1     tensor-memory owner and MMA issuer: M = 128, N, K = 16
 //              per instruction, A K-major, B (the weight, V contiguous)
 //              MN-major; two accumulators of 256 columns so the epilogue of
@@ -112,8 +115,8 @@ __device__ __forceinline__ void list_push(uint32_t (&lk)[TC_LIST], int32_t (&li)
 
 template <bool STACKED>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    lmhead_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapW,
-                     const __grid_constant__ CUtensorMap mapL, const TcArgs a) {
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapL,
+                     const TcArgs a) {
   using G = TcGeom<STACKED>;
   constexpr int NA = G::NA, NW = G::NW;
   extern __shared__ uint8_t smem_raw[];
@@ -222,7 +225,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 6) {
     // ================================================================ activation producer
     if (lane == 0) {
-      tma_prefetch_map(&mapA);
       const uint64_t pol_a = policy_evict_last();
       pdl_wait();  // the activations come from the split kernel
       int issued = 0;
@@ -238,13 +240,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tile_coords(it / a.kblocks, n, m);
         const int kb = it % a.kblocks;
         const uint32_t st = ringA_u + static_cast<uint32_t>(s) * G::A_BYTES;
+        const int64_t img = STACKED ? static_cast<int64_t>(kb) * G::A_BYTES
+                                    : (static_cast<int64_t>(m) * a.kblocks + kb) * G::A_BYTES;
         mbar_arrive_expect_tx(fullA_bar(s), G::A_BYTES);
-        if (STACKED) {
-          tma_load_2d(st, &mapA, kb * TC_KB, 0, fullA_bar(s), pol_a);
-        } else {
-          tma_load_2d(st, &mapA, kb * TC_KB, m * 2 * TC_M, fullA_bar(s), pol_a);
-          tma_load_2d(st + A_BOX_BYTES, &mapA, kb * TC_KB, m * 2 * TC_M + TC_M, fullA_bar(s), pol_a);
-        }
+        bulk_g2s(st, a.act_img + img, G::A_BYTES, fullA_bar(s), pol_a);
         issued = it + 1;
       }
       *s_issued_a = issued;
@@ -422,7 +421,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 }
 
 template <bool STACKED>
-cudaError_t launch_tc_t(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, const CUtensorMap& mapL,
+cudaError_t launch_tc_t(const TcArgs& a, const CUtensorMap& mapW, const CUtensorMap& mapL,
                         int grid, cudaStream_t stream, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -434,15 +433,15 @@ cudaError_t launch_tc_t(const TcArgs& a, const CUtensorMap& mapA, const CUtensor
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<STACKED>, mapA, mapW, mapL, a);
+  return cudaLaunchKernelEx(&cfg, lmhead_tc_kernel<STACKED>, mapW, mapL, a);
 }
 
 }  // namespace
 
-cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, const CUtensorMap& mapL,
+cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& mapW, const CUtensorMap& mapL,
                       int stacked, int grid, cudaStream_t stream, bool pdl) {
-  return stacked ? launch_tc_t<true>(a, mapA, mapW, mapL, grid, stream, pdl)
-                 : launch_tc_t<false>(a, mapA, mapW, mapL, grid, stream, pdl);
+  return stacked ? launch_tc_t<true>(a, mapW, mapL, grid, stream, pdl)
+                 : launch_tc_t<false>(a, mapW, mapL, grid, stream, pdl);
 }
 
 cudaError_t prepare_tc_gemm(int max_smem_optin) {

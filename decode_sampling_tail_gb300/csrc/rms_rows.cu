@@ -115,8 +115,10 @@ __global__ void __launch_bounds__(RMS_THREADS) rms_pack_kernel(RmsArgs a) {
 }
 
 // The same RMSNorm for the tensor-core path: the hi and lo parts of row b go
-// to two plain bf16 rows of the activation buffer (K contiguous), laid out as
-// tc_act_rows describes.  rstd is computed exactly as in rms_pack_kernel.
+// to their rows of the activation image (tc_internal.h: the tensor-core
+// kernel's shared-memory stages, 128-byte swizzle included), k-columns up to
+// the last k-block's end (zeros past H).  rstd is computed exactly as in
+// rms_pack_kernel.
 // MOE: the row is first formed by the producer step (moe.cuh) from the
 // residual and the expert slots -- h, kept in shared memory as bf16 and
 // written to the caller's buffer when one is given -- and the RMSNorm runs on
@@ -163,11 +165,8 @@ __global__ void __launch_bounds__(RMS_THREADS) rms_split_kernel(SplitArgs a) {
   __syncthreads();
   const float rstd = s_rstd;
   const float pre = a.deferred ? 1.0f : rstd;
-  const int64_t hi_row = a.stacked ? b : static_cast<int64_t>(b / 128) * 256 + (b % 128);
-  const int64_t lo_row = a.stacked ? 64 + b : hi_row + 128;
-  uint32_t* hi_dst = reinterpret_cast<uint32_t*>(a.act + hi_row * H);
-  uint32_t* lo_dst = reinterpret_cast<uint32_t*>(a.act + lo_row * H);
-  for (int h2 = 2 * threadIdx.x; h2 < H; h2 += 2 * RMS_THREADS) {
+  const int kblocks = (H + TC_KB - 1) / TC_KB;
+  for (int h2 = 2 * threadIdx.x; h2 < kblocks * TC_KB; h2 += 2 * RMS_THREADS) {
     uint32_t hi[2], lo[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -177,8 +176,8 @@ __global__ void __launch_bounds__(RMS_THREADS) rms_split_kernel(SplitArgs a) {
       hi[j] = bf16_bits(v);
       lo[j] = bf16_bits(v - __uint_as_float(hi[j] << 16));
     }
-    hi_dst[h2 >> 1] = hi[0] | (hi[1] << 16);
-    lo_dst[h2 >> 1] = lo[0] | (lo[1] << 16);
+    *reinterpret_cast<uint32_t*>(a.act_img + tc_act_image_offset(a.stacked, kblocks, b, 0, h2)) = hi[0] | (hi[1] << 16);
+    *reinterpret_cast<uint32_t*>(a.act_img + tc_act_image_offset(a.stacked, kblocks, b, 1, h2)) = lo[0] | (lo[1] << 16);
   }
   if (threadIdx.x == 0) a.row_scale[b] = a.deferred ? rstd : 1.0f;
 }

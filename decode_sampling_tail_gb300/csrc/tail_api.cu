@@ -44,7 +44,7 @@ struct tail_s {
   int32_t* topk_idx;
   int* err;
   // tensor-core path (gbs >= tc_min)
-  uint16_t* tc_act;     // [tc_act_rows(gbs_max)][H] bf16 hi/lo rows
+  uint8_t* tc_act;      // the activation image of the largest batch (tc_act_image_bytes)
   float* tc_rs;         // [gbs_max] row scales
   uint64_t* tc_lists;   // [gbs_max][tc_ntn_max][TC_LIST]
   float* tc_logits;     // [gbs_max][V] fp32 logits when the caller passes none
@@ -55,7 +55,6 @@ struct tail_s {
   const void* tc_map_l_ptr;
   int tc_map_rows;
   CUtensorMap tc_map_w;
-  CUtensorMap tc_map_a;
   CUtensorMap tc_map_l;
   // staging of tail_run_host
   void* st_hidden;
@@ -311,13 +310,14 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   e = e ? e : dalloc(&h->st_tokens, static_cast<size_t>(cfg->gbs_max), &tot);
   if (use_tc) {
     const size_t G = static_cast<size_t>(cfg->gbs_max);
-    e = e ? e : dalloc(&h->tc_act, static_cast<size_t>(tc_act_rows(cfg->gbs_max)) * cfg->H, &tot);
+    // the separate-tile layout of gbs_max rows covers the stacked one of any smaller batch
+    const size_t act_bytes = static_cast<size_t>(tc_act_image_bytes(cfg->gbs_max, cfg->H));
+    e = e ? e : dalloc(&h->tc_act, act_bytes, &tot);
     e = e ? e : dalloc(&h->tc_rs, G, &tot);
     e = e ? e : dalloc(&h->tc_lists, G * h->tc_ntn_max * TC_LIST, &tot);
     e = e ? e : dalloc(&h->tc_logits, G * cfg->V, &tot);
-    // rows of the activation buffer past a batch's rows still feed the MMA: keep them finite
-    if (e == cudaSuccess)
-      e = cudaMemset(h->tc_act, 0, static_cast<size_t>(tc_act_rows(cfg->gbs_max)) * cfg->H * sizeof(uint16_t));
+    // rows of the activation image past a batch's rows still feed the MMA: keep them finite
+    if (e == cudaSuccess) e = cudaMemset(h->tc_act, 0, act_bytes);
   }
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
   if (e == cudaSuccess && R > 0) e = cudaMemset(h->row_sync, 0, static_cast<size_t>(2 * R) * sizeof(unsigned long long));
@@ -365,8 +365,6 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   float* logits = out_logits ? out_logits : h->tc_logits;
   if (h->tc_map_w_ptr != w_t || h->tc_map_l_ptr != logits || h->tc_map_rows != gbs) {
     if (!encode_2d(&h->tc_map_w, w_t, false, static_cast<uint64_t>(c.V), static_cast<uint64_t>(c.H), 64, 64) ||
-        !encode_2d(&h->tc_map_a, h->tc_act, false, static_cast<uint64_t>(c.H),
-                   static_cast<uint64_t>(tc_act_rows(gbs)), 64, TC_M) ||
         !encode_2d(&h->tc_map_l, logits, true, static_cast<uint64_t>(c.V), static_cast<uint64_t>(gbs), 32, 32)) {
       h->tc_map_w_ptr = nullptr;
       set_last_error("cuTensorMapEncodeTiled rejected a tensor map of the tensor-core lm_head");
@@ -392,7 +390,7 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   sa.zero_pad = c.zero_interleaved_pad ? 1 : 0;
   sa.deferred = c.deferred_rms ? 1 : 0;
   sa.stacked = stacked;
-  sa.act = h->tc_act;
+  sa.act_img = h->tc_act;
   sa.row_scale = h->tc_rs;
   if (moe) {  // the split kernel forms each row from the residual and the slots itself
     sa.use_moe = 1;
@@ -403,6 +401,7 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   if (ev) cudaEventRecord(ev[1], stream);
 
   TcArgs ta;
+  ta.act_img = h->tc_act;
   ta.row_scale = h->tc_rs;
   ta.logits = logits;
   ta.ld = c.V;
@@ -415,7 +414,7 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
   ta.kblocks = (c.H + TC_KB - 1) / TC_KB;
   ta.timeout_ns = h->wait_limit_ns;
   const int ntiles = ntn * n_mb;
-  e = launch_tc(ta, h->tc_map_a, h->tc_map_w, h->tc_map_l, stacked, ntiles < h->num_sms ? ntiles : h->num_sms,
+  e = launch_tc(ta, h->tc_map_w, h->tc_map_l, stacked, ntiles < h->num_sms ? ntiles : h->num_sms,
                 stream, true);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch (tensor-core lm_head)");
   if (ev) cudaEventRecord(ev[2], stream);

@@ -23,9 +23,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// 2-D tiled store of the shared-memory box at `src` to (x, y) of `map`; parts of
-// the box outside the tensor are not written.  Completion is tracked with
-// bulk async-groups (tma_store_commit / tma_store_wait_read / tma_store_wait_all).
 // 3-D tile load (dims x fastest) with the same completion and cache hint as tma_load_2d.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar,
                                             uint64_t policy) {
@@ -36,6 +33,9 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 2-D tiled store of the shared-memory box at `src` to (x, y) of `map`; parts of
+// the box outside the tensor are not written.  Completion is tracked with
+// bulk async-groups (tma_store_commit / tma_store_wait_read / tma_store_wait_all).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(

@@ -25,14 +25,38 @@ constexpr int TC_STACK_MAX = 64; // up to this many rows, hi and lo parts share 
 constexpr int MERGE_THREADS = 256;
 constexpr int TC_MIN_ROWS = 9;   // batches of at least this many rows take the tensor-core path
 
-// Rows of the activation buffer for a batch of B rows: stacked (B <= 64) puts
-// hi parts in rows [0, 64) and lo parts in rows [64, 128); otherwise m-block mb
-// (128 batch rows) owns rows [256 mb, 256 mb + 128) for hi and the next 128 for lo.
+// The activation operand is kept in global memory as the very image of the
+// tensor-core kernel's shared-memory stages, so that one bulk copy loads a
+// stage (a 128-row tile of 64 k-columns is 16 KB: row R at byte 128 R, its
+// 16-byte chunk j at chunk position j ^ (R % 8), the 128-byte swizzle the
+// MMA descriptors read).  Stacked batches (B <= 64) hold hi parts in rows
+// [0, 64) and lo parts in rows [64, 128) of one tile per k-block; larger
+// batches hold, per m-block of 128 rows and k-block, a hi tile then a lo tile.
+// k-columns past H read as zeros.
 inline int tc_stacked(int B) { return B <= TC_STACK_MAX ? 1 : 0; }
 inline int tc_mblocks(int B) { return tc_stacked(B) ? 1 : (B + TC_M - 1) / TC_M; }
-inline int64_t tc_act_rows(int B) { return tc_stacked(B) ? TC_M : static_cast<int64_t>(tc_mblocks(B)) * 2 * TC_M; }
+inline int tc_kblocks(int H) { return (H + TC_KB - 1) / TC_KB; }
+constexpr int TC_A_TILE_BYTES = TC_M * TC_KB * 2;  // one 128-row, 64-column bf16 tile
+inline int64_t tc_act_image_bytes(int B, int H) {
+  return static_cast<int64_t>(tc_mblocks(B)) * tc_kblocks(H) * TC_A_TILE_BYTES * (tc_stacked(B) ? 1 : 2);
+}
+// Byte offset in the image of batch row b's hi (lo = 0) or lo (lo = 1) part at k-column h.
+__host__ __device__ inline int64_t tc_act_image_offset(int stacked, int kblocks, int b, int lo, int h) {
+  int R;
+  int64_t base;
+  if (stacked) {
+    R = lo ? 64 + b : b;
+    base = static_cast<int64_t>(h >> 6) * TC_A_TILE_BYTES;
+  } else {
+    R = b & (TC_M - 1);
+    base = ((static_cast<int64_t>(b / TC_M) * kblocks + (h >> 6)) * 2 + lo) * TC_A_TILE_BYTES;
+  }
+  const int c = h & 63;
+  return base + R * 128 + ((((c >> 3) ^ R) & 7) << 4) + (c & 7) * 2;
+}
 inline int tc_tile_n(int B) { return tc_stacked(B) ? TC_N_STACKED : TC_N_SEPARATE; }
 inline int tc_col_tiles(int V, int tile_n) { return (V + tile_n - 1) / tile_n; }
+
 
 struct SplitArgs {
   const void* hidden;
@@ -43,7 +67,7 @@ struct SplitArgs {
   int zero_pad;
   int deferred;
   int stacked;
-  uint16_t* act;     // [tc_act_rows(B)][H] bf16 bits
+  uint8_t* act_img;  // the activation image (tc_act_image_bytes(B, H) bytes)
   float* row_scale;  // [B]: rstd (deferred) or 1
   int use_moe = 0;   // 1: the rows are formed by the producer step from `moe` (hidden is unused)
   MoeIn moe;
@@ -52,6 +76,7 @@ struct SplitArgs {
 constexpr int SPLIT_MOE_MAX_H = 24576;
 
 struct TcArgs {
+  const uint8_t* act_img;  // the activation image written by the split kernel
   const float* row_scale;  // [B]
   float* logits;           // [B][ld] fp32: the caller's logits or scratch (always written)
   int64_t ld;
@@ -79,10 +104,9 @@ struct MergeArgs {
 };
 
 cudaError_t launch_split(const SplitArgs& a, cudaStream_t stream);
-// mapA: activation buffer [rows][H] bf16, box 64 x 128, 128-byte swizzle;
 // mapW: w_t [H][V] bf16, box 64 x 64, 128-byte swizzle;
 // mapL: logits [B][V] fp32, box 32 x 32, 128-byte swizzle.
-cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& mapA, const CUtensorMap& mapW, const CUtensorMap& mapL,
+cudaError_t launch_tc(const TcArgs& a, const CUtensorMap& mapW, const CUtensorMap& mapL,
                       int stacked, int grid, cudaStream_t stream, bool pdl);
 cudaError_t launch_merge(const MergeArgs& a, int grid, cudaStream_t stream, bool pdl);
 cudaError_t prepare_tc_gemm(int max_smem_optin);
