@@ -34,7 +34,7 @@ TC_ALL_ROWS_MAX_V = 131072
 EXPORTS = ("tail_create", "tail_run", "tail_run_ex", "tail_run_host", "tail_check", "tail_get_info",
            "tail_destroy", "tail_status_string", "tail_profile_enable", "tail_profile_read",
            "tail_set_wait_limit", "tail_debug_drop_stage", "tail_last_error", "tail_run_noalloc",
-           "tail_merge_shards", "tail_run_moe", "tail_tap_shape", "tail_run_taps")
+           "tail_merge_shards", "tail_run_moe", "tail_tap_shape", "tail_run_taps", "tail_prepare_weight")
 KERNELS = ("rms_rows", "lm_head", "merge")
 
 
@@ -95,6 +95,8 @@ def lib(path: str | None = None):
         L.tail_tap_shape.restype = ctypes.c_int
         L.tail_run_taps.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P, P, P, P, P, P]
         L.tail_run_taps.restype = ctypes.c_int
+        L.tail_prepare_weight.argtypes = [P, P, P]
+        L.tail_prepare_weight.restype = ctypes.c_int
         L.tail_run_host.argtypes = [P, P, P, P, P, i32, i32, P, P, P]
         L.tail_run_host.restype = ctypes.c_int
         L.tail_run_noalloc.argtypes = [ctypes.POINTER(tail_config), P, P, P, P, i32, i32, P, P, P, P]
@@ -306,6 +308,13 @@ class Tail:
         if rc != TAIL_OK:
             raise TailError(rc, "tail_run_ex")
         return out_tokens
+
+    def prepare_weight(self, w_t, stream=None):
+        """tail_prepare_weight: the tensor-core path's copy of w_t (None frees it)."""
+        rc = lib().tail_prepare_weight(self.h, _ptr(w_t), self._stream(stream))
+        if rc != TAIL_OK:
+            raise TailError(rc, "tail_prepare_weight")
+        self.info = tail_get_info(self.h)
 
     def run_moe(self, residual, slots, slot_w, gamma, w_t, params=None, out_tokens=None, out_logits=None,
                 out_topk_vals=None, out_topk_idx=None, out_hidden=None, n_routed=None, stream=None):

@@ -9,9 +9,10 @@
 //
 // Persistent kernel, one CTA per SM, 7 warps:
 //   warp 0     weight producer: per ring stage the 64 x N weight slice
-//              (N / 64 TMA boxes of 64 x 64, 128-byte swizzle; N = 192
-//              columns when hi and lo share a tile, else 256), requested
-//              up to NW stages ahead.
+//              (N / 64 boxes of 64 x 64, 128-byte swizzle; N = 192 columns
+//              when hi and lo share a tile, else 256), requested up to NW
+//              stages ahead: one TMA tensor-tile load per box, or, from the
+//              prepared weight (weight_pack.cu), one bulk copy per stage.
 //   warp 6     activation producer: the matching 64-wide k slice of the
 //              activation tile (hi and lo: two 128 x 64 tiles, or one tile
 //              holding both when the batch fits in 64 rows), NA stages ahead,
@@ -191,7 +192,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 0) {
     // ================================================================ weight producer
     if (lane == 0) {
-      tma_prefetch_map(&mapW);
+      const bool packed = a.w_packed != nullptr;
+      if (!packed) tma_prefetch_map(&mapW);
       const uint64_t pol_w = policy_evict_first();
       auto issue_w = [&](int it) {
         int n, m;
@@ -199,6 +201,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int kb = it % a.kblocks;
         const int s = it % NW;
         const uint32_t st = ringW_u + static_cast<uint32_t>(s) * G::W_BYTES;
+        if (packed) {
+          // the stage's boxes are adjacent blocks of the prepared weight: one bulk copy
+          const int g0 = n * G::WBOX;
+          const int nbox = min(G::WBOX, a.w_groups - g0);  // >= 1: the tile starts below V
+          const uint32_t bytes = static_cast<uint32_t>(nbox) * W_BOX_BYTES;
+          mbar_arrive_expect_tx(fullW_bar(s), bytes);
+          bulk_g2s(st, a.w_packed + (static_cast<int64_t>(kb) * a.w_groups + g0) * W_BOX_BYTES, bytes, fullW_bar(s),
+                   pol_w);
+          return;
+        }
         const int x0 = n * G::N;
         int nbox = 0;
 #pragma unroll
@@ -207,13 +219,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int j = 0; j < nbox; ++j)
           tma_load_2d(st + j * W_BOX_BYTES, &mapW, x0 + 64 * j, kb * TC_KB, fullW_bar(s), pol_w);
       };
+      // stages in flight: the whole ring unless fewer are asked for (stage it is issued once stage
+      // it - ahead has been consumed, which also frees its slot, as ahead <= NW)
+      const int ahead = (a.w_ahead > 0 && a.w_ahead < NW) ? a.w_ahead : NW;
       // the weight does not depend on the split kernel: the first stages go out before its wait
-      const int npre = min(NW, total_it);
+      const int npre = min(ahead, total_it);
       for (int it = 0; it < npre; ++it) issue_w(it);
       int issued = npre;
       for (int it = npre; it < total_it; ++it) {
         if (*s_abort) break;
-        if (!wait_or_abort(emptyW_bar(it % NW), static_cast<uint32_t>((it / NW) - 1) & 1u, a.timeout_ns, s_abort)) {
+        const int prev = it - ahead;
+        if (!wait_or_abort(emptyW_bar(prev % NW), static_cast<uint32_t>(prev / NW) & 1u, a.timeout_ns, s_abort)) {
           fail(a.err, DEV_TIMEOUT_EMPTY, s_abort);
           break;
         }

@@ -49,6 +49,9 @@ struct tail_s {
   uint64_t* tc_lists;   // [gbs_max][tc_ntn_max][TC_LIST]
   float* tc_logits;     // [gbs_max][V] fp32 logits when the caller passes none
   int tc_ntn_max;       // column tiles of the narrower tile width (the most lists a row can have)
+  uint8_t* tc_wpack;    // the prepared copy of the weight (tail_prepare_weight), or null
+  int64_t tc_wpack_bytes;
+  const void* tc_wpack_src;  // the w_t it was prepared from: runs with this pointer read the copy
   int merge_dyn;
   int merge_capc, merge_sortP, merge_smem;
   const void* tc_map_w_ptr;  // tensor maps cached for (w_t pointer, logits pointer, batch rows)
@@ -126,7 +129,7 @@ void free_all(tail_t* h) {
   void* ptrs[] = {h->apack,    h->row_scale, h->cand,      h->logit_scratch, h->meta,
                   h->row_sync, h->topk_val,  h->topk_idx,  h->err,           h->st_hidden,
                   h->st_params, h->st_tokens, h->st_logits, h->tc_act,   h->tc_rs,         h->tc_lists,
-                  h->tc_logits};
+                  h->tc_logits, h->tc_wpack};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -402,6 +405,11 @@ static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint1
 
   TcArgs ta;
   ta.act_img = h->tc_act;
+  if (h->tc_wpack != nullptr && h->tc_wpack_src == w_t) {
+    ta.w_packed = h->tc_wpack;
+    ta.w_groups = tc_weight_groups(c.V);
+    ta.w_ahead = stacked ? TC_PACKED_AHEAD_STACKED : TC_PACKED_AHEAD_SEPARATE;
+  }
   ta.row_scale = h->tc_rs;
   ta.logits = logits;
   ta.ld = c.V;
@@ -709,6 +717,40 @@ int tail_run_taps(tail_t* h, const void* hidden, const float* gamma, const uint1
   ta.bound = tap_bound;
   cudaError_t e = launch_tap_export(ta, s);
   if (e != cudaSuccess) return cuda_fail(e, "tail_run_taps: kernel launch");
+  return TAIL_OK;
+}
+
+int tail_prepare_weight(tail_t* h, const uint16_t* w_t, void* stream) {
+  if (!h) return TAIL_ERR_INVALID_ARG;
+  if (w_t && !aligned(w_t, 16)) return TAIL_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return TAIL_ERR_CUDA;
+  h->tc_wpack_src = nullptr;
+  if (!w_t) {  // release the copy
+    if (h->tc_wpack) {
+      const cudaError_t e = cudaFree(h->tc_wpack);
+      h->tc_wpack = nullptr;
+      h->scratch_bytes -= h->tc_wpack_bytes;
+      h->tc_wpack_bytes = 0;
+      if (e != cudaSuccess) return cuda_fail(e, "tail_prepare_weight: cudaFree");
+    }
+    return TAIL_OK;
+  }
+  if (h->tc_min <= 0) return TAIL_OK;  // no tensor-core path: nothing reads a prepared copy
+  if (!h->tc_wpack) {
+    const int64_t bytes = tc_packed_weight_bytes(h->cfg.H, h->cfg.V);
+    const cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&h->tc_wpack), static_cast<size_t>(bytes));
+    if (e != cudaSuccess) {
+      h->tc_wpack = nullptr;
+      return cuda_fail(e, "tail_prepare_weight: allocation of the prepared weight");
+    }
+    h->tc_wpack_bytes = bytes;
+    h->scratch_bytes += bytes;
+  }
+  const cudaError_t e = launch_weight_pack(w_t, h->cfg.H, h->cfg.V, h->tc_wpack, h->num_sms,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "tail_prepare_weight: kernel launch");
+  h->tc_wpack_src = w_t;
   return TAIL_OK;
 }
 

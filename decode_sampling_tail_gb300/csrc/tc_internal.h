@@ -57,6 +57,17 @@ __host__ __device__ inline int64_t tc_act_image_offset(int stacked, int kblocks,
 inline int tc_tile_n(int B) { return tc_stacked(B) ? TC_N_STACKED : TC_N_SEPARATE; }
 inline int tc_col_tiles(int V, int tile_n) { return (V + tile_n - 1) / tile_n; }
 
+// The prepared weight (weight_pack.cu): 8 KB blocks of 64 k-rows x 64 columns
+// in the shared-memory image of one weight box, k-block major.
+constexpr int TC_W_BLOCK_BYTES = 64 * 64 * 2;
+inline int tc_weight_groups(int V) { return (V + 63) / 64; }
+int64_t tc_packed_weight_bytes(int H, int V);
+// weight stages the tensor-core kernel keeps in flight from the prepared weight (its ring holds 6
+// stages of 24 KB when hi and lo share a tile, 3 of 32 KB otherwise)
+constexpr int TC_PACKED_AHEAD_STACKED = 5;
+constexpr int TC_PACKED_AHEAD_SEPARATE = 3;
+cudaError_t launch_weight_pack(const uint16_t* w, int H, int V, uint8_t* out, int num_sms, cudaStream_t stream);
+
 
 struct SplitArgs {
   const void* hidden;
@@ -77,6 +88,9 @@ constexpr int SPLIT_MOE_MAX_H = 24576;
 
 struct TcArgs {
   const uint8_t* act_img;  // the activation image written by the split kernel
+  const uint8_t* w_packed = nullptr;  // the prepared weight, or null: tensor-tile loads through mapW
+  int w_groups = 0;                   // 64-column groups of the prepared weight
+  int w_ahead = 0;                    // weight stages kept in flight (0: the whole ring)
   const float* row_scale;  // [B]
   float* logits;           // [B][ld] fp32: the caller's logits or scratch (always written)
   int64_t ld;

@@ -135,6 +135,28 @@ int tail_run(tail_t* h, const void* hidden, const float* gamma, const uint16_t* 
              float* out_logits_opt, void* stream);
 
 /*
+ * Weight preparation for the tensor-core path (`lm_head_weight_t` is read once
+ * a step; its layout may be chosen once, when the model is loaded).  Makes a
+ * handle-owned copy of w_t ([H, V] bf16, 16-byte aligned) in the layout of the
+ * tensor-core lm_head's shared-memory weight stages: 8 KB blocks of 64 k-rows x
+ * 64 columns with the 128-byte swizzle, k-block major, zero past H and V
+ * (tail_info.scratch_bytes grows by ceil(H/64) * ceil(V/64) * 8 KB).  The copy
+ * is written by a kernel on `stream`; later runs on other streams must be
+ * ordered after it by the caller.
+ * From then on, runs of this handle that take the tensor-core path
+ * (gbs >= tail_info.tc_min_rows) and pass the same w_t pointer read the copy:
+ * one bulk copy per weight stage instead of one tensor-tile load per 64-column
+ * box.  Results are bitwise those of the unprepared weight.  Runs with another
+ * w_t pointer, and the mma.sync path, read w_t itself.  The copy is not
+ * refreshed: after changing the contents of w_t, call this again (or stop
+ * using the copy with w_t = NULL, which frees it).
+ * Does nothing (and returns TAIL_OK) on a handle without a tensor-core path.
+ * Returns TAIL_ERR_INVALID_ARG for a misaligned w_t, TAIL_ERR_OOM when the copy
+ * cannot be allocated.
+ */
+int tail_prepare_weight(tail_t* h, const uint16_t* w_t, void* stream);
+
+/*
  * tail_run plus the sorted global top-k (the merge's output, the stage that
  * feeds the sampler; the first stage's output is tail_run_taps'):
  *   out_topk_vals_opt [gbs, k] fp32 logits in (value desc, index asc) order, or NULL;

@@ -85,7 +85,12 @@ def test_committed_traffic_is_used_only_while_the_sources_match(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel="lmhead_tail_kernel": ent["source_hash"])
     assert bench.ncu_traffic("gptoss_g8", False, ent["kernel"]) == ent["dram_bytes_per_launch"]
     assert bench.ncu_traffic("gptoss_g8", False, "some_other_kernel") is None
-    assert bench.ncu_traffic("gptoss_g8", True, ent["kernel"]) is None  # no capture with emitted logits
+    emit_ent = committed.get("gptoss_g8_emit")
+    if emit_ent is not None and emit_ent["source_hash"] == ent["source_hash"]:  # the emitting form's own capture
+        assert bench.ncu_traffic("gptoss_g8", True, ent["kernel"]) == emit_ent["dram_bytes_per_launch"]
+    else:
+        assert bench.ncu_traffic("gptoss_g8", True, ent["kernel"]) is None
+    assert bench.ncu_traffic("tiny", True, ent["kernel"]) is None  # no capture of that form
     assert bench.ncu_traffic("no_such_workload", False, ent["kernel"]) is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel="lmhead_tail_kernel": "0" * 16)
     assert bench.ncu_traffic("gptoss_g8", False, ent["kernel"]) is None
@@ -95,13 +100,16 @@ def test_committed_traffic_is_close_to_the_algorithmic_bytes():
     # a capture far above the algorithmic bytes would mean re-reads of W; below them, a wrong capture
     with open(bench.os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")) as f:
         committed = json.load(f)
-    shapes = {"gptoss_g8": (8, 2880), "padded_g64": (64, 3072), "large_g1024": (1024, 2880)}
+    shapes = {"gptoss_g8": (8, 2880), "padded_g64": (64, 3072), "adversarial_g32": (32, 2880),
+              "large_g1024": (1024, 2880)}
     for name, ent in committed.items():
-        B, H = shapes[name]
+        emit = name.endswith("_emit")
+        B, H = shapes[name[:-len("_emit")] if emit else name]
         w_bytes = 2 * H * 201088
         assert w_bytes <= ent["dram_bytes_per_launch"]
-        # the tensor-core path writes its fp32 logits to scratch for the merge's rescans
-        logits = 4 * B * 201088 if ent["kernel"] == "lmhead_tc_kernel" else 0
+        # the tensor-core path writes its fp32 logits (to scratch for the merge's rescans, when the caller
+        # takes none); the emitting form writes the caller's
+        logits = 4 * B * 201088 if emit or ent["kernel"] == "lmhead_tc_kernel" else 0
         assert ent["dram_bytes_per_launch"] <= 1.1 * (w_bytes + logits), name
 
 

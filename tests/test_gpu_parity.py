@@ -340,8 +340,8 @@ def test_tensor_core_batches_match_oracle(shape):
 @pytest.mark.parametrize("emit", [True, False], ids=["emit_on", "emit_off"])
 def test_tensor_core_saturated_tiles_scan_the_logits(V, emit):
     # columns repeated in groups of 32: every tile holding a top value holds at least 32 elements at or
-    # above the merge bound, more than its 16-entry candidate list, so the merge must rescan those tiles:
-    # in the caller's logits (emit on), or in the tiles' logits recomputed from the weight (emit off)
+    # above the merge bound, more than its 8-entry candidate list, so the merge must rescan those tiles:
+    # in the caller's logits (emit on), or in the handle's copy of them (emit off)
     w = gen.custom(24, 128, V, 64, hidden_dtype="bf16", seed=91, dup_cols=32)
     with make_tail(w) as t:
         res = tc.run_gpu(t, w, torch, emit=emit)
