@@ -24,10 +24,11 @@
 //              MN-major; two accumulators of 256 columns so the epilogue of
 //              one tile overlaps the MMAs of the next.
 //   warps 2-5  epilogue, one batch row per thread (tensor-memory lane): row
-//              scale, the fp32 logits (each warp's 32 x 32 block staged in
-//              shared memory and written by a TMA tensor store), and the
-//              tile's top TC_LIST candidates (value desc, index asc) for the
-//              merge.
+//              scale, the fp32 logits (32 x 32 blocks staged in shared
+//              memory and written by TMA tensor stores), and the tile's top
+//              TC_LIST candidates (value desc, index asc) for the merge.
+//              When hi and lo share a tile, the two warps holding a row's
+//              hi and lo parts each take half of the columns.
 // Tiles are (column tile n, m-block m) pairs taken round robin by the CTAs,
 // m varying fastest, so the CTAs that share a weight tile run it together and
 // the weight is read from HBM once.
@@ -49,7 +50,8 @@ constexpr uint32_t TC_ACC_COLS = 256;               // tensor-memory columns per
 constexpr uint32_t TC_TMEM_COLS = 2 * TC_ACC_COLS;  // two accumulators
 constexpr uint32_t W_BOX_BYTES = 64 * 64 * 2;
 constexpr uint32_t A_BOX_BYTES = 128 * 64 * 2;
-constexpr int XBUF_PITCH = 33;                      // floats per row of the stacked hi/lo exchange
+constexpr int XHALF_PITCH = 17;                     // floats per row of a half-chunk hand-over (16 + 1)
+constexpr int XHALF = 64 * XHALF_PITCH;              // floats of one direction's hand-over (64 rows)
 
 // Shared memory: the activation ring (NA stages), the weight ring (NW stages), the
 // stacked hi/lo exchange, the logits store boxes and the barriers.  The two
@@ -65,7 +67,8 @@ struct TcGeom {
   static constexpr uint32_t W_BYTES = WBOX * W_BOX_BYTES;                     // one weight stage
   static constexpr int TBUF_N = STACKED ? 1 : 2;  // 32 x 32 fp32 store boxes per epilogue warp
   static constexpr uint32_t TBUF_BYTES = 4 * TBUF_N * 4096;
-  static constexpr uint32_t XBUF_BYTES = STACKED ? (64 * XBUF_PITCH * 4 + 1023) / 1024 * 1024 : 0;
+  static constexpr uint32_t XBUF_BYTES = STACKED ? (2 * XHALF * 4 + 1023) / 1024 * 1024 : 0;
+  static_assert(!STACKED || 64 * 2 * TC_LIST * 4 <= 2 * XHALF * 4, "the list hand-over fits the exchange buffer");
   static constexpr uint32_t CTL_BYTES = 256;
   static constexpr int NA = 3;
   static constexpr int NW_FIT =
@@ -105,6 +108,22 @@ __device__ __forceinline__ void list_push(uint32_t (&lk)[TC_LIST], int32_t (&li)
   bool gt[TC_LIST];
 #pragma unroll
   for (int i = 0; i < TC_LIST; ++i) gt[i] = kc > lk[i];
+#pragma unroll
+  for (int i = TC_LIST - 1; i > 0; --i) {
+    lk[i] = gt[i - 1] ? lk[i - 1] : (gt[i] ? kc : lk[i]);
+    li[i] = gt[i - 1] ? li[i - 1] : (gt[i] ? ic : li[i]);
+  }
+  lk[0] = gt[0] ? kc : lk[0];
+  li[0] = gt[0] ? ic : li[0];
+}
+
+// list_push for an entry whose column may be below those of listed entries with the same key: the
+// order is (key desc, column asc) in full.  Keys of 0 (empty slots) are never pushed.
+__device__ __forceinline__ void list_push_ordered(uint32_t (&lk)[TC_LIST], int32_t (&li)[TC_LIST], uint32_t kc,
+                                                  int32_t ic) {
+  bool gt[TC_LIST];
+#pragma unroll
+  for (int i = 0; i < TC_LIST; ++i) gt[i] = kc != 0u && (kc > lk[i] || (kc == lk[i] && ic < li[i]));
 #pragma unroll
   for (int i = TC_LIST - 1; i > 0; --i) {
     lk[i] = gt[i - 1] ? lk[i - 1] : (gt[i] ? kc : lk[i]);
@@ -331,9 +350,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int n, m;
       tile_coords(tile_i, n, m);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * wq) << 16) + static_cast<uint32_t>(acc) * TC_ACC_COLS;
-      const bool owner = STACKED ? (wq < 2) : true;  // stacked: lanes 64..127 hold the lo parts
-      const int row = STACKED ? 32 * wq + lane : m * TC_M + 32 * wq + lane;
-      const bool valid = owner && row < a.B;
+      // stacked: warps wq and wq + 2 hold the hi and the lo parts of the same 32 batch rows
+      const int row = STACKED ? 32 * (wq & 1) + lane : m * TC_M + 32 * wq + lane;
+      const bool valid = row < a.B;
       const float rs = valid ? a.row_scale[row] : 0.f;
       uint32_t lk[TC_LIST];
       int32_t li[TC_LIST];
@@ -343,62 +362,136 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         li[i] = 0;
       }
       const int rbase = row - lane;  // first row of this warp's 32
+      if constexpr (STACKED) {
+        // Each warp of a pair forms hi + lo for one half of every 32-column chunk (the hi warp columns
+        // 0-15, the lo warp 16-31, after handing the other half over through xbuf), keeps its own
+        // list of that half, and both write their half into the pair's store box.  The lists are
+        // merged at the tile's end.
+        const bool hi_part = wq < 2;
+        const int pair = wq & 1;
+        const int xr = 32 * pair + lane;
+        float* xo = xbuf + (hi_part ? 0 : XHALF) + xr * XHALF_PITCH;        // this warp's half for its partner
+        const float* xi = xbuf + (hi_part ? XHALF : 0) + xr * XHALF_PITCH;  // the partner's half
 #pragma unroll 1
-      for (int c = 0; c < G::CHUNKS; ++c) {
-        float v[32];
-        tmem_ld32(taddr + 32u * c, v);
-        if (STACKED) {
-          if (wq >= 2) {
-            float* xr = xbuf + (32 * (wq - 2) + lane) * XBUF_PITCH;
+        for (int c = 0; c < G::CHUNKS; ++c) {
+          float v[32];
+          tmem_ld32(taddr + 32u * c, v);
+          const int col0 = n * G::N + 32 * c;
+          const bool live = col0 < a.V;  // uniform across the epilogue
+          // the pair's box this chunk reuses has been read by the store two chunks back
+          const uint32_t box = tbuf_u + static_cast<uint32_t>(pair * 2 + (store_n & 1)) * 4096u;
+          if (hi_part && lane == 0 && live) tma_store_wait_read<1>();
+          if (hi_part) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) xr[j] = v[j];
+            for (int j = 0; j < 16; ++j) xo[j] = v[16 + j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xo[j] = v[j];
           }
           named_sync(2, 128);
-          if (wq < 2) {
-            const float* xr = xbuf + (32 * wq + lane) * XBUF_PITCH;
+          float h[16];  // hi + lo of this warp's half, row-scaled
+          if (hi_part) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] += xr[j];
-          }
-          named_sync(2, 128);
-        }
-        const int col0 = n * G::N + 32 * c;
-        if (owner && col0 < a.V) {  // warp-uniform
-          const int nv = min(32, a.V - col0);  // 16 or 32: V is a multiple of 16
+            for (int j = 0; j < 16; ++j) h[j] = (v[j] + xi[j]) * rs;
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] *= rs;
-          // the logits: this warp's 32 rows x 32 columns as one 128-byte-swizzled box, stored by TMA
-          // (rows past B and columns past V are clipped by the tensor map)
-          const uint32_t box = tbuf_u + static_cast<uint32_t>(wq * G::TBUF_N + store_n % G::TBUF_N) * 4096u;
-          if (lane == 0) {  // the box this store reuses has been read by its previous store
-            if (G::TBUF_N == 2) tma_store_wait_read<1>(); else tma_store_wait_read<0>();
+            for (int j = 0; j < 16; ++j) h[j] = (xi[j] + v[16 + j]) * rs;
           }
-          __syncwarp();
+          if (live) {
+            const int qb = hi_part ? 0 : 4;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t dst = box + static_cast<uint32_t>(lane * 128 + ((q ^ (lane & 7)) << 4));
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(v[4 * q]), "f"(v[4 * q + 1]),
-                         "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
-                         : "memory");
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t dst = box + static_cast<uint32_t>(lane * 128 + (((qb + q) ^ (lane & 7)) << 4));
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(h[4 * q]), "f"(h[4 * q + 1]),
+                           "f"(h[4 * q + 2]), "f"(h[4 * q + 3])
+                           : "memory");
+            }
+            fence_proxy_async_smem();
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&mapL, col0, rbase, box, pol_l);
-            tma_store_commit();
-          }
-          ++store_n;
-          // this tile's top TC_LIST candidates of the row
+          named_sync(2, 128);  // both halves are in the box; xbuf is free for the next chunk
+          if (live) {
+            // the logits: the pair's 32 rows x 32 columns, one TMA store (rows past B and columns past V
+            // are clipped by the tensor map)
+            if (hi_part && lane == 0) {
+              tma_store_2d(&mapL, col0, rbase, box, pol_l);
+              tma_store_commit();
+            }
+            ++store_n;
+            const int cb = col0 + (hi_part ? 0 : 16);
+            const int nv = a.V - cb;  // columns of this half inside V: >= 16, or <= 0 (V is a multiple of 16)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint32_t kc = (valid && j < nv) ? float_key(v[j]) : 0u;
-            if (__any_sync(0xffffffffu, kc > lk[TC_LIST - 1])) list_push(lk, li, kc, col0 + j);
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t kc = (valid && j < nv) ? float_key(h[j]) : 0u;
+              if (__any_sync(0xffffffffu, kc > lk[TC_LIST - 1])) list_push(lk, li, kc, cb + j);
+            }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        // the lo warp's list joins the hi warp's (xbuf is free: every chunk ended with a barrier, and
+        // the next tile's first write to it follows the next tile's start barrier)
+        uint32_t* xl = reinterpret_cast<uint32_t*>(xbuf) + xr * (2 * TC_LIST);
+        if (!hi_part) {
+#pragma unroll
+          for (int i = 0; i < TC_LIST; ++i) {
+            xl[i] = lk[i];
+            xl[TC_LIST + i] = static_cast<uint32_t>(li[i]);
+          }
+        }
+        named_sync(2, 128);
+        if (hi_part) {
+#pragma unroll
+          for (int i = 0; i < TC_LIST; ++i) {
+            const uint32_t kc = xl[i];
+            if (__any_sync(0xffffffffu, kc != 0u && kc >= lk[TC_LIST - 1]))
+              list_push_ordered(lk, li, kc, static_cast<int32_t>(xl[TC_LIST + i]));
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < G::CHUNKS; ++c) {
+          float v[32];
+          tmem_ld32(taddr + 32u * c, v);
+          const int col0 = n * G::N + 32 * c;
+          if (col0 < a.V) {  // uniform across the epilogue
+            const int nv = min(32, a.V - col0);  // 16 or 32: V is a multiple of 16
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= rs;
+            // the logits: this warp's 32 rows x 32 columns as one 128-byte-swizzled box, stored by TMA
+            // (rows past B and columns past V are clipped by the tensor map)
+            const uint32_t box = tbuf_u + static_cast<uint32_t>(wq * G::TBUF_N + store_n % G::TBUF_N) * 4096u;
+            if (lane == 0) {  // the box this store reuses has been read by its previous store
+              if (G::TBUF_N == 2) tma_store_wait_read<1>(); else tma_store_wait_read<0>();
+            }
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t dst = box + static_cast<uint32_t>(lane * 128 + ((q ^ (lane & 7)) << 4));
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(v[4 * q]), "f"(v[4 * q + 1]),
+                           "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
+                           : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&mapL, col0, rbase, box, pol_l);
+              tma_store_commit();
+            }
+            ++store_n;
+            // this tile's top TC_LIST candidates of the row
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const uint32_t kc = (valid && j < nv) ? float_key(v[j]) : 0u;
+              if (__any_sync(0xffffffffu, kc > lk[TC_LIST - 1])) list_push(lk, li, kc, col0 + j);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
-      if (valid) {  // composites: key in the high word, ~column in the low word (0 for an empty slot)
+      if (valid && (!STACKED || wq < 2)) {  // composites: key in the high word, ~column in the low word (0: empty)
         uint4* dst = reinterpret_cast<uint4*>(a.lists + (static_cast<int64_t>(row) * a.ntn + n) * TC_LIST);
 #pragma unroll
         for (int i = 0; i < TC_LIST / 2; ++i) {
