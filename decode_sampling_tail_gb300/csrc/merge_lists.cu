@@ -29,6 +29,7 @@ namespace {
 
 constexpr int MERGE_HEADS_PER_LANE = 48;  // list heads one warp holds in registers: up to 1536 tiles
 constexpr int MERGE_LISTS_PB = 1;  // lists a thread takes per gather batch
+constexpr int MERGE_ONEPASS_LPT = 6;  // lists a thread takes in the one-pass gather: up to 1536 tiles
 constexpr int MERGE_SCAN_PT = 8;   // logits loads in flight per thread in the saturated-tile scan
 
 int next_pow2_host(int x) {
@@ -109,12 +110,16 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
     // then saturated and all logits are scanned)
     uint32_t x;
     if (heads_bound) {
+      // the heads into a compact array first (read 64 bytes apart they would share banks), in the
+      // candidate buffer, which the gather only fills afterwards
+      for (int j = tid; j < ntn; j += nt) keys[j] = composite_key(ls[j * TC_LIST]);
+      __syncthreads();
       if (warp == 0) {
         uint32_t hk[MERGE_HEADS_PER_LANE];
 #pragma unroll
         for (int i = 0; i < MERGE_HEADS_PER_LANE; ++i) {
           const int j = i * 32 + lane;
-          hk[i] = j < ntn ? composite_key(ls[j * TC_LIST]) : 0u;
+          hk[i] = j < ntn ? keys[j] : 0u;
         }
         const uint32_t b = warp_bound16_span_regs(hk, K);
         if (lane == 0) s_x = b;
@@ -133,7 +138,63 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_lists_kernel(const MergeA
     // top K before a batch that might not fit.  A thread reads list j's entries starting at j mod 8
     // (the lists are 64 bytes apart: in entry order the lanes would share banks).
     int ncand = 0;
-    for (int j0 = 0; j0 < ntn; j0 += nt * MERGE_LISTS_PB) {
+    // One pass when the candidates fit the buffer (the usual case: about K lists reach x, with one or
+    // two entries each): every thread counts the candidates of its lists -- none below a head under x --
+    // and one block-wide scan places them.  Otherwise (a buffer's worth of entries at or above x) the
+    // batched gather below folds the buffer to the top K between batches.
+    int cnt[MERGE_ONEPASS_LPT];
+    int tot = 0;
+#pragma unroll
+    for (int r = 0; r < MERGE_ONEPASS_LPT; ++r) {
+      const int j = tid + r * nt;
+      cnt[r] = 0;
+      if (j < ntn && composite_key(ls[j * TC_LIST]) >= x) {
+        const uint64_t* lj = ls + static_cast<int64_t>(j) * TC_LIST;
+        if (composite_key(lj[TC_LIST - 1]) >= x) {
+          sat[atomicAdd(&s_nsat, 1)] = j;
+        } else {
+          int c = 1;
+          while (composite_key(lj[c]) >= x) ++c;  // entries are in descending order; the last is below x
+          cnt[r] = c;
+        }
+      }
+      tot += cnt[r];
+    }
+    const bool onepass = ntn <= nt * MERGE_ONEPASS_LPT;
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_red[warp] = static_cast<uint32_t>(incl);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < nt / 32; ++w) {
+      const int v = static_cast<int>(s_red[w]);
+      before += w < warp ? v : 0;
+      total += v;
+    }
+    if (onepass && total <= a.capc) {
+      int pos = before + incl - tot;
+#pragma unroll
+      for (int r = 0; r < MERGE_ONEPASS_LPT; ++r) {
+        const uint64_t* lj = ls + static_cast<int64_t>(tid + r * nt) * TC_LIST;
+        for (int e = 0; e < cnt[r]; ++e, ++pos) {
+          keys[pos] = composite_key(lj[e]);
+          idx[pos] = composite_idx(lj[e]);
+        }
+      }
+      if (tid == 0) s_nc = static_cast<uint32_t>(total);
+    }
+    __syncthreads();  // s_red and the saturated lists are complete; so are the candidates
+    if (onepass && total <= a.capc) {
+      ncand = total;
+    } else {
+      if (tid == 0) s_nsat = 0;  // the batched gather marks the saturated lists again
+      __syncthreads();
+    }
+    for (int j0 = (onepass && total <= a.capc) ? ntn : 0; j0 < ntn; j0 += nt * MERGE_LISTS_PB) {
       if (ncand + nt * MERGE_LISTS_PB * TC_LIST > a.capc) ncand = fold(ncand);
       uint64_t le[MERGE_LISTS_PB][TC_LIST];
       int c[MERGE_LISTS_PB];
