@@ -117,6 +117,26 @@ __device__ __forceinline__ void list_push(uint32_t (&lk)[TC_LIST], int32_t (&li)
   li[0] = gt[0] ? ic : li[0];
 }
 
+// Pushes the chunk columns marked in `cand` (bit j: column col0 + j, value at 4-float
+// position q0 + j / 4 of this lane's 128-byte-swizzled row of the store box) in
+// increasing column order.  Only the marked ones can enter the list: every other
+// column is at or below its last entry, which only rises.  Each lane runs its own
+// candidates (fewer than the chunk's columns once the list has filled), reading
+// their values back from shared memory.
+__device__ __forceinline__ void push_candidates(uint32_t (&lk)[TC_LIST], int32_t (&li)[TC_LIST], uint32_t cand,
+                                                uint32_t box, int q0, int col0) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t row = box + static_cast<uint32_t>(lane * 128);
+  while (cand != 0u) {
+    const int j = __ffs(cand) - 1;
+    cand &= cand - 1u;
+    const uint32_t q = static_cast<uint32_t>(q0 + (j >> 2));
+    float val;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(val) : "r"(row + (((q ^ (lane & 7)) << 4) | ((j & 3) << 2))));
+    list_push(lk, li, float_key(val), col0 + j);
+  }
+}
+
 // list_push for an entry whose column may be below those of listed entries with the same key: the
 // order is (key desc, column asc) in full.  Keys of 0 (empty slots) are never pushed.
 __device__ __forceinline__ void list_push_ordered(uint32_t (&lk)[TC_LIST], int32_t (&li)[TC_LIST], uint32_t kc,
@@ -419,11 +439,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ++store_n;
             const int cb = col0 + (hi_part ? 0 : 16);
             const int nv = a.V - cb;  // columns of this half inside V: >= 16, or <= 0 (V is a multiple of 16)
+            uint32_t cand = 0u;  // this half's columns above the list's last entry before the chunk
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint32_t kc = (valid && j < nv) ? float_key(h[j]) : 0u;
-              if (__any_sync(0xffffffffu, kc > lk[TC_LIST - 1])) list_push(lk, li, kc, cb + j);
-            }
+            for (int j = 0; j < 16; ++j)
+              cand |= ((valid && j < nv) && float_key(h[j]) > lk[TC_LIST - 1]) ? (1u << j) : 0u;
+            push_candidates(lk, li, cand, box, hi_part ? 0 : 4, cb);
           }
         }
         tc_fence_before();
@@ -480,11 +500,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             ++store_n;
             // this tile's top TC_LIST candidates of the row
+            uint32_t cand = 0u;  // columns above the list's last entry before the chunk
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const uint32_t kc = (valid && j < nv) ? float_key(v[j]) : 0u;
-              if (__any_sync(0xffffffffu, kc > lk[TC_LIST - 1])) list_push(lk, li, kc, col0 + j);
-            }
+            for (int j = 0; j < 32; ++j) cand |= ((valid && j < nv) && float_key(v[j]) > lk[TC_LIST - 1]) ? (1u << j) : 0u;
+            push_candidates(lk, li, cand, box, 0, col0);
           }
         }
         tc_fence_before();
