@@ -70,6 +70,7 @@ def test_null_handle_calls(L):
     assert L.tail_run_host(None, None, None, None, None, 4, 1, None, None, None) == dst.TAIL_ERR_INVALID_ARG
     assert L.tail_check(None) == dst.TAIL_ERR_INVALID_ARG
     assert L.tail_get_info(None, None) == dst.TAIL_ERR_INVALID_ARG
+    assert L.tail_prepare_weight(None, None, None) == dst.TAIL_ERR_INVALID_ARG
     L.tail_destroy(None)
 
 

@@ -352,6 +352,26 @@ def test_tensor_core_saturated_tiles_scan_the_logits(V, emit):
     assert exact + exempt == w.B
 
 
+@pytest.mark.parametrize("B", [24, 80], ids=["shared_tiles", "separate_tiles"])
+def test_tensor_core_late_saturated_tile_keeps_its_logits(B):
+    # The last column tiles hold 32 equal columns scaled by 4: for the rows they reach, those tiles
+    # saturate late in the launch (after the other tiles' lists are in), and the merge must rescan
+    # them from the logits the lm_head kept -- the handle's copy (emit off) or the caller's (emit on),
+    # bitwise the same result, checked against the oracle.
+    w = gen.custom(B, 2048, 98304, 64, hidden_dtype="bf16", seed=95)
+    src = (w.w_t[:, 5000].astype(np.uint32) << 16).view(np.float32) * np.float32(4.0)
+    w.w_t[:, 98304 - 200:98304 - 168] = ((src.view(np.uint32) >> 16).astype(np.uint16))[:, None]
+    with make_tail(w) as t:
+        on = tc.run_gpu(t, w, torch, emit=True)
+        off = tc.run_gpu(t, w, torch, emit=False)
+    assert np.array_equal(on.topk_idx, off.topk_idx) and np.array_equal(on.tokens, off.tokens)
+    assert np.array_equal(on.topk_vals.view(np.uint32), off.topk_vals.view(np.uint32))
+    # the planted ties are among every row's top k whose scale lets them in, so the tile saturates
+    assert np.isin(np.arange(98304 - 200, 98304 - 168), on.topk_idx).any()
+    exact, exempt = full_check(w, on)
+    assert exact + exempt == w.B
+
+
 def _scale_columns(w, c0, c1, pow2):
     """Multiplies W columns [c0, c1) by 2**pow2 (exact on bf16 values)."""
     f = (w.w_t[:, c0:c1].astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** pow2)
