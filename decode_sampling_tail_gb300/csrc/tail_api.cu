@@ -63,6 +63,7 @@ struct tail_s {
   void* st_hidden;
   float* st_params;
   int32_t* st_tokens;
+  int32_t* st_tokens_mapped;  // pinned, mapped host memory [gbs_max]: the kernels write the tokens there
   float* st_logits;
   // wait bound of the kernels and the dropped-stage test hook
   uint64_t wait_limit_ns;
@@ -132,6 +133,7 @@ void free_all(tail_t* h) {
                   h->tc_logits, h->tc_wpack};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  if (h->st_tokens_mapped) cudaFreeHost(h->st_tokens_mapped);
 }
 
 // cuTensorMapEncodeTiled, reached through the runtime (the library links no driver library).
@@ -782,19 +784,45 @@ int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const 
     }
     h->scratch_bytes += static_cast<int64_t>(c.gbs_max) * c.V * 4;
   }
+  // the tokens go straight to pinned, mapped host memory (no device-to-host copy), then to the caller
+  int32_t* tok_dev = h->st_tokens;
+  if (params_host && !h->st_tokens_mapped) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&h->st_tokens_mapped), static_cast<size_t>(c.gbs_max) * 4,
+                      cudaHostAllocMapped) != cudaSuccess) {
+      h->st_tokens_mapped = nullptr;
+      cudaGetLastError();  // fall back to the device staging and a copy
+    }
+  }
+  if (params_host && h->st_tokens_mapped) {
+    void* d = nullptr;
+    if (cudaHostGetDevicePointer(&d, h->st_tokens_mapped, 0) == cudaSuccess) tok_dev = static_cast<int32_t*>(d);
+    else cudaGetLastError();
+  }
+  // pinned parameters are read by the kernels where they are; others are copied first
+  const float* par_dev = params_host ? h->st_params : nullptr;
+  bool copy_params = params_host != nullptr;
+  if (params_host) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, params_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer != nullptr && aligned(pa.devicePointer, 4)) {
+      par_dev = static_cast<const float*>(pa.devicePointer);
+      copy_params = false;
+    }
+    cudaGetLastError();
+  }
   const size_t hbytes = static_cast<size_t>(gbs) * c.H * elem_bytes(c.hidden_dtype);
   e = cudaMemcpyAsync(h->st_hidden, hidden_host, hbytes, cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess && params_host)
+  if (e == cudaSuccess && copy_params)
     e = cudaMemcpyAsync(h->st_params, params_host, static_cast<size_t>(gbs) * n_param_cols * 4,
                         cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return TAIL_ERR_CUDA;
   }
-  int rc = tail_run_ex(h, h->st_hidden, gamma, w_t, params_host ? h->st_params : nullptr, n_param_cols, gbs,
-                       h->st_tokens, out_logits_host_opt ? h->st_logits : nullptr, nullptr, nullptr, stream);
+  int rc = tail_run_ex(h, h->st_hidden, gamma, w_t, par_dev, n_param_cols, gbs, tok_dev,
+                       out_logits_host_opt ? h->st_logits : nullptr, nullptr, nullptr, stream);
   if (rc) return rc;
-  if (params_host)
+  if (params_host && tok_dev == h->st_tokens)
     e = cudaMemcpyAsync(out_tokens_host, h->st_tokens, static_cast<size_t>(gbs) * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess && out_logits_host_opt)
     e = cudaMemcpyAsync(out_logits_host_opt, h->st_logits, static_cast<size_t>(gbs) * c.V * 4,
@@ -804,6 +832,8 @@ int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const 
     cudaGetLastError();
     return TAIL_ERR_CUDA;
   }
+  if (params_host && tok_dev != h->st_tokens)
+    memcpy(out_tokens_host, h->st_tokens_mapped, static_cast<size_t>(gbs) * 4);
   return TAIL_OK;
 }
 

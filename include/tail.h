@@ -71,9 +71,10 @@ typedef struct {
 /*
  * lm_head realisations.  The mma.sync kernel streams W once for up
  * to 8 rows and fuses the top-k and the sampler; it issues one bulk copy per
- * W row per stage, so its time hardly falls below ~150 us however narrow the
- * vocabulary.  The tensor-core path (split, tcgen05 lm_head with per-tile
- * candidate lists, merge + sampler) serves any batch in one pass.
+ * W row per CTA, so a narrow vocabulary leaves it bound by the copy engine's
+ * request rate (a 256 x 4096 weight takes ~35 us a step).  The tensor-core
+ * path (split, tcgen05 lm_head with per-tile candidate lists, merge +
+ * sampler) serves any batch in one pass.
  */
 typedef enum {
   TAIL_PATH_AUTO = 0,   /* tensor cores for every batch when V <= TAIL_TC_ALL_ROWS_MAX_V,
@@ -245,12 +246,16 @@ int tail_run_moe(tail_t* h, const uint16_t* residual, const void* slots, int32_t
 
 /*
  * End-to-end form for callers holding the per-step inputs in host memory:
- * copies hidden_host [gbs, H] and params_host [gbs, n_param_cols] into
- * handle-owned device staging, runs the tail on `stream`, copies the tokens
- * (and the logits, when out_logits_host_opt is non-NULL) back to host memory
- * and synchronises the stream before returning.  gamma and w_t stay device
- * pointers (model weights are resident).  Pinned host buffers make the copies
- * asynchronous; pageable ones work too.
+ * copies hidden_host [gbs, H] into handle-owned device staging, runs the tail
+ * on `stream`, brings the tokens (and the logits, when out_logits_host_opt is
+ * non-NULL) back to host memory and synchronises the stream before returning.
+ * params_host [gbs, n_param_cols] is copied to device staging too, unless it
+ * is pinned (page-locked and mapped, as cudaHostAlloc memory is): the kernels
+ * then read it in place.  The kernels write the tokens into a handle-owned
+ * pinned, mapped buffer (made at the first call; a device buffer and a copy if
+ * that allocation fails), copied to out_tokens_host after the synchronisation.
+ * gamma and w_t stay device pointers (model weights are resident).  Pinned host
+ * buffers make the copies asynchronous; pageable ones work too.
  */
 int tail_run_host(tail_t* h, const void* hidden_host, const float* gamma, const uint16_t* w_t,
                   const float* params_host, int32_t n_param_cols, int32_t gbs,

@@ -179,6 +179,14 @@ def test_host_entry_point_matches_device_entry_point(path):
         toks = np.zeros(w.B, np.int32)
         logits = np.zeros((w.B, w.V), np.float32)
         t.run_host(w.hidden, gamma, w_t, w.params, toks, logits)
+        # pinned inputs: the parameters are read in place; the tokens come back through mapped memory
+        hid_p = torch.from_numpy(np.ascontiguousarray(w.hidden.view(np.int16))).pin_memory()
+        par_p = torch.from_numpy(np.ascontiguousarray(w.params)).pin_memory()
+        tok_p = torch.full((w.B,), -7, dtype=torch.int32).pin_memory()
+        for _ in range(2):  # the mapped staging is made by the first call, reused by the second
+            tok_p.fill_(-7)
+            t.run_host(hid_p, gamma, w_t, par_p, tok_p)
+            assert np.array_equal(tok_p.numpy(), dev.tokens)
     assert np.array_equal(toks, dev.tokens)
     assert np.array_equal(logits.view(np.uint32), dev.logits.view(np.uint32))
 
