@@ -99,58 +99,90 @@ __device__ __forceinline__ void fail(int* err, int code, volatile int* abort_fla
   *abort_flag = 1;
 }
 
-// Inserts (kc, ic) into the list (lk, li), kept in (key desc, column asc) order
-// in registers.  Columns arrive in increasing order, so a key equal to a
-// listed one goes after it (strict compares).  Every slot takes its new entry
-// from the old list in parallel (no serial bubble chain); a key at or below
-// the last one leaves the list unchanged.
-__device__ __forceinline__ void list_push(uint32_t (&lk)[TC_LIST], int32_t (&li)[TC_LIST], uint32_t kc, int32_t ic) {
-  bool gt[TC_LIST];
-#pragma unroll
-  for (int i = 0; i < TC_LIST; ++i) gt[i] = kc > lk[i];
-#pragma unroll
-  for (int i = TC_LIST - 1; i > 0; --i) {
-    lk[i] = gt[i - 1] ? lk[i - 1] : (gt[i] ? kc : lk[i]);
-    li[i] = gt[i - 1] ? li[i - 1] : (gt[i] ? ic : li[i]);
-  }
-  lk[0] = gt[0] ? kc : lk[0];
-  li[0] = gt[0] ? ic : li[0];
+// A tile's candidate list per row is kept as TC_LIST composites in registers: key
+// in the high word, ~column in the low word (0 for an empty slot), in descending
+// order -- (value desc, index asc) -- the layout the merge reads.  It is updated
+// per chunk with fixed comparator networks (no data-dependent loops).
+
+// a >= b afterwards
+__device__ __forceinline__ void cas_desc(uint64_t& a, uint64_t& b) {
+  const uint64_t x = a, y = b;
+  a = x > y ? x : y;
+  b = x > y ? y : x;
 }
 
-// Pushes the chunk columns marked in `cand` (bit j: column col0 + j, value at 4-float
-// position q0 + j / 4 of this lane's 128-byte-swizzled row of the store box) in
-// increasing column order.  Only the marked ones can enter the list: every other
-// column is at or below its last entry, which only rises.  Each lane runs its own
-// candidates (fewer than the chunk's columns once the list has filled), reading
-// their values back from shared memory.
-__device__ __forceinline__ void push_candidates(uint32_t (&lk)[TC_LIST], int32_t (&li)[TC_LIST], uint32_t cand,
-                                                uint32_t box, int q0, int col0) {
+// v[O, O + 8) into descending order (bitonic network, 24 comparators)
+template <int O, int N>
+__device__ __forceinline__ void sort8_desc(uint64_t (&v)[N]) {
+#pragma unroll
+  for (int k = 2; k <= 8; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          if ((i & k) == 0) cas_desc(v[O + i], v[O + l]);
+          else cas_desc(v[O + l], v[O + i]);
+        }
+      }
+}
+
+// t[0, 8) bitonic -> descending (half-cleaners, 12 comparators)
+__device__ __forceinline__ void bitonic_merge8_desc(uint64_t (&t)[TC_LIST]) {
+#pragma unroll
+  for (int j = 4; j > 0; j >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i ^ j) > i) cas_desc(t[i], t[i ^ j]);
+}
+
+// a = the top 8 of a and b (both descending): the element-wise maximum of a and reversed b holds
+// them as a bitonic sequence
+__device__ __forceinline__ void merge_top8(uint64_t (&a)[TC_LIST], const uint64_t (&b)[TC_LIST]) {
+#pragma unroll
+  for (int i = 0; i < TC_LIST; ++i) a[i] = a[i] > b[TC_LIST - 1 - i] ? a[i] : b[TC_LIST - 1 - i];
+  bitonic_merge8_desc(a);
+}
+
+// out = the top 8 of c[O, O + 16), descending (c is reordered)
+template <int O, int N>
+__device__ __forceinline__ void top8_of16(uint64_t (&c)[N], uint64_t (&out)[TC_LIST]) {
+  sort8_desc<O>(c);
+  sort8_desc<O + 8>(c);
+#pragma unroll
+  for (int i = 0; i < TC_LIST; ++i) out[i] = c[O + i] > c[O + 15 - i] ? c[O + i] : c[O + 15 - i];
+  bitonic_merge8_desc(out);
+}
+
+__device__ __forceinline__ uint64_t cand_composite(bool ok, float v, int col) {
+  return ok ? (static_cast<uint64_t>(float_key(v)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(col)) : 0ull;
+}
+
+// Inserts composite c into the descending list L.  Every slot takes its new entry from the old list in
+// parallel (no serial bubble chain); a composite at or below the last entry leaves L unchanged.
+__device__ __forceinline__ void list_push(uint64_t (&L)[TC_LIST], uint64_t c) {
+  bool gt[TC_LIST];
+#pragma unroll
+  for (int i = 0; i < TC_LIST; ++i) gt[i] = c > L[i];
+#pragma unroll
+  for (int i = TC_LIST - 1; i > 0; --i) L[i] = gt[i - 1] ? L[i - 1] : (gt[i] ? c : L[i]);
+  L[0] = gt[0] ? c : L[0];
+}
+
+// Pushes the chunk columns marked in `cand` (bit j: column col0 + j, its value at float j of this
+// lane's 128-byte-swizzled row of the store box), each lane its own: once the list has filled, a
+// chunk holds few columns above its last entry, and only those can enter.
+__device__ __forceinline__ void push_candidates(uint64_t (&L)[TC_LIST], uint32_t cand, uint32_t box, int col0) {
   const int lane = threadIdx.x & 31;
   const uint32_t row = box + static_cast<uint32_t>(lane * 128);
   while (cand != 0u) {
     const int j = __ffs(cand) - 1;
     cand &= cand - 1u;
-    const uint32_t q = static_cast<uint32_t>(q0 + (j >> 2));
     float val;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(val) : "r"(row + (((q ^ (lane & 7)) << 4) | ((j & 3) << 2))));
-    list_push(lk, li, float_key(val), col0 + j);
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(val) : "r"(row + ((((j >> 2) ^ (lane & 7)) << 4) | ((j & 3) << 2))));
+    list_push(L, cand_composite(true, val, col0 + j));
   }
-}
-
-// list_push for an entry whose column may be below those of listed entries with the same key: the
-// order is (key desc, column asc) in full.  Keys of 0 (empty slots) are never pushed.
-__device__ __forceinline__ void list_push_ordered(uint32_t (&lk)[TC_LIST], int32_t (&li)[TC_LIST], uint32_t kc,
-                                                  int32_t ic) {
-  bool gt[TC_LIST];
-#pragma unroll
-  for (int i = 0; i < TC_LIST; ++i) gt[i] = kc != 0u && (kc > lk[i] || (kc == lk[i] && ic < li[i]));
-#pragma unroll
-  for (int i = TC_LIST - 1; i > 0; --i) {
-    lk[i] = gt[i - 1] ? lk[i - 1] : (gt[i] ? kc : lk[i]);
-    li[i] = gt[i - 1] ? li[i - 1] : (gt[i] ? ic : li[i]);
-  }
-  lk[0] = gt[0] ? kc : lk[0];
-  li[0] = gt[0] ? ic : li[0];
 }
 
 template <bool STACKED>
@@ -374,13 +406,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int row = STACKED ? 32 * (wq & 1) + lane : m * TC_M + 32 * wq + lane;
       const bool valid = row < a.B;
       const float rs = valid ? a.row_scale[row] : 0.f;
-      uint32_t lk[TC_LIST];
-      int32_t li[TC_LIST];
+      uint64_t L[TC_LIST];  // this tile's top TC_LIST candidates of the row (composites, descending)
 #pragma unroll
-      for (int i = 0; i < TC_LIST; ++i) {
-        lk[i] = 0u;  // below every key of a finite value
-        li[i] = 0;
-      }
+      for (int i = 0; i < TC_LIST; ++i) L[i] = 0ull;
       const int rbase = row - lane;  // first row of this warp's 32
       if constexpr (STACKED) {
         // Each warp of a pair forms hi + lo for one half of every 32-column chunk (the hi warp columns
@@ -439,11 +467,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             ++store_n;
             const int cb = col0 + (hi_part ? 0 : 16);
             const int nv = a.V - cb;  // columns of this half inside V: >= 16, or <= 0 (V is a multiple of 16)
-            uint32_t cand = 0u;  // this half's columns above the list's last entry before the chunk
+            uint64_t c16[16];
+            uint64_t cmax = 0ull;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              cand |= ((valid && j < nv) && float_key(h[j]) > lk[TC_LIST - 1]) ? (1u << j) : 0u;
-            push_candidates(lk, li, cand, box, hi_part ? 0 : 4, cb);
+            for (int j = 0; j < 16; ++j) {
+              c16[j] = cand_composite(valid && j < nv, h[j], cb + j);
+              cmax = c16[j] > cmax ? c16[j] : cmax;
+            }
+            if (__any_sync(0xffffffffu, cmax > L[TC_LIST - 1])) {  // the list can change
+              uint64_t t8[TC_LIST];
+              top8_of16<0>(c16, t8);
+              merge_top8(L, t8);
+            }
           }
         }
         tc_fence_before();
@@ -451,22 +486,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) mbar_arrive(tempty_bar(acc));
         // the lo warp's list joins the hi warp's (xbuf is free: every chunk ended with a barrier, and
         // the next tile's first write to it follows the next tile's start barrier)
-        uint32_t* xl = reinterpret_cast<uint32_t*>(xbuf) + xr * (2 * TC_LIST);
+        uint64_t* xl = reinterpret_cast<uint64_t*>(xbuf) + xr * TC_LIST;
         if (!hi_part) {
 #pragma unroll
-          for (int i = 0; i < TC_LIST; ++i) {
-            xl[i] = lk[i];
-            xl[TC_LIST + i] = static_cast<uint32_t>(li[i]);
-          }
+          for (int i = 0; i < TC_LIST; ++i) xl[i] = L[i];
         }
         named_sync(2, 128);
         if (hi_part) {
+          uint64_t o[TC_LIST];
 #pragma unroll
-          for (int i = 0; i < TC_LIST; ++i) {
-            const uint32_t kc = xl[i];
-            if (__any_sync(0xffffffffu, kc != 0u && kc >= lk[TC_LIST - 1]))
-              list_push_ordered(lk, li, kc, static_cast<int32_t>(xl[TC_LIST + i]));
-          }
+          for (int i = 0; i < TC_LIST; ++i) o[i] = xl[i];
+          merge_top8(L, o);
         }
       } else {
 #pragma unroll 1
@@ -499,25 +529,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               tma_store_commit();
             }
             ++store_n;
-            // this tile's top TC_LIST candidates of the row
-            uint32_t cand = 0u;  // columns above the list's last entry before the chunk
+            // this tile's top TC_LIST candidates of the row: the first chunk fills the list through the
+            // networks; later chunks push only their columns above its last entry
+            if (c == 0) {
+              uint64_t c32[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) cand |= ((valid && j < nv) && float_key(v[j]) > lk[TC_LIST - 1]) ? (1u << j) : 0u;
-            push_candidates(lk, li, cand, box, 0, col0);
+              for (int j = 0; j < 32; ++j) c32[j] = cand_composite(valid && j < nv, v[j], col0 + j);
+              uint64_t u8[TC_LIST];
+              top8_of16<0>(c32, L);
+              top8_of16<16>(c32, u8);
+              merge_top8(L, u8);
+            } else {
+              uint32_t cand = 0u;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                cand |= cand_composite(valid && j < nv, v[j], col0 + j) > L[TC_LIST - 1] ? (1u << j) : 0u;
+              push_candidates(L, cand, box, col0);
+            }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(acc));
       }
-      if (valid && (!STACKED || wq < 2)) {  // composites: key in the high word, ~column in the low word (0: empty)
-        uint4* dst = reinterpret_cast<uint4*>(a.lists + (static_cast<int64_t>(row) * a.ntn + n) * TC_LIST);
+      if (valid && (!STACKED || wq < 2)) {
+        ulonglong2* dst = reinterpret_cast<ulonglong2*>(a.lists + (static_cast<int64_t>(row) * a.ntn + n) * TC_LIST);
 #pragma unroll
-        for (int i = 0; i < TC_LIST / 2; ++i) {
-          const uint32_t lo0 = lk[2 * i] ? 0xFFFFFFFFu - static_cast<uint32_t>(li[2 * i]) : 0u;
-          const uint32_t lo1 = lk[2 * i + 1] ? 0xFFFFFFFFu - static_cast<uint32_t>(li[2 * i + 1]) : 0u;
-          dst[i] = make_uint4(lo0, lk[2 * i], lo1, lk[2 * i + 1]);
-        }
+        for (int i = 0; i < TC_LIST / 2; ++i) dst[i] = make_ulonglong2(L[2 * i], L[2 * i + 1]);
       }
     }
     if (lane == 0) tma_store_wait_all();  // the logits are in global memory before the CTA leaves
