@@ -117,12 +117,38 @@ __global__ void __launch_bounds__(RMS_THREADS) rms_pack_kernel(RmsArgs a) {
 // The same RMSNorm for the tensor-core path: the hi and lo parts of row b go
 // to their rows of the activation image (tc_internal.h: the tensor-core
 // kernel's shared-memory stages, 128-byte swizzle included), k-columns up to
-// the last k-block's end (zeros past H).  rstd is computed exactly as in
-// rms_pack_kernel.
+// the last k-block's end (zeros past H).  A thread takes groups of 8
+// consecutive columns (one 16-byte load of 16-bit elements, two of fp32; one
+// 16-byte store each of hi and lo): Σx² runs group by group, then over the
+// warps in order, so rstd is deterministic and the same for every input type.
 // MOE: the row is first formed by the producer step (moe.cuh) from the
 // residual and the expert slots -- h, kept in shared memory as bf16 and
 // written to the caller's buffer when one is given -- and the RMSNorm runs on
 // it in the same order as on a bf16 input.
+template <int DT>
+__device__ __forceinline__ void load8_widen(const void* p, int64_t i, float (&x)[8]) {
+  if constexpr (DT == 0) {
+    const float4 u = *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
+    const float4 w = *reinterpret_cast<const float4*>(static_cast<const float*>(p) + i + 4);
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+    x[4] = w.x; x[5] = w.y; x[6] = w.z; x[7] = w.w;
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p) + i);
+    const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint16_t e0 = static_cast<uint16_t>(q[j] & 0xFFFFu), e1 = static_cast<uint16_t>(q[j] >> 16);
+      if constexpr (DT == 1) {
+        x[2 * j] = __half2float(__ushort_as_half(e0));
+        x[2 * j + 1] = __half2float(__ushort_as_half(e1));
+      } else {
+        x[2 * j] = __uint_as_float(static_cast<uint32_t>(e0) << 16);
+        x[2 * j + 1] = __uint_as_float(static_cast<uint32_t>(e1) << 16);
+      }
+    }
+  }
+}
+
 template <int DT, bool MOE>
 __global__ void __launch_bounds__(RMS_THREADS) rms_split_kernel(SplitArgs a) {
   pdl_wait();  // the activation buffer is reused across steps
@@ -131,27 +157,35 @@ __global__ void __launch_bounds__(RMS_THREADS) rms_split_kernel(SplitArgs a) {
   __shared__ float s_rstd;
   extern __shared__ uint16_t s_h[];  // MOE: the row's h
   const int b = blockIdx.x;
-  const int H = a.H;
+  const int H = a.H;  // a multiple of 16
   const int64_t row = static_cast<int64_t>(b) * H;
   const int active_end = a.zero_pad ? H : a.Hu;
-  auto elem = [&](int h) -> float {
-    if constexpr (MOE) return __uint_as_float(static_cast<uint32_t>(s_h[h]) << 16);
-    else return load_widen<DT>(a.hidden, row + h);
+  auto group = [&](int h0, float (&x)[8]) {  // columns h0 .. h0 + 7 of the row
+    if constexpr (MOE) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(static_cast<uint32_t>(s_h[h0 + j]) << 16);
+    } else {
+      load8_widen<DT>(a.hidden, row + h0, x);
+    }
   };
   float ss = 0.f;
-  if constexpr (MOE) {
-    for (int h = threadIdx.x; h < H; h += RMS_THREADS) {
-      const uint32_t hb = moe_lane_h(a.moe, b, H, h);
-      s_h[h] = static_cast<uint16_t>(hb);
-      if (a.moe.h_out) a.moe.h_out[row + h] = static_cast<uint16_t>(hb);
-      const float v = __uint_as_float(hb << 16);
-      if (h < active_end) ss = fmaf(v, v, ss);
+  for (int g = threadIdx.x; g < H / 8; g += RMS_THREADS) {
+    const int h0 = 8 * g;
+    float x[8];
+    if constexpr (MOE) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t hb = moe_lane_h(a.moe, b, H, h0 + j);
+        s_h[h0 + j] = static_cast<uint16_t>(hb);
+        if (a.moe.h_out) a.moe.h_out[row + h0 + j] = static_cast<uint16_t>(hb);
+        x[j] = __uint_as_float(hb << 16);
+      }
+    } else {
+      group(h0, x);
     }
-  } else {
-    for (int h = threadIdx.x; h < active_end; h += RMS_THREADS) {
-      const float v = load_widen<DT>(a.hidden, row + h);
-      ss = fmaf(v, v, ss);
-    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (h0 + j < active_end) ss = fmaf(x[j], x[j], ss);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -166,18 +200,30 @@ __global__ void __launch_bounds__(RMS_THREADS) rms_split_kernel(SplitArgs a) {
   const float rstd = s_rstd;
   const float pre = a.deferred ? 1.0f : rstd;
   const int kblocks = (H + TC_KB - 1) / TC_KB;
-  for (int h2 = 2 * threadIdx.x; h2 < kblocks * TC_KB; h2 += 2 * RMS_THREADS) {
-    uint32_t hi[2], lo[2];
+  for (int g = threadIdx.x; g < kblocks * (TC_KB / 8); g += RMS_THREADS) {
+    const int h0 = 8 * g;
+    float x[8];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int h = h2 + j;
-      float v = 0.f;
-      if (h < active_end) v = (elem(h) * pre) * a.gamma[h];
-      hi[j] = bf16_bits(v);
-      lo[j] = bf16_bits(v - __uint_as_float(hi[j] << 16));
+    for (int j = 0; j < 8; ++j) x[j] = 0.f;
+    if (h0 < H) group(h0, x);
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      uint32_t hb[2], lb[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int h = h0 + j + u;
+        const float v = h < active_end ? (x[j + u] * pre) * a.gamma[h] : 0.f;
+        hb[u] = bf16_bits(v);
+        lb[u] = bf16_bits(v - __uint_as_float(hb[u] << 16));
+      }
+      hi[j / 2] = hb[0] | (hb[1] << 16);
+      lo[j / 2] = lb[0] | (lb[1] << 16);
     }
-    *reinterpret_cast<uint32_t*>(a.act_img + tc_act_image_offset(a.stacked, kblocks, b, 0, h2)) = hi[0] | (hi[1] << 16);
-    *reinterpret_cast<uint32_t*>(a.act_img + tc_act_image_offset(a.stacked, kblocks, b, 1, h2)) = lo[0] | (lo[1] << 16);
+    *reinterpret_cast<uint4*>(a.act_img + tc_act_image_offset(a.stacked, kblocks, b, 0, h0)) =
+        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(a.act_img + tc_act_image_offset(a.stacked, kblocks, b, 1, h0)) =
+        make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
   if (threadIdx.x == 0) a.row_scale[b] = a.deferred ? rstd : 1.0f;
 }

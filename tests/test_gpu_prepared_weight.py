@@ -101,3 +101,33 @@ def test_prepare_weight_on_a_handle_without_tensor_core_path_is_a_no_op():
     exact, exempt = tc.check_tokens(res.tokens, res.topk_vals, res.topk_idx, *tc.oracle_rows(w, np.arange(w.B)),
                                     w.params, w.k)
     assert exact + exempt == w.B
+
+
+def test_prepared_weight_serves_the_producer_step_and_the_taps():
+    # tail_run_moe and tail_run_taps run the same tensor-core pass: with the prepared copy their
+    # outputs (the combined hidden state, the tokens, the stage-1 lists) are bitwise those of W itself
+    w = gen.custom(24, 256, 12352, 64, hidden_dtype="bf16", seed=4400)
+    hidden, gamma, w_t, p = tc.to_device(w, torch, "cuda:0")
+    g = torch.Generator().manual_seed(4401)
+    S = 4
+    slots = torch.randn(w.B, S, w.H, generator=g).to("cuda:0")
+    slot_w = torch.rand(w.B, S, generator=g).to("cuda:0")
+    resid = hidden
+
+    def run_all(t):
+        tok = torch.full((w.B,), -7, dtype=torch.int32, device="cuda:0")
+        h_out = torch.empty(w.B, w.H, dtype=torch.int16, device="cuda:0")
+        t.run_moe(resid, slots, slot_w, gamma, w_t, p, out_tokens=tok, out_hidden=h_out, n_routed=S - 2)
+        tok2 = torch.full((w.B,), -7, dtype=torch.int32, device="cuda:0")
+        taps = t.run_taps(hidden, gamma, w_t, p, out_tokens=tok2)
+        torch.cuda.synchronize()
+        t.check()
+        return [tok.cpu().numpy(), h_out.cpu().numpy(), tok2.cpu().numpy()] + [x.cpu().numpy() for x in taps]
+
+    with make_tail(w) as t:
+        assert t.info.tc_min_rows and w.B >= t.info.tc_min_rows
+        plain = run_all(t)
+        t.prepare_weight(w_t)
+        prepared = run_all(t)
+    for a_, b_ in zip(plain, prepared):
+        assert np.array_equal(a_.view(np.uint8), b_.view(np.uint8))
