@@ -142,8 +142,9 @@ int tail_run(tail_t* h, const void* hidden, const float* gamma, const uint16_t* 
  * tensor-core lm_head's shared-memory weight stages: 8 KB blocks of 64 k-rows x
  * 64 columns with the 128-byte swizzle, k-block major, zero past H and V
  * (tail_info.scratch_bytes grows by ceil(H/64) * ceil(V/64) * 8 KB).  The copy
- * is written by a kernel on `stream`; later runs on other streams must be
- * ordered after it by the caller.
+ * is written by a kernel on `stream`: runs on other streams must be ordered
+ * after it by the caller, and runs still reading an earlier copy must have
+ * finished before it is rewritten (a release with w_t = NULL synchronises).
  * From then on, runs of this handle that take the tensor-core path
  * (gbs >= tail_info.tc_min_rows) and pass the same w_t pointer read the copy:
  * one bulk copy per weight stage instead of one tensor-tile load per 64-column
