@@ -119,6 +119,20 @@ def test_producer_keeps_the_shared_sum_apart(path):
     assert np.array_equal(h_gpu, h_ref)
 
 
+@pytest.mark.parametrize("slot_dtype", ["f32", "bf16"])
+def test_producer_fused_few_slots_ragged_stage(slot_dtype):
+    # 5 slots (3 routed, 2 shared): the fused form's slot rows past S must read as zeros; H = 208 is
+    # 13 k-steps of 16, so the last stage of the activation warp holds 16 columns instead of 32
+    w = gen.custom(7, 208, 6144, 24, hidden_dtype="bf16", seed=317)
+    y, wts = _slots(w.B, w.H, slot_dtype, 318, S=5)
+    h_ref = oracle.moe_combine(w.hidden, y, wts, n_routed=3)
+    with make_tail(w, path="gemv") as t:
+        res, h_gpu = _run_moe(t, w, y, wts, n_routed=3)
+        plain = tc.run_gpu(t, dataclasses.replace(w, hidden=h_ref), torch)
+    assert np.array_equal(h_gpu, h_ref)
+    _same_tail(res, plain)
+
+
 def test_producer_step_with_many_slots():
     # 40 slots (30 routed, 10 shared) of small weights: above the fused limit, the combine kernel runs first
     w = gen.custom(4, 128, 4096, 16, hidden_dtype="bf16", seed=307)
