@@ -56,8 +56,9 @@ def parse(argv=None):
                          "S slices' candidates; the all-gather between GPUs is not part of one GPU's timing)")
     ap.add_argument("--params", default="4", choices=["4", "3", "none"],
                     help="sampling_params columns: 4 (explicit u), 3 (u = 0.5), none (no sampler)")
-    ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tensor"],
-                    help="lm_head realisation: auto (by vocabulary width), mma.sync up to 8 rows, or tensor cores")
+    ap.add_argument("--path", default="auto", choices=["auto", "gemv", "tensor", "small"],
+                    help="lm_head realisation: auto (by vocabulary width), mma.sync up to 8 rows, tensor cores, "
+                         "or the one-launch small path (small problems, up to 8 rows)")
     ap.add_argument("--moe-slots", type=int, default=0,
                     help="time tail_run_moe: the hidden state formed from the residual and this many fp32 "
                          "expert slots (the producer step) inside each step; 0 = off")
@@ -96,6 +97,8 @@ ROOFLINE_KERNEL_SOURCES = {
                            "select.cuh", "tc_common.cuh"),
     "lmhead_tc_kernel": ("common.cuh", "internal.h", "lmhead_tc.cu", "moe_internal.h", "select.cuh",
                          "tc_common.cuh", "tc_internal.h"),
+    "small_tail_kernel": ("common.cuh", "internal.h", "moe_internal.h", "sampler.cuh", "select.cuh",
+                          "small_internal.h", "small_tail.cu"),
 }
 
 
@@ -320,8 +323,9 @@ def run_vocab_shards(args, w, dev, dst, torch):
 
 
 # the other workloads of the default run's compact record: (workload, emit_logits)
-CONFIGS = [("gptoss_g8", True), ("tiny", False), ("padded_g64", False), ("adversarial_g32", False),
-           ("large_g1024", False)]
+# (workload, emit_logits, lm_head path): tiny also on the one-launch small path
+CONFIGS = [("gptoss_g8", True, "auto"), ("tiny", False, "auto"), ("tiny", False, "small"),
+           ("padded_g64", False, "auto"), ("adversarial_g32", False, "auto"), ("large_g1024", False, "auto")]
 
 
 def torchrun_cmd(argv, gpus: int, port: int):
@@ -358,8 +362,11 @@ class Runner:
         self.stream = torch.cuda.Stream(dev)
         t = self.t
         self.tc_path = t.info.tc_min_rows > 0 and w.B >= t.info.tc_min_rows
+        self.small = t.info.lmhead_path == 3
         self.prepared = False
-        if self.tc_path:  # split -> tensor-core lm_head -> merge + sampler, one pass
+        if self.small:    # one launch: activations, logits, top-k and draw
+            self.passes, self.launches_per_step, self.kernel = 1, 1, "small_tail_kernel"
+        elif self.tc_path:  # split -> tensor-core lm_head -> merge + sampler, one pass
             self.passes, self.launches_per_step, self.kernel = 1, 3, "lmhead_tc_kernel"
             if not getattr(args, "no_prepare", False):  # once, as at model load: outside every timed region
                 with torch.cuda.stream(self.stream):
@@ -601,11 +608,15 @@ def time_blocks(r, steps, blocks, dist):
     return out
 
 
-def config_record(args, name, emit, dev, local_rank, torch, dst, dist, world):
+def path_name(r) -> str:
+    return "small" if r.small else "tensor" if r.tc_path else "mma.sync"
+
+
+def config_record(args, name, emit, path, dev, local_rank, torch, dst, dist, world):
     """Compact measurement of one more workload with the run's K and W (no CPU baseline)."""
     import gen
     w = gen.make(name)
-    r = Runner(args, w, emit, dev, local_rank, torch, dst)
+    r = Runner(argparse.Namespace(**{**vars(args), "path": path}), w, emit, dev, local_rank, torch, dst)
     try:
         r.warm(args.warmup)
         ms = statistics.median(time_blocks(r, args.steps, args.blocks, dist))
@@ -614,7 +625,7 @@ def config_record(args, name, emit, dev, local_rank, torch, dst, dist, world):
         e2e = None if args.no_e2e else r.e2e(args.steps, dist, world)
         rec = {"workload": name, "emit_logits": emit, "gbs": w.B, "us_per_step": 1e3 * ms / args.steps,
                "rows_per_s": job_rows_per_s(w.B, args.steps, world, ms),
-               "lm_head_path": "tensor" if r.tc_path else "mma.sync",
+               "lm_head_path": path_name(r),
                "weight": "prepared" if r.prepared else "w_t",
                "kernel_us": {k: 1e3 * v for k, v in kus.items()},
                "roofline": {k: roof[k] for k in ("bound", "kernel", "achieved", "peak", "unit", "frac", "traffic",
@@ -692,7 +703,7 @@ def main(argv=None):
     e2e = None if args.no_e2e else r.e2e(args.steps, dist, world)
     roof = r.roofline(lm_ms)
     tc_path, flush_buf, launches_per_step = r.tc_path, r.flush_buf, r.launches_per_step
-    prepared = r.prepared
+    prepared, lm_path = r.prepared, path_name(r)
     r.close()
     del r
     torch.cuda.empty_cache()
@@ -701,7 +712,7 @@ def main(argv=None):
     configs = None
     if not args.no_configs and args.workload == "gptoss_g8" and not emit and args.moe_slots == 0 \
             and args.params == "4" and not args.legacy_rms and args.path == "auto":
-        configs = [config_record(args, n, e, dev, local_rank, torch, dst, dist, world) for n, e in CONFIGS]
+        configs = [config_record(args, n, e, p, dev, local_rank, torch, dst, dist, world) for n, e, p in CONFIGS]
 
     if rank != 0:
         if dist:
@@ -731,7 +742,7 @@ def main(argv=None):
                           f"no flush: the {2 * w.H * w.V / 1e9:.2f} GB weight is larger than L2 and streams "
                           "from HBM every step"),
                    "timed": f"{args.blocks} blocks of {args.steps} steps; the headline is the median block",
-                   "lm_head_path": "tensor" if tc_path else "mma.sync",
+                   "lm_head_path": lm_path,
                    "weight": ("the handle's prepared copy (tail_prepare_weight, made once before timing)"
                               if prepared else "w_t as given"),
                    "producer": (f"MoE combine + residual add, {args.moe_slots} fp32 slots, the last 2 shared (tail_run_moe)"

@@ -27,8 +27,9 @@ TAIL_ERR_CUDA = -3
 TAIL_ERR_OOM = -4
 TAIL_ERR_DEVICE = -5
 # tail_path: which lm_head serves which batch sizes ("gemv": mma.sync kernel up to 8 rows,
-# "tensor": tensor-core path for every batch, "auto": "tensor" for narrow vocabularies)
-PATHS = {"auto": 0, "gemv": 1, "tensor": 2}
+# "tensor": tensor-core path for every batch, "auto": "tensor" for narrow vocabularies,
+# "small": one launch for every batch of a small problem, bound by latency)
+PATHS = {"auto": 0, "gemv": 1, "tensor": 2, "small": 3}
 TC_ALL_ROWS_MAX_V = 131072
 
 EXPORTS = ("tail_create", "tail_run", "tail_run_ex", "tail_run_host", "tail_check", "tail_get_info",

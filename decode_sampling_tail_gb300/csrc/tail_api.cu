@@ -18,6 +18,7 @@
 #include "abi_common.h"
 #include "internal.h"
 #include "moe_internal.h"
+#include "small_internal.h"
 #include "taps_internal.h"
 #include "tc_internal.h"
 
@@ -59,6 +60,12 @@ struct tail_s {
   int tc_map_rows;
   CUtensorMap tc_map_w;
   CUtensorMap tc_map_l;
+  // one-launch small path (cfg.path TAIL_PATH_SMALL): every batch
+  int small;
+  int small_dyn;                 // the kernel's dynamic shared memory limit
+  float* sm_logits;              // [gbs_max][V] fp32 logits when the caller passes none
+  unsigned long long* sm_sync;   // [gbs_max] per-row arrival words, zero between launches
+  uint32_t* sm_smax;             // [gbs_max][SMALL_MAX_SLABS] the slabs' largest keys of each row
   // staging of tail_run_host
   void* st_hidden;
   float* st_params;
@@ -130,7 +137,7 @@ void free_all(tail_t* h) {
   void* ptrs[] = {h->apack,    h->row_scale, h->cand,      h->logit_scratch, h->meta,
                   h->row_sync, h->topk_val,  h->topk_idx,  h->err,           h->st_hidden,
                   h->st_params, h->st_tokens, h->st_logits, h->tc_act,   h->tc_rs,         h->tc_lists,
-                  h->tc_logits, h->tc_wpack};
+                  h->tc_logits, h->tc_wpack, h->sm_logits, h->sm_sync, h->sm_smax};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->st_tokens_mapped) cudaFreeHost(h->st_tokens_mapped);
@@ -220,7 +227,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   *out = nullptr;
   int rc = validate_config(cfg);
   if (rc) return rc;
-  if (cfg->path < TAIL_PATH_AUTO || cfg->path > TAIL_PATH_TENSOR) return TAIL_ERR_INVALID_ARG;
+  if (cfg->path < TAIL_PATH_AUTO || cfg->path > TAIL_PATH_SMALL) return TAIL_ERR_INVALID_ARG;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return TAIL_ERR_INVALID_ARG;
   DeviceGuard guard(device);
@@ -258,7 +265,19 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
       plan_merge(cfg->k, tc_col_tiles(cfg->V, TC_N_SEPARATE), h->merge_dyn, &capc2, &sortP2, &smem2) &&
       capc2 == h->merge_capc && sortP2 == h->merge_sortP;
   if (smem2 > h->merge_smem) h->merge_smem = smem2;
-  if (cfg->path == TAIL_PATH_TENSOR)
+  if (cfg->path == TAIL_PATH_SMALL) {  // one launch for every batch, when the problem fits its limits
+    cudaError_t se = prepare_small(static_cast<int>(prop.sharedMemPerBlockOptin), &h->small_dyn);
+    if (se != cudaSuccess) {
+      delete h;
+      return cuda_fail(se, "cudaFuncSetAttribute (small tail kernel)");
+    }
+    if (!plan_small(cfg->gbs_max, cfg->H, cfg->V, cfg->k, h->num_sms, h->small_dyn).ok) {
+      delete h;
+      return TAIL_ERR_UNSUPPORTED;
+    }
+    h->small = 1;
+    h->tc_min = cfg->gbs_max + 1;  // no batch reaches the tensor-core path
+  } else if (cfg->path == TAIL_PATH_TENSOR)
     h->tc_min = 1;
   else if (cfg->path == TAIL_PATH_AUTO && cfg->V <= TAIL_TC_ALL_ROWS_MAX_V && tc_ok)
     h->tc_min = 1;
@@ -271,7 +290,7 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
   }
   if (!use_tc) h->tc_min = 0;
   // smaller batches run on the mma.sync lm_head, up to TC_MIN_ROWS - 1 rows a pass
-  h->rows_pass = h->tc_min == 1 ? 0 : cfg->gbs_max < TC_MIN_ROWS - 1 ? cfg->gbs_max : TC_MIN_ROWS - 1;
+  h->rows_pass = (h->tc_min == 1 || h->small) ? 0 : cfg->gbs_max < TC_MIN_ROWS - 1 ? cfg->gbs_max : TC_MIN_ROWS - 1;
   int max_dyn = 0;
   cudaError_t pe2 = prepare_gemv(h->max_smem, &max_dyn);
   if (pe2 != cudaSuccess) {
@@ -324,6 +343,12 @@ int tail_create(const tail_config* cfg, int device, tail_t** out) {
     // rows of the activation image past a batch's rows still feed the MMA: keep them finite
     if (e == cudaSuccess) e = cudaMemset(h->tc_act, 0, act_bytes);
   }
+  if (h->small) {
+    e = e ? e : dalloc(&h->sm_logits, static_cast<size_t>(cfg->gbs_max) * cfg->V, &tot);
+    e = e ? e : dalloc(&h->sm_sync, static_cast<size_t>(cfg->gbs_max), &tot);
+    e = e ? e : dalloc(&h->sm_smax, static_cast<size_t>(cfg->gbs_max) * SMALL_MAX_SLABS, &tot);
+    if (e == cudaSuccess) e = cudaMemset(h->sm_sync, 0, static_cast<size_t>(cfg->gbs_max) * sizeof(unsigned long long));
+  }
   if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
   if (e == cudaSuccess && R > 0) e = cudaMemset(h->row_sync, 0, static_cast<size_t>(2 * R) * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(h->apack, 0, ksteps * mt_max * APACK_TILE_BYTES);
@@ -357,6 +382,57 @@ static cudaError_t launch_pdl(tail_t* h, Launch launch) {
 }
 
 extern "C" {
+
+// The small path: one launch forms the activations, the logits, the top k and the tokens of every row.
+static int run_small(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
+                     int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits, float* out_topk_vals,
+                     int32_t* out_topk_idx, cudaStream_t stream) {
+  const tail_config& c = h->cfg;
+  const SmallPlan plan = plan_small(gbs, c.H, c.V, c.k, h->num_sms, h->small_dyn);
+  if (!plan.ok) return TAIL_ERR_UNSUPPORTED;  // not reached: the plan of gbs_max rows held at create
+  cudaEvent_t* ev = (h->prof_on && h->prof_n < PROF_MAX) ? h->prof_ev + h->prof_n * PROF_EV : nullptr;
+  if (ev) {
+    ++h->prof_n;
+    cudaEventRecord(ev[0], stream);
+    cudaEventRecord(ev[1], stream);  // no RMSNorm kernel: the launch forms the activations
+  }
+  SmallArgs a;
+  a.hidden = hidden;
+  a.dtype = c.hidden_dtype;
+  a.gamma = gamma;
+  a.w = w_t;
+  a.logits = out_logits ? out_logits : h->sm_logits;
+  a.topk_val = out_topk_vals ? out_topk_vals : h->topk_val;
+  a.topk_idx = out_topk_idx ? out_topk_idx : h->topk_idx;
+  a.topk_ld = c.k;
+  a.params = params;
+  a.ncols = ncols;
+  a.tokens = params ? out_tokens : nullptr;
+  a.sync = h->sm_sync;
+  a.smax = h->sm_smax;
+  a.err = h->err;
+  a.timeout_ns = h->wait_limit_ns;
+  a.B = gbs;
+  a.H = c.H;
+  a.Hu = c.hidden_actual;
+  a.V = c.V;
+  a.K = c.k;
+  a.zero_pad = c.zero_interleaved_pad ? 1 : 0;
+  a.deferred = c.deferred_rms ? 1 : 0;
+  a.eps = c.eps;
+  a.slab_cols = plan.slab_cols;
+  a.nslab = plan.nslab;
+  a.sortP = plan.sortP;
+  a.cap = plan.cap;
+  a.smem_bytes = plan.smem_bytes;
+  const cudaError_t e = launch_pdl(h, [&](bool pdl) { return launch_small(a, stream, pdl); });
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch (small tail)");
+  if (ev) {
+    cudaEventRecord(ev[2], stream);
+    cudaEventRecord(ev[3], stream);  // the top k and the draw run inside the same launch
+  }
+  return TAIL_OK;
+}
 
 // Batches of tc_min rows or more: split -> tensor-core lm_head -> merge + sampler, one pass.
 static int run_tc(tail_t* h, const void* hidden, const float* gamma, const uint16_t* w_t, const float* params,
@@ -482,6 +558,9 @@ static int run_impl(tail_t* h, const void* hidden, const float* gamma, const uin
                     const float* params, int32_t ncols, int32_t gbs, int32_t* out_tokens, float* out_logits,
                     float* out_topk_vals, int32_t* out_topk_idx, cudaStream_t stream, const MoeIn* moe = nullptr) {
   const tail_config& c = h->cfg;
+  if (h->small)  // moe is null here: moe_fusable does not hold on the small path
+    return run_small(h, hidden, gamma, w_t, params, ncols, gbs, out_tokens, out_logits, out_topk_vals, out_topk_idx,
+                     stream);
   if (h->tc_min > 0 && gbs >= h->tc_min)
     return run_tc(h, hidden, gamma, w_t, params, ncols, gbs, out_tokens, out_logits, out_topk_vals, out_topk_idx,
                   stream, moe);
@@ -662,6 +741,7 @@ int tail_run_moe(tail_t* h, const uint16_t* residual, const void* slots, int32_t
 int tail_tap_shape(const tail_t* h, int32_t gbs, int32_t* kind, int32_t* n_chunks, int32_t* cap,
                    int32_t* chunk_lo_host_opt) {
   if (!h || !kind || !n_chunks || !cap || gbs < 1 || gbs > h->cfg.gbs_max) return TAIL_ERR_INVALID_ARG;
+  if (h->small) return TAIL_ERR_UNSUPPORTED;  // one top k over the whole row: no stage-1 chunks to tap
   const int V = h->cfg.V;
   if (h->tc_min > 0 && gbs >= h->tc_min) {
     const int tn = tc_tile_n(gbs);
@@ -851,6 +931,7 @@ int tail_check(tail_t* h) {
     cudaMemset(h->err, 0, sizeof(int));
     // a wait that ran out leaves the per-row arrival words of the interrupted run behind
     if (h->rows_pass > 0) cudaMemset(h->row_sync, 0, static_cast<size_t>(2 * h->rows_pass) * sizeof(unsigned long long));
+    if (h->small) cudaMemset(h->sm_sync, 0, static_cast<size_t>(h->cfg.gbs_max) * sizeof(unsigned long long));
     cudaDeviceSynchronize();
     return TAIL_ERR_DEVICE;
   }
@@ -924,6 +1005,11 @@ int tail_get_info(const tail_t* h, tail_info* out) {
   if (h->rows_pass > 0 && h->cfg.deferred_rms) {
     const GemvPlan p = plan_gemv(h->rows_pass, h->cfg.H, h->cfg.V, h->cfg.k, h->nslab, h->max_smem);
     if (p.logits_in_smem && p.mt <= FUSED_MAX_MT) out->kernels_per_run = 1;
+  }
+  if (h->small) {
+    out->lmhead_path = 3;
+    out->rows_per_pass = h->cfg.gbs_max;
+    out->kernels_per_run = 1;
   }
   out->scratch_bytes = h->scratch_bytes;
   out->tc_min_rows = h->tc_min;

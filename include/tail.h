@@ -74,14 +74,24 @@ typedef struct {
  * W row per CTA, so a narrow vocabulary leaves it bound by the copy engine's
  * request rate (a 256 x 4096 weight takes ~35 us a step).  The tensor-core
  * path (split, tcgen05 lm_head with per-tile candidate lists, merge +
- * sampler) serves any batch in one pass.
+ * sampler) serves any batch in one pass.  The small path is one launch of
+ * CUDA-core arithmetic for problems bound by latency: each CTA forms the
+ * activations (fp32, no bf16 rounding) and the fp32 logits of a vocabulary
+ * slab with plain loads, and CTA b then keeps row b's exact top k over all V
+ * logits and draws its token.
  */
 typedef enum {
   TAIL_PATH_AUTO = 0,   /* tensor cores for every batch when V <= TAIL_TC_ALL_ROWS_MAX_V,
                            else as TAIL_PATH_GEMV */
   TAIL_PATH_GEMV = 1,   /* mma.sync kernel for gbs <= 8, tensor cores for gbs >= 9 */
-  TAIL_PATH_TENSOR = 2  /* tensor cores for every batch (TAIL_ERR_UNSUPPORTED at create
+  TAIL_PATH_TENSOR = 2, /* tensor cores for every batch (TAIL_ERR_UNSUPPORTED at create
                            when the merge cannot be planned for k and V) */
+  TAIL_PATH_SMALL = 3   /* the one-launch small path for every batch: TAIL_ERR_UNSUPPORTED at
+                           create unless gbs_max <= 8, H <= 8192, V <= 16384 and one CTA's
+                           shared memory holds gbs_max x (H + 4096) fp32 values and a row's
+                           V keys and indices.  No stage-1 taps (tail_tap_shape and
+                           tail_run_taps return TAIL_ERR_UNSUPPORTED); tail_run_moe forms h
+                           with a kernel of its own first. */
 } tail_path;
 
 #define TAIL_TC_ALL_ROWS_MAX_V 131072
@@ -93,12 +103,13 @@ typedef struct {
   int32_t merge_groups;     /* 0: the top-k merge runs inside the lm_head launch */
   int32_t lmhead_path;      /* 1: mma.sync lm_head + top-k + sampler launch;
                                2: the same, launched with programmatic serialization (it overlaps
-                               the previous kernel on the stream until its dependency wait) */
-  int32_t rows_per_pass;    /* rows one mma.sync lm_head pass covers */
+                               the previous kernel on the stream until its dependency wait);
+                               3: the one-launch small path (TAIL_PATH_SMALL) */
+  int32_t rows_per_pass;    /* rows one mma.sync lm_head pass covers (the small path: gbs_max) */
   int32_t kernels_per_run;  /* kernel launches of one full pass on the mma.sync path: 1 when the
                                lm_head kernel forms the deferred-RMSNorm activations itself (up to
                                16 rows whose slab logits fit in shared memory), else 2 (RMSNorm
-                               kernel + lm_head) */
+                               kernel + lm_head); 1 on the small path */
   int64_t scratch_bytes;    /* device scratch owned by the handle */
   int32_t tc_min_rows;      /* runs with gbs >= this take the tensor-core path (split, tcgen05
                                lm_head with per-tile candidate lists, merge + sampler: 3 kernels,

@@ -90,7 +90,7 @@ def _same_tail(res, plain, emit=True):
 
 
 @pytest.mark.parametrize("slot_dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("path", ["gemv", "tensor"])
+@pytest.mark.parametrize("path", ["gemv", "tensor", "small"])
 def test_producer_fused_tail_matches_oracle(slot_dtype, path):
     w = gen.custom(6, 256, 8192, 32, hidden_dtype="bf16", seed=301)
     y, wts = _slots(w.B, w.H, slot_dtype, 302)
@@ -104,7 +104,7 @@ def test_producer_fused_tail_matches_oracle(slot_dtype, path):
     assert exact + exempt == w.B
 
 
-@pytest.mark.parametrize("path", ["gemv", "tensor"])
+@pytest.mark.parametrize("path", ["gemv", "tensor", "small"])
 def test_producer_keeps_the_shared_sum_apart(path):
     # planted lanes on which the two orders of the page's thread give different bits
     w = gen.custom(4, 128, 4096, 16, hidden_dtype="bf16", seed=311)

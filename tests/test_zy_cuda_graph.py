@@ -35,7 +35,7 @@ def _same(out, ref):
     assert np.array_equal(tokens, ref.tokens)
 
 
-@pytest.mark.parametrize("path", ["gemv", "tensor"])
+@pytest.mark.parametrize("path", ["gemv", "tensor", "small"])
 def test_graph_replays_match_eager_runs(path):
     dev = torch.device("cuda:0")
     w1 = gen.custom(8, 512, 16384, 64, hidden_dtype="bf16", seed=401)
