@@ -11,6 +11,7 @@ constexpr int SMALL_THREADS = 512;
 constexpr int SMALL_MAX_ROWS = 8;      // rows a launch covers: one owner CTA each
 constexpr int SMALL_MAX_H = 8192;
 constexpr int SMALL_MAX_V = 16384;     // a row's keys and indices sit in one CTA's shared memory
+static_assert(SMALL_MAX_V % SMALL_THREADS == 0, "the owner holds SMALL_MAX_V / SMALL_THREADS keys a thread");
 constexpr int SMALL_PREFETCH = 4;      // weight chunks a thread loads before the dependency wait
 constexpr int SMALL_MAX_SLABS = 160;   // CTAs a launch may have (5 slab maxima a lane of one warp)
 

@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) small_tail_kernel(const Smal
       float s = 0.f;
       if (o < nout) {
         const int b = o / ncols, col = o - b * ncols;
+#pragma unroll 8
         for (int q = r; q < G; q += T) s += part[(q * B + b) * SW + col];
       }
       for (int off = T >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
@@ -229,14 +230,24 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) small_tail_kernel(const Smal
     const int nslab = gridDim.x;
     int m = a.cap + 1;  // the gathered count; above cap: no gather yet, or one that overflowed
     if (nslab >= K) {  // the bound from the slabs' maxima, then one pass over the logits
+      // warp 0 requests the maxima first; every thread then requests its logits (positions tid, tid + nt,
+      // ...) and holds them as they arrive, while warp 0 forms the bound
+      uint32_t mk[SMALL_MAX_SLABS / 32];
       if (warp == 0) {
-        uint32_t mk[SMALL_MAX_SLABS / 32];
 #pragma unroll
         for (int i = 0; i < SMALL_MAX_SLABS / 32; ++i) {
           const int sl = i * 32 + lane;
           mk[i] = sl < nslab ? __ldcg(a.smax + row * nslab + sl) : 0u;
         }
-        const uint32_t xb = warp_bound16_regs(mk, K) & 0xffff0000u;
+      }
+      float lv[SMALL_MAX_V / SMALL_THREADS];
+#pragma unroll
+      for (int u = 0; u < SMALL_MAX_V / SMALL_THREADS; ++u) {
+        const int j = tid + u * nt;
+        lv[u] = j < V ? __ldcg(lg + j) : 0.f;
+      }
+      if (warp == 0) {
+        const uint32_t xb = warp_bound16_regs(mk, K);
         if (lane == 0) {
           s_misc[0] = 0u;
           s_misc[1] = xb;
@@ -244,9 +255,11 @@ __global__ void __launch_bounds__(SMALL_THREADS, 1) small_tail_kernel(const Smal
       }
       __syncthreads();
       const uint32_t xb = s_misc[1];
-      for (int j = tid; j < V; j += nt) {
-        const uint32_t kv = float_key(__ldcg(lg + j));
-        if (kv >= xb) {
+#pragma unroll
+      for (int u = 0; u < SMALL_MAX_V / SMALL_THREADS; ++u) {
+        const int j = tid + u * nt;
+        const uint32_t kv = float_key(lv[u]);
+        if (j < V && kv >= xb) {
           const unsigned pos = atomicAdd(&s_misc[0], 1u);
           if (pos < static_cast<unsigned>(a.cap)) comp[pos] = composite(kv, j);
         }
