@@ -215,3 +215,73 @@ def test_narrow_slabs_and_k_above_the_slab_width(V, nslab, K):
         cand, _ = _slab_candidates(rows[r], K, nslab, True)
         order = cand[np.lexsort((cand, -L[r, cand]))][:K]
         assert np.array_equal(order, want[r])
+
+
+# ------------------------------------------------------------------ the one-launch small path
+#
+# Each CTA owns slab_cols columns (the smallest multiple of 8 that covers V with at most one CTA per
+# SM) and publishes, per row, its largest key.  The row's owner takes a lower bound of the K-th
+# largest key: with at least K slabs, the largest 16-bit prefix (low bits zero) that K slab maxima
+# reach -- the maxima are distinct elements, so K elements reach it too; else the largest 16-bit
+# prefix that K of the row's keys reach.  Every key at or above the bound is gathered; when more
+# than the gather buffer holds (max(1024, 2K), a multiple of 32) reach the slab bound, the row
+# bound is tried, and past that the exact selection over the whole row runs.
+
+def _bound16(keys, K):
+    keys = np.asarray(keys, np.uint64)
+    t = 0
+    for bit in range(31, 15, -1):
+        c = t | (1 << bit)
+        if int(np.count_nonzero(keys >= c)) >= K:
+            t = c
+    return t
+
+
+def _small_candidates(row, K, num_sms=152):
+    V = row.size
+    key = _keys(row)
+    per = -(-(V // 8) // num_sms)
+    sw = 8 * per
+    nslab = -(-V // sw)
+    cap = max(1024, 2 * K)
+    cap = max((cap + 31) & ~31, 1 << (K - 1).bit_length())
+    if nslab >= K:
+        maxima = [key[c * sw:min(V, (c + 1) * sw)].max() for c in range(nslab)]
+        sel = np.nonzero(key >= _bound16(maxima, K))[0]
+        if sel.size <= cap:
+            return sel, "slab_bound"
+    sel = np.nonzero(key >= _bound16(key, K))[0]
+    if sel.size <= cap:
+        return sel, "row_bound"
+    return np.arange(V), "whole_row"
+
+
+def _small_rows(kind, V, rng):
+    r = rng.standard_normal((3, V)).astype(np.float32)
+    if kind == "clustered":  # every top element inside one slab: the slab maxima bound is low
+        r[:, 700:740] += 20.0
+    elif kind == "tied":  # columns repeated 8 times: a slab's maximum ties with its neighbours
+        r = np.repeat(r[:, : V // 8], 8, axis=1)
+    elif kind == "band":  # every value within a narrow band: most keys share their top 16 bits
+        r = (1.0 + r * 1e-3).astype(np.float32)
+    elif kind == "constant":
+        r = np.full((2, V), 0.75, np.float32)
+    return r
+
+
+@pytest.mark.parametrize("kind", ["random", "clustered", "tied", "band", "constant"])
+@pytest.mark.parametrize("V,K", [(4096, 16), (2000, 200), (16384, 1024), (16, 16), (4080, 40)])
+def test_small_path_gather_holds_the_exact_top_k(kind, V, K):
+    rng = np.random.default_rng(31)
+    rows = _small_rows(kind, V, rng)
+    L = rows.astype(np.float64)
+    _, want = oracle.topk(L, K)
+    for r in range(rows.shape[0]):
+        cand, branch = _small_candidates(rows[r], K)
+        assert set(want[r].tolist()) <= set(cand.tolist()), branch
+        order = cand[np.lexsort((cand, -L[r, cand]))][:K]
+        assert np.array_equal(order, want[r]), branch
+        if kind == "random" and (V, K) == (4096, 16):  # the tiny shape: the slab bound, a few dozen keys
+            assert branch == "slab_bound" and cand.size < 4 * K
+        if kind == "constant" and V > 1024:
+            assert branch == "whole_row"
