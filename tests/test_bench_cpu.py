@@ -100,16 +100,16 @@ def test_committed_traffic_is_close_to_the_algorithmic_bytes():
     # a capture far above the algorithmic bytes would mean re-reads of W; below them, a wrong capture
     with open(bench.os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")) as f:
         committed = json.load(f)
-    shapes = {"gptoss_g8": (8, 2880), "padded_g64": (64, 3072), "adversarial_g32": (32, 2880),
-              "large_g1024": (1024, 2880)}
+    shapes = {"gptoss_g8": (8, 2880, 201088), "padded_g64": (64, 3072, 201088),
+              "adversarial_g32": (32, 2880, 201088), "large_g1024": (1024, 2880, 201088), "tiny": (1, 256, 4096)}
     for name, ent in committed.items():
         emit = name.endswith("_emit")
-        B, H = shapes[name[:-len("_emit")] if emit else name]
-        w_bytes = 2 * H * 201088
+        B, H, V = shapes[name[:-len("_emit")] if emit else name]
+        w_bytes = 2 * H * V
         assert w_bytes <= ent["dram_bytes_per_launch"]
         # the tensor-core path writes its fp32 logits (to scratch for the merge's rescans, when the caller
         # takes none); the emitting form writes the caller's
-        logits = 4 * B * 201088 if emit or ent["kernel"] == "lmhead_tc_kernel" else 0
+        logits = 4 * B * V if emit or ent["kernel"] == "lmhead_tc_kernel" else 0
         assert ent["dram_bytes_per_launch"] <= 1.1 * (w_bytes + logits), name
 
 
