@@ -160,3 +160,14 @@ def test_world_size_must_match_gpus(monkeypatch):
         bench.main(["--gpus", "2"])
     assert "WORLD_SIZE=4" in str(ex.value.code)
     assert bench.world_mismatch(2, 2) is None and bench.world_mismatch(1, 1) is None
+
+
+def test_config_records_cover_the_workloads_and_the_small_path():
+    names = {n for n, _, _ in bench.CONFIGS}
+    assert {"gptoss_g8", "tiny", "padded_g64", "adversarial_g32", "large_g1024"} <= names
+    assert ("tiny", False, "small") in bench.CONFIGS  # tiny also on the one-launch small path
+    assert all(p in ("auto", "gemv", "tensor", "small") for _, _, p in bench.CONFIGS)
+    fake = types.SimpleNamespace
+    assert bench.path_name(fake(small=True, tc_path=False)) == "small"
+    assert bench.path_name(fake(small=False, tc_path=True)) == "tensor"
+    assert bench.path_name(fake(small=False, tc_path=False)) == "mma.sync"
