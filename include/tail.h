@@ -25,6 +25,12 @@
  *     happens except in tail_run_host, tail_check and tail_destroy.
  *   - One run per handle at a time: concurrent runs on one handle share its
  *     scratch and race.
+ *   - The weights are read from the start of a launch, before its dependency
+ *     wait on the previous kernel of the stream (programmatic dependent
+ *     launch): w_t on every path, gamma too on the small path.  A kernel that
+ *     writes them must be ordered before the run by more than stream order
+ *     (an event, or a synchronisation); the hidden rows, the parameters and
+ *     the outputs follow stream order.
  *   - Every call returns TAIL_OK (0) or a negative tail_status.  Nothing
  *     aborts, traps or prints.
  */
